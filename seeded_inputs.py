@@ -1,0 +1,88 @@
+"""Seeded synthetic inputs shared by the tests, the benchmark and the oracle.
+
+This module only draws random numbers and casts them; it holds none of the
+attention arithmetic, so both the CUDA path and the CPU oracle may use it.
+
+Recipe: every tensor is drawn on the CPU as float32 from its own
+``torch.Generator`` (Q from ``seed``, K from ``seed + 1``, V from ``seed + 2``,
+dO from ``seed + 3``), multiplied by its standard deviation, then rounded to
+the compute dtype.  The oracle upcasts exactly these rounded values to fp64,
+so both sides see bit-identical inputs.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+
+import torch
+
+DTYPES = {"fp16": torch.float16, "bf16": torch.bfloat16}
+
+
+def randn(shape, seed: int, dtype: torch.dtype, std: float = 1.0) -> torch.Tensor:
+    """i.i.d. N(0, std^2) on the CPU, drawn in fp32 and rounded to ``dtype``."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    x = torch.randn(*shape, generator=g, dtype=torch.float32)
+    if std != 1.0:
+        x.mul_(std)
+    return x.to(dtype)
+
+
+@dataclass(frozen=True)
+class Workload:
+    """One attention problem: shapes [B, H, S, D], dtype, mask and input law."""
+
+    name: str
+    B: int
+    H: int
+    S: int
+    D: int
+    dtype: str = "fp16"
+    causal: bool = False
+    qk_std: float = 1.0
+    backward: bool = False
+    seed: int = 0
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.D)
+
+    @property
+    def torch_dtype(self) -> torch.dtype:
+        return DTYPES[self.dtype]
+
+    def describe(self) -> str:
+        mask = "causal" if self.causal else "non-causal"
+        return f"B{self.B} H{self.H} S{self.S} D{self.D} {self.dtype} {mask}"
+
+
+def make_inputs(w: Workload, with_dout: bool | None = None) -> dict:
+    """CPU tensors q, k, v (and do) for workload ``w`` per the module recipe."""
+    shape = (w.B, w.H, w.S, w.D)
+    dt = w.torch_dtype
+    out = {
+        "q": randn(shape, w.seed, dt, w.qk_std),
+        "k": randn(shape, w.seed + 1, dt, w.qk_std),
+        "v": randn(shape, w.seed + 2, dt),
+    }
+    if with_dout if with_dout is not None else w.backward:
+        out["do"] = randn(shape, w.seed + 3, dt)
+    return out
+
+
+# The five workloads the library is measured and checked on.
+CONFIGS = {
+    "c1": Workload("c1_noncausal_fwd_B1H1S256D64_fp16", 1, 1, 256, 64, "fp16", False),
+    "c2": Workload("c2_causal_fwd_B4H16S4096D64_fp16", 4, 16, 4096, 64, "fp16", True),
+    "c4": Workload("c4_noncausal_fwdbwd_B2H32S8192D128_bf16", 2, 32, 8192, 128, "bf16", False,
+                   qk_std=math.sqrt(2.0), backward=True),
+    "c5": Workload("c5_causal_fwd_B1H8S32768D128_fp16", 1, 8, 32768, 128, "fp16", True),
+}
+# Config 3: causal fwd+bwd, batch 8 with no head dimension (H = 1), bf16.
+C3_D = (16, 32, 64, 128)
+C3_S = (256, 1024, 4096, 8192, 16384)
+for _d in C3_D:
+    for _s in C3_S:
+        CONFIGS[f"c3_d{_d}_s{_s}"] = Workload(
+            f"c3_causal_fwdbwd_B8H1S{_s}D{_d}_bf16", 8, 1, _s, _d, "bf16", True, backward=True)
