@@ -1,0 +1,407 @@
+"""Benchmark: exact attention forward + backward on one GB300 per process.
+
+One step = the whole hot path on one batch: fa_fwd (O, L) then fa_bwd
+(Delta, dK/dV, dQ) on the causal B4 H16 S4096 D64 fp16 workload, inputs
+resident in HBM.  Prints ONE JSON line (rank 0):
+
+  value     whole-job TFLOP/s over the timed steps, counting 4*B*H*S^2*D / 2
+            (causal) for the forward and 2.5x that for the backward;
+  e2e       the same metric through the C ABI with host buffers: every step
+            copies q, k, v, dO from pinned host memory and O, L, dQ, dK, dV back;
+  roofline  the dominant kernel's algorithmic FLOPs (or bytes) per launch over
+            its CUDA-event duration, against the measured peak;
+  cpu_baseline  the fp64 CPU oracle on a bounded sample (rank 0, N = 1).
+
+`--impl reference` times the CPU oracle (the reference arm of this build) on
+the same workload, one (b, h) head per step.
+
+Multi-GPU (torchrun): every rank runs the same workload on its own GPU with no
+data exchange (weak scaling); value = all ranks' FLOPs / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd/bwd TFLOPS and % of GB300 FP16 tensor peak (B4 H16 S4096 D64 causal)"
+WORKLOAD = "c2"
+FLUSH_BYTES = 256 << 20  # > 129 MB L2
+KERNEL_SOURCES = ["exact_attention_18_gb300/csrc/fa_fwd.cu", "exact_attention_18_gb300/csrc/fa_bwd.cu",
+                  "exact_attention_18_gb300/csrc/fa_kernel_common.cuh", "exact_attention_18_gb300/csrc/sm103_ptx.cuh"]
+
+
+def conv_flops(w):
+    """FLOP convention: forward 4*B*H*S^2*D (halved when causal); backward 2.5x forward."""
+    f = 4.0 * w.B * w.H * w.S * w.S * w.D
+    if w.causal:
+        f /= 2
+    return f, 2.5 * f
+
+
+def kernel_work(w):
+    """Algorithmic work per launch of each kernel (FLOPs of its tensor-core GEMMs, or HBM bytes)."""
+    units = w.B * w.H * w.S * w.S * w.D / (2.0 if w.causal else 1.0)
+    rows = w.B * w.H * w.S
+    return {
+        "fa_fwd_kernel": ("tensor", 4.0 * units),            # S = QK^T, O += PV
+        "fa_bwd_preprocess_kernel": ("hbm", rows * w.D * 2 * 2 + rows * 4),  # read O, dO; write Delta
+        "fa_bwd_dkdv_kernel": ("tensor", 8.0 * units),       # S^T, dP^T, dV, dK
+        "fa_bwd_dq_kernel": ("tensor", 6.0 * units),         # S, dP, dQ
+    }
+
+
+def sources_digest():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "tensor_tflops": d["bf16_tflops"],
+                "tensor_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "tensor_tflops": 1900.0, "tensor_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def load_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it matches the current kernels."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return {}
+    with open(path) as f:
+        d = json.load(f)
+    if d.get("sources_digest") != sources_digest():
+        return {}
+    return d.get("bytes_per_launch", {})
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling every 200 ms while the benchmark runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.samples = []
+        self.proc = None
+        self.marks = []
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", gpu_id], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def mark(self):
+        self.marks.append(time.time())
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        inside = [p for t, p in self.samples if t0 - 0.25 <= t <= t1 + 0.25] or [p for _, p in self.samples]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+        sm = [num(p[1]) for p in inside if num(p[1]) is not None]
+        mx = [num(p[2]) for p in inside if num(p[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in inside for i in range(4) if p[5 + i].lower().startswith("active")})
+        power = [num(p[3]) for p in inside if num(p[3]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(inside), "power_w_max": max(power) if power else None}
+
+
+def cpu_oracle_step(inp, w, heads):
+    """The fp64 oracle forward + backward on the listed (b, h) heads (test infrastructure)."""
+    import oracle
+    for b, h in heads:
+        q, k, v, do = (inp[n][b, h] for n in ("q", "k", "v", "do"))
+        oracle.forward(q, k, v, w.causal, w.scale)
+        oracle.backward(q, k, v, do, w.causal, w.scale)
+
+
+def cpu_baseline(inp, w, n_heads: int):
+    import torch
+    heads = [(i // w.H % w.B, i % w.H) for i in range(n_heads)]
+    t0 = time.perf_counter()
+    cpu_oracle_step(inp, w, heads)
+    dt = time.perf_counter() - t0
+    f, b = conv_flops(w)
+    flops = (f + b) * n_heads / (w.B * w.H)
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": torch.get_num_threads(), "kind": "oracle",
+            "sample": f"fp64 oracle fwd+bwd on {n_heads} of the {w.B * w.H} (b,h) heads, S={w.S} D={w.D} causal, "
+                      f"{dt:.2f} s; convention FLOPs of those heads / wall time"}
+
+
+def run_reference(args, w):
+    """Reference arm: the CPU oracle as it stands, one head per step, rank 0 only."""
+    import torch
+    from seeded_inputs import make_inputs
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    inp = make_inputs(w, with_dout=True)
+    nh = w.B * w.H
+    for i in range(args.warmup):
+        cpu_oracle_step(inp, w, [((i // w.H) % w.B, i % w.H)])
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        j = (args.warmup + i) % nh
+        cpu_oracle_step(inp, w, [(j // w.H, j % w.H)])
+    dt = time.perf_counter() - t0
+    f, b = conv_flops(w)
+    flops_per_step = (f + b) / nh
+    value = flops_per_step * args.steps / dt / 1e12
+    sample = f"fp64 CPU oracle fwd+bwd of one (b,h) head of {w.describe()} per step"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "S": w.S, "D": w.D, "causal": w.causal,
+                       "sample_per_step": "one (b,h) head"},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": torch.get_num_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-heads", type=int, default=16, help="heads in the CPU oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    from seeded_inputs import CONFIGS
+    w = CONFIGS[WORKLOAD]
+    w = type(w)(w.name, w.B, w.H, w.S, w.D, w.dtype, w.causal, w.qk_std, True, w.seed)
+    if args.impl == "reference":
+        run_reference(args, w)
+        return
+
+    import torch
+    import exact_attention_18_gb300 as fa
+    from seeded_inputs import make_inputs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    inp = make_inputs(w, with_dout=True)
+    q, k, v, do = (inp[n].to(dev) for n in ("q", "k", "v", "do"))
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    ws_bytes = fa.fa_bwd_workspace_size(w.B, w.H, w.S, w.D)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    dt_code = fa.FA_FP16 if w.dtype == "fp16" else fa.FA_BF16
+    B, H, S, D = w.B, w.H, w.S, w.D
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        st = fa.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, S, D,
+                       w.causal, w.scale, dt_code, sp)
+        if st:
+            raise RuntimeError(f"fa_fwd: {fa.fa_status_string(st)} {fa.fa_last_error_detail()}")
+        marks = None if ev is None else [e.cuda_event for e in ev[1:5]]
+        st = fa.fa_bwd_marked(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
+                              lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, S, D, w.causal,
+                              w.scale, dt_code, ws.data_ptr(), ws_bytes, sp, marks)
+        if st:
+            raise RuntimeError(f"fa_bwd: {fa.fa_status_string(st)} {fa.fa_last_error_detail()}")
+
+    visible = os.environ.get("CUDA_VISIBLE_DEVICES")
+    gpu_id = visible.split(",")[local].strip() if visible else str(local)
+    sampler = ClockSampler(gpu_id)
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if fa.fa_check_device_errors(sp) != 0:
+        raise RuntimeError("device error during warm-up: " + fa.fa_last_error_detail())
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    for e in evs:  # create the CUDA events (torch creates them on first record) before the C side records them
+        for x in e:
+            x.record(stream)
+    barrier()
+    t_wall0 = time.time()
+    for i in range(args.steps):
+        flush.zero_()  # L2 flush between timed steps, outside the step's events
+        step(evs[i])
+    barrier()
+    t_wall1 = time.time()
+    if fa.fa_check_device_errors(sp) != 0:
+        raise RuntimeError("device error during the timed steps: " + fa.fa_last_error_detail())
+
+    names = ["fa_fwd_kernel", "fa_bwd_preprocess_kernel", "fa_bwd_dkdv_kernel", "fa_bwd_dq_kernel"]
+    per = {n: [] for n in names}
+    step_ms = []
+    for e in evs:
+        # fwd = e0->e1 (the fa_fwd launch); bwd kernels between the marks e1..e4
+        ts = [e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2]), e[2].elapsed_time(e[3]), e[3].elapsed_time(e[4])]
+        for n, t in zip(names, ts):
+            per[n].append(t)
+        step_ms.append(e[0].elapsed_time(e[4]))
+    total_ms = sum(step_ms)
+    if dist is not None:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    f_fwd, f_bwd = conv_flops(w)
+    value = world * (f_fwd + f_bwd) * args.steps / (total_ms * 1e-3) / 1e12
+    fwd_ms = statistics.mean(per["fa_fwd_kernel"])
+    bwd_ms = statistics.mean([a + b + c for a, b, c in zip(per["fa_bwd_preprocess_kernel"],
+                                                           per["fa_bwd_dkdv_kernel"], per["fa_bwd_dq_kernel"])])
+    peaks = load_peaks()
+    work = kernel_work(w)
+    avg = {n: statistics.mean(per[n]) for n in names}
+    dom = max(names, key=lambda n: avg[n])
+    kind, amount = work[dom]
+    traffic = load_traffic().get(dom)
+    if kind == "tensor":
+        achieved = amount / (avg[dom] * 1e-3) / 1e12
+        roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peaks["tensor_tflops"],
+                "unit": "TFLOP/s", "frac": achieved / peaks["tensor_tflops"], "traffic": traffic,
+                "peak_note": f"{peaks['source']} bf16 dense burst (fp16 runs at the same nominal rate)"}
+    else:
+        achieved = amount / (avg[dom] * 1e-3) / 1e9
+        roof = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": traffic, "peak_note": peaks["source"] + " copy"}
+
+    kernels = {}
+    for n in names:
+        kd, amt = work[n]
+        if kd == "tensor":
+            ach = amt / (avg[n] * 1e-3) / 1e12
+            kernels[n] = {"ms": avg[n], "TFLOP/s": ach, "frac_of_tensor_peak": ach / peaks["tensor_tflops"]}
+        else:
+            ach = amt / (avg[n] * 1e-3) / 1e9
+            kernels[n] = {"ms": avg[n], "GB/s": ach, "frac_of_hbm_peak": ach / peaks["hbm_gbs"]}
+
+    # ---------------------------------------------------------------- end to end through host buffers
+    e2e = None
+    if not args.no_e2e:
+        pin = {n: inp[n].pin_memory() for n in ("q", "k", "v", "do")}
+        outs = {"o": torch.empty(o.shape, dtype=o.dtype).pin_memory(),
+                "lse": torch.empty(lse.shape, dtype=lse.dtype).pin_memory(),
+                "dq": torch.empty(q.shape, dtype=q.dtype).pin_memory(),
+                "dk": torch.empty(q.shape, dtype=q.dtype).pin_memory(),
+                "dv": torch.empty(q.shape, dtype=q.dtype).pin_memory()}
+        h2d = sum(t.numel() * t.element_size() for t in pin.values())
+        d2h = sum(t.numel() * t.element_size() for t in outs.values())
+        dev_in = {"q": q, "k": k, "v": v, "do": do}
+        dev_out = {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
+
+        def e2e_step():
+            for n in pin:
+                dev_in[n].copy_(pin[n], non_blocking=True)
+            step()
+            for n in outs:
+                outs[n].copy_(dev_out[n], non_blocking=True)
+
+        for _ in range(args.warmup):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        barrier()
+        e2e_ms = e0.elapsed_time(e1)
+        if dist is not None:
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": world * (f_fwd + f_bwd) * args.steps / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps}
+    sampler.stop()
+    clocks = sampler.summary(t_wall0, t_wall1)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(inp, w, args.cpu_heads)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "fp16", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "S": w.S, "D": w.D, "causal": w.causal,
+                       "global_batch": w.B * world, "seq_len": w.S, "parallelism": f"independent x{world}",
+                       "step": "fa_fwd + fa_bwd", "l2": "flushed between timed steps (256 MiB write)",
+                       "flop_convention": "fwd 4*B*H*S^2*D/2 (causal), bwd 2.5x fwd"},
+            "fwd": {"ms": fwd_ms, "TFLOP/s": f_fwd / (fwd_ms * 1e-3) / 1e12,
+                    "frac_of_tensor_peak": f_fwd / (fwd_ms * 1e-3) / 1e12 / peaks["tensor_tflops"]},
+            "bwd": {"ms": bwd_ms, "TFLOP/s": f_bwd / (bwd_ms * 1e-3) / 1e12,
+                    "frac_of_tensor_peak": f_bwd / (bwd_ms * 1e-3) / 1e12 / peaks["tensor_tflops"]},
+            "kernels": kernels,
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "clocks": clocks,
+            "gpu_launches": 4 * args.steps,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

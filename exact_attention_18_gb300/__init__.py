@@ -1,0 +1,184 @@
+"""Python binding of the exact-attention C-ABI library (fa.h) for GB300.
+
+Argument marshalling only: every step of the attention computation runs in
+the library's CUDA kernels.  PyTorch supplies device memory and streams.
+
+The raw entry points keep the C names and signatures (pointers as ints):
+``fa_fwd``, ``fa_bwd``, ``fa_bwd_marked``, ``fa_bwd_workspace_size``, ``fa_status_string``,
+``fa_last_error_detail``, ``fa_check_device_errors``.  ``forward`` and
+``backward`` wrap them for contiguous [B, H, S, D] CUDA tensors.
+
+The first call loads the compiled library and raises if it has not been built
+(``python -m exact_attention_18_gb300.build``); there is no fallback
+implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libfa_gb300.so")
+
+__all__ = ["fa_fwd", "fa_bwd", "fa_bwd_marked", "fa_bwd_workspace_size", "fa_status_string", "fa_last_error_detail",
+           "fa_check_device_errors", "forward", "backward", "FAError", "FA_FP16", "FA_BF16", "STATUS",
+           "library_path", "load_library"]
+
+FA_FP16, FA_BF16 = 0, 1
+STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_ALIGNMENT",
+          4: "FA_ERR_WORKSPACE", 5: "FA_ERR_CUDA", 6: "FA_ERR_TIMEOUT"}
+
+_lib = None
+
+
+def _load():
+    """Load the compiled library once; raise if it has not been built (no fallback)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"the CUDA library {LIB_PATH} is not built; run "
+                           "`python -m exact_attention_18_gb300.build` (nvcc, sm_103a) first")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i64, i32, f32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.fa_fwd.restype = i32
+    lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i32, f32, i32, vp]
+    lib.fa_bwd_workspace_size.restype = sz
+    lib.fa_bwd_workspace_size.argtypes = [i64, i64, i64, i64]
+    lib.fa_bwd.restype = i32
+    lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i32, f32, i32, vp, sz, vp]
+    lib.fa_bwd_marked.restype = i32
+    lib.fa_bwd_marked.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i32, f32, i32, vp, sz,
+                                  vp, ctypes.POINTER(vp)]
+    lib.fa_status_string.restype = ctypes.c_char_p
+    lib.fa_status_string.argtypes = [i32]
+    lib.fa_last_error_detail.restype = ctypes.c_char_p
+    lib.fa_last_error_detail.argtypes = []
+    lib.fa_check_device_errors.restype = i32
+    lib.fa_check_device_errors.argtypes = [vp]
+    _lib = lib
+    return lib
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def load_library():
+    """The ctypes handle of the compiled library (loading it if needed)."""
+    return _load()
+
+
+# ----------------------------------------------------------------------- raw C ABI
+def fa_fwd(q, k, v, o, lse, B, H, S, D, causal, scale, dtype, stream) -> int:
+    return _load().fa_fwd(q, k, v, o, lse, B, H, S, D, int(causal), float(scale), int(dtype), stream)
+
+
+def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, S, D, causal, scale, dtype, workspace, workspace_bytes,
+           stream) -> int:
+    return _load().fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, S, D, int(causal), float(scale), int(dtype),
+                       workspace, workspace_bytes, stream)
+
+
+def fa_bwd_marked(q, k, v, o, dout, lse, dq, dk, dv, B, H, S, D, causal, scale, dtype, workspace,
+                  workspace_bytes, stream, marks) -> int:
+    arr = None
+    if marks is not None:
+        arr = (ctypes.c_void_p * 4)(*[m if m else None for m in marks])
+    return _load().fa_bwd_marked(q, k, v, o, dout, lse, dq, dk, dv, B, H, S, D, int(causal), float(scale),
+                                 int(dtype), workspace, workspace_bytes, stream, arr)
+
+
+def fa_bwd_workspace_size(B, H, S, D) -> int:
+    return _load().fa_bwd_workspace_size(B, H, S, D)
+
+
+def fa_status_string(status: int) -> str:
+    return _load().fa_status_string(status).decode()
+
+
+def fa_last_error_detail() -> str:
+    return _load().fa_last_error_detail().decode()
+
+
+def fa_check_device_errors(stream=None) -> int:
+    return _load().fa_check_device_errors(stream)
+
+
+# ----------------------------------------------------------------------- tensor wrappers
+class FAError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {STATUS.get(status, status)}: {fa_last_error_detail()}")
+        self.status = status
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise FAError(status, what)
+
+
+def _dtype_code(t):
+    import torch
+    if t.dtype == torch.float16:
+        return FA_FP16
+    if t.dtype == torch.bfloat16:
+        return FA_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}; use float16 or bfloat16")
+
+
+def _stream_ptr(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _bhsd(x, name):
+    if x.dim() == 3:  # [B, S, D] with no head dimension
+        x = x.unsqueeze(1)
+    if x.dim() != 4 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor [B, H, S, D] (or [B, S, D])")
+    return x
+
+
+def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None, stream=None):
+    """O and fp32 natural-log LSE of exact attention; tensors [B, H, S, D] (or [B, S, D])."""
+    import torch
+    squeeze = q.dim() == 3
+    q, k, v = _bhsd(q, "q"), _bhsd(k, "k"), _bhsd(v, "v")
+    if k.shape != q.shape or v.shape != q.shape or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must share shape and dtype")
+    B, H, S, D = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    o = torch.empty_like(q) if out is None else out.view(q.shape)
+    l = torch.empty((B, H, S), dtype=torch.float32, device=q.device) if lse is None else lse.view(B, H, S)
+    _check(fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), l.data_ptr(), B, H, S, D, causal,
+                  scale, _dtype_code(q), _stream_ptr(stream)), "fa_fwd")
+    if squeeze:
+        return o.squeeze(1), l.squeeze(1)
+    return o, l
+
+
+def backward(q, k, v, o, do, lse, causal: bool = False, scale: float | None = None, dq=None, dk=None, dv=None,
+             workspace=None, stream=None):
+    """dQ, dK, dV of exact attention from the forward's O and LSE (recompute backward)."""
+    import torch
+    squeeze = q.dim() == 3
+    q, k, v, o, do = (_bhsd(x, n) for x, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (do, "do")))
+    B, H, S, D = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    lse = lse.reshape(B, H, S)
+    dq = torch.empty_like(q) if dq is None else dq.view(q.shape)
+    dk = torch.empty_like(q) if dk is None else dk.view(q.shape)
+    dv = torch.empty_like(q) if dv is None else dv.view(q.shape)
+    need = fa_bwd_workspace_size(B, H, S, D)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _check(fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
+                  dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, S, D, causal, scale, _dtype_code(q),
+                  workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_ptr(stream)),
+           "fa_bwd")
+    if squeeze:
+        return dq.squeeze(1), dk.squeeze(1), dv.squeeze(1)
+    return dq, dk, dv

@@ -1,0 +1,250 @@
+// C-ABI entry points: argument validation, tensor-map encoding and launches.
+// Nothing here computes attention; every arithmetic step runs in the kernels.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "fa_internal.cuh"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+
+// One error word per device; kernels receive its address.
+static __device__ int g_fa_device_error = 0;
+
+int* device_error_word() {
+  static int* addr[64] = {nullptr};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* a = nullptr;
+    if (cudaGetSymbolAddress(&a, g_fa_device_error) != cudaSuccess) return nullptr;
+    addr[dev] = static_cast<int*>(a);
+  }
+  return addr[dev];
+}
+
+}  // namespace fa
+
+namespace {
+
+thread_local char g_detail[256] = "";
+
+fa_status fail(fa_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+fa_status fail(fa_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_detail, sizeof(g_detail), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+// cuTensorMapEncodeTiled, fetched from the driver through the runtime so the
+// library does not link against libcuda directly.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// [BH, S, D] 16-bit tensor as a 3-D map {D, S, BH}; box {row_bytes/2, 128, 1}.
+// Rows past S read as zero.
+fa_status encode_qkv_map(CUtensorMap* map, const void* base, bool bf16, int64_t D, int64_t S, int64_t BH,
+                         const char* name) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const int rb = fa::row_bytes_for(static_cast<int>(D));
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D * 2), static_cast<cuuint64_t>(S * D * 2)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(rb / 2), 128u, 1u};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUtensorMapSwizzle swz = rb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                     : (rb == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
+  CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "tensor map for %s: cuTensorMapEncodeTiled error %d", name, (int)r);
+  return FA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+fa_status check_common(int64_t B, int64_t H, int64_t S, int64_t D, float scale, fa_dtype dtype) {
+  if (B < 0 || H < 0 || S < 0) return fail(FA_ERR_INVALID_ARG, "negative size: B=%lld H=%lld S=%lld",
+                                           (long long)B, (long long)H, (long long)S);
+  if (dtype != FA_FP16 && dtype != FA_BF16) return fail(FA_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+  if (!std::isfinite(scale)) return fail(FA_ERR_INVALID_ARG, "scale must be finite");
+  if (D != 16 && D != 32 && D != 64 && D != 128)
+    return fail(FA_ERR_UNSUPPORTED, "head dimension D=%lld is not one of 16, 32, 64, 128", (long long)D);
+  if (B > 0 && H > (int64_t(1) << 31) / B) return fail(FA_ERR_UNSUPPORTED, "B*H must be below 2^31");
+  if (S >= (int64_t(1) << 31)) return fail(FA_ERR_UNSUPPORTED, "S must be below 2^31");
+  if ((S + 127) / 128 > 65535) return fail(FA_ERR_UNSUPPORTED, "S=%lld exceeds 65535 tiles of 128", (long long)S);
+  // element count must fit comfortably in 64-bit byte offsets
+  if (B * H > 0 && S * D > (int64_t(1) << 60) / (B * H)) return fail(FA_ERR_UNSUPPORTED, "tensor too large");
+  return FA_OK;
+}
+
+fa_status check_ptr(const void* p, const char* name) {
+  if (!p) return fail(FA_ERR_INVALID_ARG, "%s is NULL", name);
+  if (!aligned16(p)) return fail(FA_ERR_ALIGNMENT, "%s is not 16-byte aligned", name);
+  return FA_OK;
+}
+
+fa_status from_cuda(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return FA_OK;
+  return fail(FA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+}  // namespace
+
+extern "C" {
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H, int64_t S,
+                 int64_t D, int causal, float scale, fa_dtype dtype, void* stream) {
+  g_detail[0] = 0;
+  fa_status st = check_common(B, H, S, D, scale, dtype);
+  if (st != FA_OK) return st;
+  if ((st = check_ptr(q, "q")) || (st = check_ptr(k, "k")) || (st = check_ptr(v, "v")) ||
+      (st = check_ptr(o, "o")) || (st = check_ptr(lse, "lse")))
+    return st;
+  const int64_t BH = B * H;
+  if (BH == 0 || S == 0) return FA_OK;
+  const bool bf16 = dtype == FA_BF16;
+  CUtensorMap tq, tk, tv;
+  if ((st = encode_qkv_map(&tq, q, bf16, D, S, BH, "q")) || (st = encode_qkv_map(&tk, k, bf16, D, S, BH, "k")) ||
+      (st = encode_qkv_map(&tv, v, bf16, D, S, BH, "v")))
+    return st;
+  fa::FwdParams p;
+  p.o = o;
+  p.lse = lse;
+  p.S = static_cast<int>(S);
+  p.n_m_tiles = static_cast<int>((S + fa::kBlockM - 1) / fa::kBlockM);
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = scale * kLog2e;
+  p.err = fa::device_error_word();
+  if (!p.err) return fail(FA_ERR_CUDA, "cannot resolve the device error word on the current device");
+  return from_cuda(fa::launch_fwd(static_cast<int>(D), bf16, tq, tk, tv, p, static_cast<int>(BH),
+                                  static_cast<cudaStream_t>(stream)),
+                   "forward launch");
+}
+
+size_t fa_bwd_workspace_size(int64_t B, int64_t H, int64_t S, int64_t D) {
+  (void)D;
+  if (B <= 0 || H <= 0 || S <= 0) return 0;
+  const size_t bytes = static_cast<size_t>(B) * static_cast<size_t>(H) * static_cast<size_t>(S) * sizeof(float);
+  return (bytes + 255) & ~static_cast<size_t>(255);
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                 void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t S, int64_t D, int causal, float scale,
+                 fa_dtype dtype, void* workspace, size_t workspace_bytes, void* stream) {
+  return fa_bwd_marked(q, k, v, o, dout, lse, dq, dk, dv, B, H, S, D, causal, scale, dtype, workspace,
+                       workspace_bytes, stream, nullptr);
+}
+
+fa_status fa_bwd_marked(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                        const float* lse, void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t S, int64_t D,
+                        int causal, float scale, fa_dtype dtype, void* workspace, size_t workspace_bytes,
+                        void* stream, void* const* marks) {
+  g_detail[0] = 0;
+  fa_status st = check_common(B, H, S, D, scale, dtype);
+  if (st != FA_OK) return st;
+  if ((st = check_ptr(q, "q")) || (st = check_ptr(k, "k")) || (st = check_ptr(v, "v")) ||
+      (st = check_ptr(o, "o")) || (st = check_ptr(dout, "dout")) || (st = check_ptr(lse, "lse")) ||
+      (st = check_ptr(dq, "dq")) || (st = check_ptr(dk, "dk")) || (st = check_ptr(dv, "dv")))
+    return st;
+  const int64_t BH = B * H;
+  if (BH == 0 || S == 0) return FA_OK;
+  const size_t need = fa_bwd_workspace_size(B, H, S, D);
+  if (!workspace) return fail(FA_ERR_WORKSPACE, "workspace is NULL (%zu bytes needed)", need);
+  if (workspace_bytes < need)
+    return fail(FA_ERR_WORKSPACE, "workspace has %zu bytes, %zu needed", workspace_bytes, need);
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(FA_ERR_ALIGNMENT, "workspace is not 256-byte aligned");
+  const bool bf16 = dtype == FA_BF16;
+  CUtensorMap tq, tk, tv, tdo;
+  if ((st = encode_qkv_map(&tq, q, bf16, D, S, BH, "q")) || (st = encode_qkv_map(&tk, k, bf16, D, S, BH, "k")) ||
+      (st = encode_qkv_map(&tv, v, bf16, D, S, BH, "v")) ||
+      (st = encode_qkv_map(&tdo, dout, bf16, D, S, BH, "dout")))
+    return st;
+  fa::BwdParams p;
+  p.o = o;
+  p.dout = dout;
+  p.lse = lse;
+  p.delta = static_cast<float*>(workspace);
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.S = static_cast<int>(S);
+  p.BH = static_cast<int>(BH);
+  p.n_tiles = static_cast<int>((S + 127) / 128);
+  p.causal = causal ? 1 : 0;
+  p.scale = scale;
+  p.scale_log2 = scale * kLog2e;
+  p.err = fa::device_error_word();
+  if (!p.err) return fail(FA_ERR_CUDA, "cannot resolve the device error word on the current device");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int Di = static_cast<int>(D);
+  auto mark = [&](int i) -> fa_status {
+    if (!marks || !marks[i]) return FA_OK;
+    return from_cuda(cudaEventRecord(static_cast<cudaEvent_t>(marks[i]), s), "event record");
+  };
+  if ((st = mark(0))) return st;
+  if ((st = from_cuda(fa::launch_bwd_preprocess(Di, bf16, p, s), "backward preprocess launch"))) return st;
+  if ((st = mark(1))) return st;
+  if ((st = from_cuda(fa::launch_bwd_dkdv(Di, bf16, tq, tk, tv, tdo, p, s), "backward dK/dV launch"))) return st;
+  if ((st = mark(2))) return st;
+  if ((st = from_cuda(fa::launch_bwd_dq(Di, bf16, tq, tk, tv, tdo, p, s), "backward dQ launch"))) return st;
+  return mark(3);
+}
+
+const char* fa_status_string(fa_status status) {
+  switch (status) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+    case FA_ERR_ALIGNMENT: return "FA_ERR_ALIGNMENT";
+    case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+  }
+  return "FA_ERR_UNKNOWN";
+}
+
+const char* fa_last_error_detail(void) { return g_detail; }
+
+fa_status fa_check_device_errors(void* stream) {
+  g_detail[0] = 0;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return from_cuda(e, "stream synchronize");
+  int code = 0;
+  e = cudaMemcpyFromSymbol(&code, fa::g_fa_device_error, sizeof(int));
+  if (e != cudaSuccess) return from_cuda(e, "read device error word");
+  if (code != 0) {
+    const int zero = 0;
+    cudaMemcpyToSymbol(fa::g_fa_device_error, &zero, sizeof(int));
+    return fail(FA_ERR_TIMEOUT, "device pipeline wait timed out (code %d)", code);
+  }
+  return FA_OK;
+}
+
+}  // extern "C"

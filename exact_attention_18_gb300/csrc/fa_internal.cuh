@@ -1,0 +1,63 @@
+// Internal declarations shared by the host entry points and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fa {
+
+constexpr int kBlockM = 128;  // query rows per tile (= TMEM lanes)
+constexpr int kBlockN = 128;  // key rows per tile
+
+struct FwdParams {
+  void* o;             // [BH, S, D] output
+  float* lse;          // [BH, S] natural-log logsumexp
+  int S;               // sequence length
+  int n_m_tiles;       // ceil(S / kBlockM)
+  int causal;          // nonzero: key j visible to query i iff j <= i
+  float scale_log2;    // scale * log2(e): scores enter exp2 in base 2
+  int* err;            // device error word (set when a pipeline wait times out)
+};
+
+struct BwdParams {
+  const void* o;       // [BH, S, D] forward output
+  const void* dout;    // [BH, S, D] loss gradient w.r.t. O
+  const float* lse;    // [BH, S] natural-log logsumexp from the forward
+  float* delta;        // [BH, S] workspace: rowsum(dO o O)
+  void* dq;            // [BH, S, D]
+  void* dk;            // [BH, S, D]
+  void* dv;            // [BH, S, D]
+  int S;
+  int BH;
+  int n_tiles;         // ceil(S / 128)
+  int causal;
+  float scale;         // softmax scale (dQ, dK factor)
+  float scale_log2;    // scale * log2(e)
+  int* err;            // device error word
+};
+
+// Tensor maps for one [BH, S, D] 16-bit tensor viewed as 3-D {D, S, BH},
+// box {row_bytes / 2, 128, 1} with the swizzle matching row_bytes.
+struct TensorMaps3 {
+  CUtensorMap a, b, c;
+};
+
+// Launchers (one per kernel family); they dispatch on D and dtype.
+cudaError_t launch_fwd(int D, bool bf16, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const FwdParams& p, int BH, cudaStream_t stream);
+
+cudaError_t launch_bwd_preprocess(int D, bool bf16, const BwdParams& p, cudaStream_t stream);
+cudaError_t launch_bwd_dkdv(int D, bool bf16, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream);
+cudaError_t launch_bwd_dq(int D, bool bf16, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream);
+
+// Address of this process's device error word on the current device.
+int* device_error_word();
+
+// Bytes per swizzled shared-memory row for head dimension D (16-bit elements):
+// 32 for D = 16, 64 for D = 32, 128 for D >= 64 (D = 128 uses two column chunks).
+inline int row_bytes_for(int D) { return D * 2 < 128 ? D * 2 : 128; }
+
+}  // namespace fa

@@ -1,0 +1,102 @@
+// Helpers shared by the forward and backward kernels: shared-memory tile
+// geometry, MMA operand descriptors for TMA-swizzled tiles, bounded waits
+// that stay warp-uniform, and 16-bit packing.
+#pragma once
+
+#include <type_traits>
+
+#include "fa_internal.cuh"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+
+// A [128, D] tile of 16-bit elements as TMA writes it: `kChunks` column
+// chunks of 128 rows x kRowBytes, each swizzled at kRowBytes granularity.
+template <int D>
+struct TileGeom {
+  static constexpr int kRowBytes = D * 2 < 128 ? D * 2 : 128;
+  static constexpr int kChunks = D * 2 / kRowBytes;
+  static constexpr int kChunkBytes = 128 * kRowBytes;
+  static constexpr int kTileBytes = 128 * D * 2;
+  static constexpr uint32_t kSwz = ptx::swizzle_code_for(kRowBytes);
+};
+
+// Operand descriptor for K-step kk (16 elements along D) of a tile read
+// K-major (rows = M or N, D contiguous).
+template <int D>
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile_addr, int kk) {
+  using G = TileGeom<D>;
+  const int off = kk * 32;
+  return ptx::make_sdesc(tile_addr + (off / G::kRowBytes) * G::kChunkBytes + (off % G::kRowBytes), 16,
+                         8 * G::kRowBytes, G::kSwz);
+}
+
+// Operand descriptor for K-step kk (tile rows 16kk..16kk+15) of a tile read
+// MN-major (the tile's D columns are the N dimension, its rows the K dimension).
+template <int D>
+__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile_addr, int kk) {
+  using G = TileGeom<D>;
+  return ptx::make_sdesc(tile_addr + kk * 16 * G::kRowBytes, G::kChunkBytes, 8 * G::kRowBytes, G::kSwz);
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  if constexpr (BF16) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  } else {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+
+// All 32 lanes wait; the outcome is made warp-uniform (any failure = failure),
+// so the warp-collective tcgen05 loads and stores that follow never diverge.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* err, int code) {
+  const bool ok = ptx::mbar_wait(bar, parity, abort, err, code);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Bounded wait that ignores the abort flag: used at teardown for the CTA's
+// own copies and MMAs, which complete without help from other warps.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, int* err) {
+  if (ptx::mbar_try_wait(bar, parity)) return;
+  const unsigned long long t0 = ptx::globaltimer();
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if (ptx::globaltimer() - t0 > ptx::kWaitLimitNs) {
+      ptx::record_error(err, kErrTimeoutDrain);
+      return;
+    }
+  }
+}
+
+// Named barrier among the `nthreads` threads (a multiple of 32) that use `id`.
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Barrier over `nthreads` threads with id `id` that also returns the AND of
+// every participant's `v`.
+__device__ __forceinline__ bool named_sync_and(int id, int nthreads, bool v) {
+  uint32_t out;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\t"
+      "bar.red.and.pred po, %2, %3, pi;\n\tselp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(out)
+      : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(nthreads)
+      : "memory");
+  return out != 0;
+}
+
+// Store 16 fp32 values (times `mul`) as 16 16-bit elements at dst (32 bytes).
+template <bool BF16>
+__device__ __forceinline__ void store_row16(void* dst, const uint32_t* v, float mul) {
+  uint32_t w[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) w[i] = pack2<BF16>(__uint_as_float(v[2 * i]) * mul, __uint_as_float(v[2 * i + 1]) * mul);
+  uint4* d = reinterpret_cast<uint4*>(dst);
+  d[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+}  // namespace fa

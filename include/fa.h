@@ -1,0 +1,135 @@
+/*
+ * fa.h — C ABI of the exact-attention library for one NVIDIA GB300 (sm_103a).
+ *
+ * The library computes exact scaled-dot-product attention
+ *
+ *     O = softmax(scale * Q K^T) V
+ *
+ * FlashAttention-2 style: an outer loop over 128-row query blocks and an inner
+ * loop over 128-row key/value blocks with an online softmax (running row
+ * maximum m and running sum l), so the [S, S] score matrix never reaches
+ * memory.  Only O and the per-row logsumexp L are written.  The backward pass
+ * recomputes the probabilities from L.  Definitions followed:
+ *   - forward recurrence and L: "从零训练语言模型（第二部分：FlashAttention 与设备内存）"
+ *     §安全 / 在线 softmax and §使用 LSE 连接正向和反向传播;
+ *     "T5 讲解：FlashAttention forward" §④ (online softmax update), §⑤ (causal
+ *     block skipping), §⑥ (default scale 1/sqrt(D));
+ *   - backward: the same "第二部分" page §反向传播 (P = exp(S - L), dV = P^T dO,
+ *     dP = dO V^T, dS = P o (dP - D), dQ = dS K * scale, dK = dS^T Q * scale),
+ *     and the CS336 Assignment 2 write-up, "4. Problem (flash_backward)"
+ *     (recompute backward with the row vector D = rowsum(dO o O)).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Layout: every matrix argument (q, k, v, o, dout, dq, dk, dv) is a dense,
+ *   contiguous row-major tensor [B, H, S, D] of 16-bit floats (fp16 or bf16,
+ *   chosen by `dtype`), element strides (H*S*D, S*D, D, 1).  Query and key
+ *   lengths are equal (S).  `lse` is fp32 [B, H, S]; it holds the NATURAL-log
+ *   logsumexp of the scaled scores, L_i = ln sum_j exp(scale * q_i . k_j).
+ * Causal: when `causal` is nonzero, query i attends to keys j <= i (top-left
+ *   aligned mask).  Every query row then sees at least key 0.
+ * Scale: any finite float; the usual value is 1/sqrt(D).
+ * Supported: D in {16, 32, 64, 128}; S >= 0; B, H >= 0; B*H < 2^31;
+ *   S < 2^31.  S == 0 or B*H == 0 is a valid empty call that launches nothing.
+ * Pointers: DEVICE pointers of the current CUDA device, each 16-byte aligned
+ *   (the tensor-memory-access engine requires it).
+ * Ownership: the caller owns every buffer and the stream.  The library
+ *   allocates no memory, keeps no pointer after a call returns, and does not
+ *   synchronise: results are ready when `stream` reaches the launched work.
+ * Stream: a cudaStream_t passed as void* (NULL = the legacy default stream).
+ * Errors: every entry point validates all arguments before launching anything
+ *   and returns FA_OK or an fa_status code; nothing is launched on error.
+ *   fa_last_error_detail() gives a one-line description of the last failure
+ *   on the calling thread.  Kernels never trap: a device-side pipeline wait
+ *   that exceeds its time limit (2 s) ends the kernel and sets a device error
+ *   word that fa_check_device_errors() reads.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1, /* null pointer, negative size, non-finite scale, bad dtype */
+  FA_ERR_UNSUPPORTED = 2, /* head dimension not in {16,32,64,128}, or sizes too large */
+  FA_ERR_ALIGNMENT = 3,   /* a pointer is not 16-byte aligned */
+  FA_ERR_WORKSPACE = 4,   /* workspace missing or smaller than fa_bwd_workspace_size() */
+  FA_ERR_CUDA = 5,        /* a CUDA runtime/driver call or a kernel launch failed */
+  FA_ERR_TIMEOUT = 6      /* a device pipeline wait exceeded its limit (see fa_check_device_errors) */
+} fa_status;
+
+typedef enum { FA_FP16 = 0, FA_BF16 = 1 } fa_dtype;
+
+/*
+ * Forward pass.
+ *   q, k, v : [B, H, S, D] inputs (read only).
+ *   o       : [B, H, S, D] output, same dtype; O = softmax(scale Q K^T (+mask)) V.
+ *   lse     : [B, H, S] fp32 output, natural-log logsumexp per query row.
+ * Per query block the kernel visits only key blocks that are not wholly above
+ * the diagonal when causal ("T5 讲解" §⑤), masks element-wise only in the
+ * diagonal block and in a ragged last key block, and writes O / l and
+ * L = m + ln l in the epilogue.
+ */
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
+                 int64_t S, int64_t D, int causal, float scale, fa_dtype dtype, void* stream);
+
+/*
+ * Bytes of device workspace fa_bwd needs for these sizes: the fp32 row vector
+ * D_i = rowsum(dO o O) for every (b, h, i), rounded up to 256 bytes.
+ */
+size_t fa_bwd_workspace_size(int64_t B, int64_t H, int64_t S, int64_t D);
+
+/*
+ * Backward pass (recompute).  Given the forward inputs, its outputs o and lse,
+ * and the loss gradient dout = dL/dO, writes dq, dk, dv ([B, H, S, D], same
+ * dtype).  Three kernels run in order on `stream`:
+ *   1. D_i = rowsum(dO o O) into the workspace (fp32);
+ *   2. per 128-key block: dV = sum_i P^T dO and dK = scale * sum_i dS^T Q over the
+ *      query blocks that see it, P = exp(S - L) recomputed from lse;
+ *   3. per 128-query block: dQ = scale * sum_j dS K over its visible key blocks.
+ * workspace: device buffer of at least fa_bwd_workspace_size() bytes, 256-byte
+ * aligned, owned by the caller; its contents on entry do not matter.
+ */
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                 const float* lse, void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t S, int64_t D,
+                 int causal, float scale, fa_dtype dtype, void* workspace, size_t workspace_bytes,
+                 void* stream);
+
+/*
+ * fa_bwd with timing marks.  Same arguments, same three launches, same
+ * results; in addition, each non-NULL entry of `marks` (a cudaEvent_t passed
+ * as void*, owned by the caller) is recorded on `stream`: marks[0] before the
+ * Delta kernel, marks[1] after it, marks[2] after the dK/dV kernel, marks[3]
+ * after the dQ kernel.  Lets a caller time each kernel with CUDA events on
+ * the stream that runs it.  `marks` itself may be NULL.
+ */
+fa_status fa_bwd_marked(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                        const float* lse, void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t S,
+                        int64_t D, int causal, float scale, fa_dtype dtype, void* workspace,
+                        size_t workspace_bytes, void* stream, void* const* marks);
+
+/* Static, human-readable name of a status code. */
+const char* fa_status_string(fa_status status);
+
+/* One-line description of the last failure on the calling thread ("" if none). */
+const char* fa_last_error_detail(void);
+
+/*
+ * Synchronises `stream`, then reads and clears the device error word that the
+ * kernels set when a pipeline wait times out.  Returns FA_ERR_TIMEOUT if it
+ * was set, FA_ERR_CUDA if the synchronisation failed, else FA_OK.  Meant for
+ * tests and debugging; the compute entry points never synchronise.
+ */
+fa_status fa_check_device_errors(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

@@ -1,0 +1,110 @@
+"""The C-ABI library loads, exports every entry point fa.h declares, and rejects
+bad arguments before any CUDA call (these tests need no GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import exact_attention_18_gb300 as fa
+from exact_attention_18_gb300 import build as fab
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "fa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fab.build_library()
+    return fa.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_status_string",
+                     "fa_last_error_detail", "fa_check_device_errors"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in fa.h but not exported"
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_status_strings(lib):
+    for code, name in fa.STATUS.items():
+        assert fa.fa_status_string(code) == name
+    assert fa.fa_status_string(99) == "FA_ERR_UNKNOWN"
+
+
+def test_workspace_size(lib):
+    assert fa.fa_bwd_workspace_size(2, 32, 8192, 128) == 2 * 32 * 8192 * 4
+    assert fa.fa_bwd_workspace_size(1, 1, 3, 64) == 256  # rounded up to 256 bytes
+    assert fa.fa_bwd_workspace_size(0, 4, 16, 64) == 0
+
+
+P = 0x10000  # a fake, 16-byte aligned address: never dereferenced by these calls
+
+
+def fwd(**kw):
+    a = dict(q=P, k=P, v=P, o=P, lse=P, B=1, H=1, S=128, D=64, causal=0, scale=0.125, dtype=0, stream=None)
+    a.update(kw)
+    return fa.fa_fwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["S"], a["D"], a["causal"],
+                     a["scale"], a["dtype"], a["stream"])
+
+
+def bwd(**kw):
+    a = dict(q=P, k=P, v=P, o=P, do=P, lse=P, dq=P, dk=P, dv=P, B=1, H=1, S=128, D=64, causal=0, scale=0.125,
+             dtype=0, ws=P * 16, wsb=1 << 20, stream=None)
+    a.update(kw)
+    return fa.fa_bwd(a["q"], a["k"], a["v"], a["o"], a["do"], a["lse"], a["dq"], a["dk"], a["dv"], a["B"], a["H"],
+                     a["S"], a["D"], a["causal"], a["scale"], a["dtype"], a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(D=48), 2), (dict(D=256), 2), (dict(D=8), 2),
+    (dict(q=0), 1), (dict(lse=0), 1), (dict(o=0), 1),
+    (dict(k=P + 8), 3), (dict(v=P + 2), 3), (dict(lse=P + 4), 3),
+    (dict(S=-1), 1), (dict(B=-2), 1),
+    (dict(scale=float("inf")), 1), (dict(scale=float("nan")), 1),
+    (dict(dtype=7), 1),
+    (dict(S=65536 * 128), 2),
+])
+def test_fwd_rejects_bad_arguments(lib, kw, status):
+    assert fwd(**kw) == status
+    assert fa.fa_last_error_detail() != ""
+
+
+@pytest.mark.parametrize("kw", [dict(B=0), dict(H=0), dict(S=0)])
+def test_fwd_empty_is_a_no_op(lib, kw):
+    assert fwd(**kw) == 0
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(D=96), 2), (dict(do=0), 1), (dict(dq=P + 8), 3), (dict(ws=0), 4), (dict(wsb=100), 4),
+    (dict(ws=P * 16 + 16), 3), (dict(scale=float("-inf")), 1),
+])
+def test_bwd_rejects_bad_arguments(lib, kw, status):
+    assert bwd(**kw) == status
+    assert fa.fa_last_error_detail() != ""
+
+
+def test_bwd_empty_is_a_no_op(lib):
+    assert bwd(S=0) == 0
+    assert bwd(B=0, ws=0, wsb=0) == 0
+
+
+def test_binding_has_no_fallback(monkeypatch):
+    """Without the compiled library the binding raises instead of computing anything."""
+    import importlib
+    mod = importlib.import_module("exact_attention_18_gb300")
+    monkeypatch.setattr(mod, "_lib", None)
+    monkeypatch.setattr(mod, "LIB_PATH", "/nonexistent/libfa_gb300.so")
+    with pytest.raises(RuntimeError, match="not built"):
+        mod.fa_status_string(0)
