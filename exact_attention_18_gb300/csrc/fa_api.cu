@@ -123,11 +123,11 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   g_detail[0] = 0;
   fa_status st = check_common(B, H, S, D, scale, dtype);
   if (st != FA_OK) return st;
+  const int64_t BH = B * H;
+  if (BH == 0 || S == 0) return FA_OK;  // empty: nothing is read or written, pointers may be NULL
   if ((st = check_ptr(q, "q")) || (st = check_ptr(k, "k")) || (st = check_ptr(v, "v")) ||
       (st = check_ptr(o, "o")) || (st = check_ptr(lse, "lse")))
     return st;
-  const int64_t BH = B * H;
-  if (BH == 0 || S == 0) return FA_OK;
   const bool bf16 = dtype == FA_BF16;
   CUtensorMap tq, tk, tv;
   if ((st = encode_qkv_map(&tq, q, bf16, D, S, BH, "q")) || (st = encode_qkv_map(&tk, k, bf16, D, S, BH, "k")) ||
@@ -168,12 +168,12 @@ fa_status fa_bwd_marked(const void* q, const void* k, const void* v, const void*
   g_detail[0] = 0;
   fa_status st = check_common(B, H, S, D, scale, dtype);
   if (st != FA_OK) return st;
+  const int64_t BH = B * H;
+  if (BH == 0 || S == 0) return FA_OK;  // empty: nothing is read or written, pointers may be NULL
   if ((st = check_ptr(q, "q")) || (st = check_ptr(k, "k")) || (st = check_ptr(v, "v")) ||
       (st = check_ptr(o, "o")) || (st = check_ptr(dout, "dout")) || (st = check_ptr(lse, "lse")) ||
       (st = check_ptr(dq, "dq")) || (st = check_ptr(dk, "dk")) || (st = check_ptr(dv, "dv")))
     return st;
-  const int64_t BH = B * H;
-  if (BH == 0 || S == 0) return FA_OK;
   const size_t need = fa_bwd_workspace_size(B, H, S, D);
   if (!workspace) return fail(FA_ERR_WORKSPACE, "workspace is NULL (%zu bytes needed)", need);
   if (workspace_bytes < need)

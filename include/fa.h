@@ -32,7 +32,8 @@
  * Supported: D in {16, 32, 64, 128}; S >= 0; B, H >= 0; B*H < 2^31;
  *   S < 2^31.  S == 0 or B*H == 0 is a valid empty call that launches nothing.
  * Pointers: DEVICE pointers of the current CUDA device, each 16-byte aligned
- *   (the tensor-memory-access engine requires it).
+ *   (the tensor-memory-access engine requires it).  In an empty call they are
+ *   not used and may be NULL.
  * Ownership: the caller owns every buffer and the stream.  The library
  *   allocates no memory, keeps no pointer after a call returns, and does not
  *   synchronise: results are ready when `stream` reaches the launched work.

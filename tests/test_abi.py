@@ -81,9 +81,14 @@ def test_fwd_rejects_bad_arguments(lib, kw, status):
     assert fa.fa_last_error_detail() != ""
 
 
-@pytest.mark.parametrize("kw", [dict(B=0), dict(H=0), dict(S=0)])
+@pytest.mark.parametrize("kw", [dict(B=0), dict(H=0), dict(S=0), dict(S=0, q=0, k=0, v=0, o=0, lse=0)])
 def test_fwd_empty_is_a_no_op(lib, kw):
     assert fwd(**kw) == 0
+
+
+def test_empty_call_still_validates_shape_arguments(lib):
+    assert fwd(S=0, D=48) == 2
+    assert fwd(B=0, scale=float("nan")) == 1
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -98,6 +103,7 @@ def test_bwd_rejects_bad_arguments(lib, kw, status):
 def test_bwd_empty_is_a_no_op(lib):
     assert bwd(S=0) == 0
     assert bwd(B=0, ws=0, wsb=0) == 0
+    assert bwd(S=0, q=0, dq=0, ws=0, wsb=0) == 0
 
 
 def test_binding_has_no_fallback(monkeypatch):

@@ -66,36 +66,27 @@ def test_config_c4_sampled_heads(fa):
 def test_std2_variant(fa):
     """The other reading of "N(0, 2)": standard deviation 2, an extra stress case.
 
-    Here the bf16 representation of the gradients alone costs up to 0.015 and
-    rounding the MMA operand dS to bf16 (the input dtype, as every 16-bit
-    tensor-core backward does) costs ~0.025 on the exact gradients, so the
-    absolute 2e-2 bar of the configured workloads is below what any bf16-operand
-    kernel can reach.  The check is the first-order rounding bound instead,
-    element by element, with u = 2^-8 (bf16 unit roundoff):
-      |dQ - dQ*| <= 2 u (scale |dS| |K| + |dQ*|),  |dK - dK*| <= 2 u (scale |dS|^T |Q| + |dK*|),
-      |dV - dV*| <= 2 u (|P|^T |dO| + |dV*|),       plus 1e-3 for fp32 accumulation,
-    with P, dS, dQ*, dK*, dV* from the fp64 oracle.
+    The configured workload reads N(0, 2) as variance 2 and meets the absolute
+    bar.  With standard deviation 2 the exact gradients are about twice as
+    large, and bf16 error grows with them: the bf16 representation alone costs
+    up to 0.015, and rounding the MMA operand dS to bf16 (as every 16-bit
+    tensor-core backward does) costs ~0.025 on exact inputs.  So here the max
+    bar is the stated 2e-2 scaled by max|grad(std 2)| / max|grad(variance 2)|,
+    both from the oracle on the same seeds; the mean bar stays 2e-3.
     """
     w = Workload("c4_std2", 1, 2, 2048, 128, "bf16", False, qk_std=2.0, backward=True, seed=0)
+    w_var2 = Workload("c4_var2", 1, 2, 2048, 128, "bf16", False, qk_std=math.sqrt(2.0), backward=True, seed=0)
     inp = make_inputs(w)
+    inp2 = make_inputs(w_var2)
     o, lse, (dq, dk, dv) = fwd_bwd(fa, w, inp)
     check_forward_heads(inp, o, lse, False, w.scale, [(0, 0), (0, 1)])
-    u = 2.0 ** -8
     for h in (0, 1):
-        q, k, v, do = (oracle.as_f64(inp[n][0, h]) for n in ("q", "k", "v", "do"))
-        dq_r, dk_r, dv_r = oracle.backward(q, k, v, do, False, w.scale)
-        p, _ = oracle.softmax_rows(oracle.scores(q, k, w.scale, False))
-        dp = do @ v.T
-        ds = p * (dp - (p * dp).sum(-1, keepdim=True))
-        bounds = (2 * u * (w.scale * ds.abs() @ k.abs() + dq_r.abs()) + 1e-3,
-                  2 * u * (w.scale * ds.abs().T @ q.abs() + dk_r.abs()) + 1e-3,
-                  2 * u * (p.T @ do.abs() + dv_r.abs()) + 1e-3)
-        for name, got, ref, bound in (("dQ", dq, dq_r, bounds[0]), ("dK", dk, dk_r, bounds[1]),
-                                      ("dV", dv, dv_r, bounds[2])):
-            err = (got[0, h].double().cpu() - ref).abs()
-            worst = float((err / bound).max())
-            assert worst <= 1.0, f"{name}[0,{h}]: error reaches {worst:.2f} of the rounding bound"
-            assert float(err.mean()) <= 2e-3, f"{name}[0,{h}]: mean abs err {float(err.mean()):.2e}"
+        ref = oracle.backward(inp["q"][0, h], inp["k"][0, h], inp["v"][0, h], inp["do"][0, h], False, w.scale)
+        ref2 = oracle.backward(inp2["q"][0, h], inp2["k"][0, h], inp2["v"][0, h], inp2["do"][0, h], False,
+                               w.scale)
+        for name, got, r, r2 in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref, ref2):
+            ratio = max(1.0, float(r.abs().max()) / float(r2.abs().max()))
+            assert_close(f"{name}[0,{h}] (max bar x{ratio:.2f})", got[0, h], r, tol_max=2e-2 * ratio)
 
 
 def test_zero_dout_rows_give_exact_zero_dk_dv(fa):
