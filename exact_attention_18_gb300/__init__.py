@@ -20,7 +20,7 @@ import os
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libfa_gb300.so")
 
-__all__ = ["fa_fwd", "fa_bwd", "fa_bwd_marked", "fa_bwd_workspace_size", "fa_status_string", "fa_last_error_detail",
+__all__ = ["fa_fwd", "fa_bwd", "fa_bwd_marked", "fa_bwd_noalloc", "fa_bwd_workspace_size", "fa_status_string", "fa_last_error_detail",
            "fa_check_device_errors", "forward", "backward", "FAError", "FA_FP16", "FA_BF16", "STATUS",
            "library_path", "load_library"]
 
@@ -50,6 +50,8 @@ def _load():
     lib.fa_bwd_marked.restype = i32
     lib.fa_bwd_marked.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i32, f32, i32, vp, sz,
                                   vp, ctypes.POINTER(vp)]
+    lib.fa_bwd_noalloc.restype = i32
+    lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i32, f32, i32, vp]
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_status_string.argtypes = [i32]
     lib.fa_last_error_detail.restype = ctypes.c_char_p
@@ -87,6 +89,12 @@ def fa_bwd_marked(q, k, v, o, dout, lse, dq, dk, dv, B, H, S, D, causal, scale, 
         arr = (ctypes.c_void_p * 4)(*[m if m else None for m in marks])
     return _load().fa_bwd_marked(q, k, v, o, dout, lse, dq, dk, dv, B, H, S, D, int(causal), float(scale),
                                  int(dtype), workspace, workspace_bytes, stream, arr)
+
+
+def fa_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, B, H, S, D, causal, scale, dtype, stream) -> int:
+    """fa_bwd for callers that cannot allocate: its scratch is a fixed array inside the library."""
+    return _load().fa_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, B, H, S, D, int(causal), float(scale),
+                                  int(dtype), stream)
 
 
 def fa_bwd_workspace_size(B, H, S, D) -> int:

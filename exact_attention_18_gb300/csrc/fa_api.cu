@@ -31,6 +31,42 @@ int* device_error_word() {
 
 }  // namespace fa
 
+// ---------------------------------------------------------------------------
+// Scratch for fa_bwd_noalloc.  Some callers cannot allocate device memory at
+// the point where they need the backward pass (a custom allocator that must
+// not be re-entered, a memory pool that is already fully carved up, code
+// running under a framework that forbids cudaMalloc on its hot path).  For
+// them the backward's one scratch buffer, the fp32 row vector D, lives in this
+// fixed array instead of a caller workspace.  Every GPU that loads the library
+// holds it (8 MiB) until the process exits.
+namespace fa {
+constexpr int64_t kNoAllocMaxRows = int64_t(1) << 21;  // B*H*S rows: 2 Mi floats = 8 MiB
+static __device__ __align__(256) float g_noalloc_delta[kNoAllocMaxRows];
+
+// Device address of g_noalloc_delta on the current device.  In host code the
+// array's name only stands for the symbol, so the address is looked up once
+// per device (with that device current) and cached.
+float* noalloc_delta_address(cudaError_t* err) {
+  static float* addr[64] = {nullptr};
+  static std::mutex mu;
+  int dev = 0;
+  *err = cudaGetDevice(&dev);
+  if (*err != cudaSuccess) return nullptr;
+  if (dev < 0 || dev >= 64) {
+    *err = cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* a = nullptr;
+    *err = cudaGetSymbolAddress(&a, g_noalloc_delta);
+    if (*err != cudaSuccess) return nullptr;
+    addr[dev] = static_cast<float*>(a);
+  }
+  return addr[dev];
+}
+}  // namespace fa
+
 namespace {
 
 thread_local char g_detail[256] = "";
@@ -215,6 +251,26 @@ fa_status fa_bwd_marked(const void* q, const void* k, const void* v, const void*
   if ((st = mark(2))) return st;
   if ((st = from_cuda(fa::launch_bwd_dq(Di, bf16, tq, tk, tv, tdo, p, s), "backward dQ launch"))) return st;
   return mark(3);
+}
+
+fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                         const float* lse, void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t S,
+                         int64_t D, int causal, float scale, fa_dtype dtype, void* stream) {
+  g_detail[0] = 0;
+  fa_status st = check_common(B, H, S, D, scale, dtype);
+  if (st != FA_OK) return st;
+  const int64_t BH = B * H;
+  if (BH == 0 || S == 0) return FA_OK;
+  if (BH > fa::kNoAllocMaxRows / S)
+    return fail(FA_ERR_UNSUPPORTED, "fa_bwd_noalloc: B*H*S = %lld rows exceeds its fixed scratch of %lld rows",
+                (long long)(BH * S), (long long)fa::kNoAllocMaxRows);
+  cudaError_t e = cudaSuccess;
+  float* delta = fa::noalloc_delta_address(&e);
+  if (!delta) return from_cuda(e, "fa_bwd_noalloc: address of the scratch array");
+  // The same three kernels as fa_bwd, with the scratch array as the workspace.
+  // The Delta kernel overwrites every row it uses, so nothing needs clearing.
+  return fa_bwd_marked(q, k, v, o, dout, lse, dq, dk, dv, B, H, S, D, causal, scale, dtype, delta,
+                       static_cast<size_t>(fa::kNoAllocMaxRows) * sizeof(float), stream, nullptr);
 }
 
 const char* fa_status_string(fa_status status) {

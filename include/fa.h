@@ -115,6 +115,29 @@ fa_status fa_bwd_marked(const void* q, const void* k, const void* v, const void*
                         int64_t D, int causal, float scale, fa_dtype dtype, void* workspace,
                         size_t workspace_bytes, void* stream, void* const* marks);
 
+/*
+ * fa_bwd without a workspace argument, for callers that cannot allocate
+ * device memory when they run the backward pass (for example code inside a
+ * custom allocator or a fully carved-up memory pool, or a framework that
+ * forbids cudaMalloc on its hot path).  The pages describe no such variant:
+ * it has no counterpart there.
+ *
+ * Same arguments and results as fa_bwd minus the workspace.  The scratch row
+ * vector D lives in a fixed device array inside the library (8 MiB, held by
+ * every GPU that loads the library until the process exits), so
+ * B*H*S may not exceed 2^21 rows; larger calls return FA_ERR_UNSUPPORTED.
+ * The call allocates nothing: no cudaMalloc, cudaFree or allocating library
+ * routine.  Its first call on a device looks up the array's device address
+ * (with that device current) and caches it; make that first call before any
+ * stream capture.  All calls share the one array and it keeps the last
+ * call's contents (each call overwrites the rows it uses before reading
+ * them): calls whose work overlaps on the GPU, e.g. on two streams at once,
+ * race on it and must be serialised by the caller.
+ */
+fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                         const float* lse, void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t S,
+                         int64_t D, int causal, float scale, fa_dtype dtype, void* stream);
+
 /* Static, human-readable name of a status code. */
 const char* fa_status_string(fa_status status);
 
