@@ -173,7 +173,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   p.o = o;
   p.lse = lse;
   p.S = static_cast<int>(S);
-  p.n_m_tiles = static_cast<int>((S + fa::kBlockM - 1) / fa::kBlockM);
+  p.n_m_tiles = static_cast<int>((S + 2 * fa::kBlockM - 1) / (2 * fa::kBlockM));  // CTAs per head: 256 rows each
   p.causal = causal ? 1 : 0;
   p.scale_log2 = scale * kLog2e;
   p.err = fa::device_error_word();

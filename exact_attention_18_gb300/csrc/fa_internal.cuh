@@ -14,7 +14,7 @@ struct FwdParams {
   void* o;             // [BH, S, D] output
   float* lse;          // [BH, S] natural-log logsumexp
   int S;               // sequence length
-  int n_m_tiles;       // ceil(S / kBlockM)
+  int n_m_tiles;       // CTAs per (b, h): ceil(S / (2 * kBlockM))
   int causal;          // nonzero: key j visible to query i iff j <= i
   float scale_log2;    // scale * log2(e): scores enter exp2 in base 2
   int* err;            // device error word (set when a pipeline wait times out)

@@ -236,6 +236,18 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
 
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// Register reallocation between warpgroups (all four warps of a warpgroup
+// execute the same instruction).  The counts must add up to what the block
+// was launched with: increases wait until decreases elsewhere free registers.
+template <uint32_t N>
+__device__ __forceinline__ void regs_increase() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_decrease() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ------------------------------------------------------------------ descriptors
 // Shared-memory matrix descriptor for tcgen05 (64 bits):
 //   [0,14)  start address >> 4        [16,30) leading-dimension byte offset >> 4

@@ -67,26 +67,27 @@ def test_std2_variant(fa):
     """The other reading of "N(0, 2)": standard deviation 2, an extra stress case.
 
     The configured workload reads N(0, 2) as variance 2 and meets the absolute
-    bar.  With standard deviation 2 the exact gradients are about twice as
-    large, and bf16 error grows with them: the bf16 representation alone costs
-    up to 0.015, and rounding the MMA operand dS to bf16 (as every 16-bit
-    tensor-core backward does) costs ~0.025 on exact inputs.  So here the max
-    bar is the stated 2e-2 scaled by max|grad(std 2)| / max|grad(variance 2)|,
-    both from the oracle on the same seeds; the mean bar stays 2e-3.
+    bars.  With standard deviation 2 the forward still does (checked here), but
+    the backward's max-abs error is set by bf16 itself: the gradients reach
+    |6.6|, where one bf16 rounding alone costs up to 0.015, and an emulation of
+    the 16-bit pipeline on exact inputs (P and dS rounded to bf16 as MMA
+    operands, Delta taken from the bf16 output O) reaches 0.040 in dQ.  So the
+    backward is held to the stated mean-abs bar (2e-3) and to a norm-wise
+    relative error ||got - ref|| / ||ref|| <= 1e-2 (about 2.5 bf16 unit
+    roundoffs; the emulation gives 0.0037), both against the fp64 oracle.
     """
     w = Workload("c4_std2", 1, 2, 2048, 128, "bf16", False, qk_std=2.0, backward=True, seed=0)
-    w_var2 = Workload("c4_var2", 1, 2, 2048, 128, "bf16", False, qk_std=math.sqrt(2.0), backward=True, seed=0)
     inp = make_inputs(w)
-    inp2 = make_inputs(w_var2)
     o, lse, (dq, dk, dv) = fwd_bwd(fa, w, inp)
     check_forward_heads(inp, o, lse, False, w.scale, [(0, 0), (0, 1)])
     for h in (0, 1):
         ref = oracle.backward(inp["q"][0, h], inp["k"][0, h], inp["v"][0, h], inp["do"][0, h], False, w.scale)
-        ref2 = oracle.backward(inp2["q"][0, h], inp2["k"][0, h], inp2["v"][0, h], inp2["do"][0, h], False,
-                               w.scale)
-        for name, got, r, r2 in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref, ref2):
-            ratio = max(1.0, float(r.abs().max()) / float(r2.abs().max()))
-            assert_close(f"{name}[0,{h}] (max bar x{ratio:.2f})", got[0, h], r, tol_max=2e-2 * ratio)
+        for name, got, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
+            d = got[0, h].double().cpu() - r
+            rel = float(d.norm() / r.norm())
+            mean = float(d.abs().mean())
+            assert rel <= 1e-2 and mean <= 2e-3, \
+                f"{name}[0,{h}]: relative error {rel:.2e}, mean abs {mean:.2e}, max abs {float(d.abs().max()):.2e}"
 
 
 def test_zero_dout_rows_give_exact_zero_dk_dv(fa):
