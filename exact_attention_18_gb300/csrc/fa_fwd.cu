@@ -14,7 +14,9 @@
 //   warp 9     MMA issuer.  Per key block j it issues, in this order,
 //              O0 += P0(j-1) V(j-1), S0 = Q0 K(j)^T, O1 += P1(j-1) V(j-1),
 //              S1 = Q1 K(j)^T, so while one warpgroup runs the softmax of its
-//              tile the tensor core works on the other tile.
+//              tile the tensor core works on the other tile (the warp
+//              specialisation and matmul/softmax overlap of "Inside
+//              FlashAttention" §5.1-5.2).
 // TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D), O1 after it.
 // P (16-bit) is written over the first 64 columns of its tile's S and read
 // by the P V MMA straight from TMEM.  The tensor core runs one CTA's MMAs in
