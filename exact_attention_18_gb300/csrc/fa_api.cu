@@ -100,16 +100,16 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// [BH, S, D] 16-bit tensor as a 3-D map {D, S, BH}; box {row_bytes/2, 128, 1}.
+// [BH, S, D] 16-bit tensor as a 3-D map {D, S, BH}; box {row_bytes/2, box_rows, 1}.
 // Rows past S read as zero.
 fa_status encode_qkv_map(CUtensorMap* map, const void* base, bool bf16, int64_t D, int64_t S, int64_t BH,
-                         const char* name) {
+                         const char* name, unsigned box_rows = 128) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   const int rb = fa::row_bytes_for(static_cast<int>(D));
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(BH)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(D * 2), static_cast<cuuint64_t>(S * D * 2)};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(rb / 2), 128u, 1u};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(rb / 2), static_cast<cuuint32_t>(box_rows), 1u};
   cuuint32_t estr[3] = {1u, 1u, 1u};
   CUtensorMapSwizzle swz = rb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
                                      : (rb == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
@@ -165,9 +165,11 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
       (st = check_ptr(o, "o")) || (st = check_ptr(lse, "lse")))
     return st;
   const bool bf16 = dtype == FA_BF16;
+  // Q in 128-row boxes (a CTA's own tiles); K and V in 64-row boxes (each CTA
+  // of a cluster pair loads half of every block for both).
   CUtensorMap tq, tk, tv;
-  if ((st = encode_qkv_map(&tq, q, bf16, D, S, BH, "q")) || (st = encode_qkv_map(&tk, k, bf16, D, S, BH, "k")) ||
-      (st = encode_qkv_map(&tv, v, bf16, D, S, BH, "v")))
+  if ((st = encode_qkv_map(&tq, q, bf16, D, S, BH, "q")) || (st = encode_qkv_map(&tk, k, bf16, D, S, BH, "k", 64)) ||
+      (st = encode_qkv_map(&tv, v, bf16, D, S, BH, "v", 64)))
     return st;
   fa::FwdParams p;
   p.o = o;
@@ -217,10 +219,15 @@ fa_status fa_bwd_marked(const void* q, const void* k, const void* v, const void*
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return fail(FA_ERR_ALIGNMENT, "workspace is not 256-byte aligned");
   const bool bf16 = dtype == FA_BF16;
-  CUtensorMap tq, tk, tv, tdo;
-  if ((st = encode_qkv_map(&tq, q, bf16, D, S, BH, "q")) || (st = encode_qkv_map(&tk, k, bf16, D, S, BH, "k")) ||
-      (st = encode_qkv_map(&tv, v, bf16, D, S, BH, "v")) ||
-      (st = encode_qkv_map(&tdo, dout, bf16, D, S, BH, "dout")))
+  fa::BwdMaps maps;
+  if ((st = encode_qkv_map(&maps.q128, q, bf16, D, S, BH, "q")) ||
+      (st = encode_qkv_map(&maps.k128, k, bf16, D, S, BH, "k")) ||
+      (st = encode_qkv_map(&maps.v128, v, bf16, D, S, BH, "v")) ||
+      (st = encode_qkv_map(&maps.do128, dout, bf16, D, S, BH, "dout")) ||
+      (st = encode_qkv_map(&maps.q64, q, bf16, D, S, BH, "q", 64)) ||
+      (st = encode_qkv_map(&maps.k64, k, bf16, D, S, BH, "k", 64)) ||
+      (st = encode_qkv_map(&maps.v64, v, bf16, D, S, BH, "v", 64)) ||
+      (st = encode_qkv_map(&maps.do64, dout, bf16, D, S, BH, "dout", 64)))
     return st;
   fa::BwdParams p;
   p.o = o;
@@ -233,6 +240,7 @@ fa_status fa_bwd_marked(const void* q, const void* k, const void* v, const void*
   p.S = static_cast<int>(S);
   p.BH = static_cast<int>(BH);
   p.n_tiles = static_cast<int>((S + 127) / 128);
+  p.n_partner = static_cast<int>((S + 63) / 64);
   p.causal = causal ? 1 : 0;
   p.scale = scale;
   p.scale_log2 = scale * kLog2e;
@@ -247,9 +255,9 @@ fa_status fa_bwd_marked(const void* q, const void* k, const void* v, const void*
   if ((st = mark(0))) return st;
   if ((st = from_cuda(fa::launch_bwd_preprocess(Di, bf16, p, s), "backward preprocess launch"))) return st;
   if ((st = mark(1))) return st;
-  if ((st = from_cuda(fa::launch_bwd_dkdv(Di, bf16, tq, tk, tv, tdo, p, s), "backward dK/dV launch"))) return st;
+  if ((st = from_cuda(fa::launch_bwd_dkdv(Di, bf16, maps, p, s), "backward dK/dV launch"))) return st;
   if ((st = mark(2))) return st;
-  if ((st = from_cuda(fa::launch_bwd_dq(Di, bf16, tq, tk, tv, tdo, p, s), "backward dQ launch"))) return st;
+  if ((st = from_cuda(fa::launch_bwd_dq(Di, bf16, maps, p, s), "backward dQ launch"))) return st;
   return mark(3);
 }
 

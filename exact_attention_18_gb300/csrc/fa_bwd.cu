@@ -11,24 +11,28 @@
 // FlashAttention-2 Leaderboard", which avoids atomics):
 //   1. bwd_preprocess: Delta for every row (memory-bound, one pass over O, dO);
 //   2. bwd_main<KV_OUTER = true>:  one CTA per (b*h, 128-key tile), looping
-//      over the query tiles that see it; accumulates dV and dK in TMEM;
+//      over 64-row blocks of the queries that see it; dV and dK stay in TMEM;
 //   3. bwd_main<KV_OUTER = false>: one CTA per (b*h, 128-query tile), looping
-//      over its visible key tiles; accumulates dQ in TMEM.
-// Causal: a key tile starts at the diagonal query tile, a query tile stops at
-// the diagonal key tile (CS336 write-up, causal tile skipping); the mask is
-// applied element-wise only on the diagonal tile and on ragged tails.
+//      over 64-row blocks of its visible keys; dQ stays in TMEM.
+// Causal: a key tile starts at its diagonal query block, a query tile stops at
+// its diagonal key block (CS336 write-up, causal tile skipping); the mask is
+// applied element-wise only on diagonal blocks and on ragged tails.
 //
-// bwd_main is written once for both passes.  In each iteration it computes
-// two score-shaped products with the CTA's resident tiles A1, A2 as the MMA
-// A operands and the streamed tiles B1, B2 as B operands:
+// bwd_main is written once for both passes.  Per partner block i it computes
+// two score-shaped products with the CTA's resident 128-row tiles A1, A2 as
+// the MMA A operands and the streamed 64-row tiles B1, B2 as B operands:
 //   X = A1 B1^T,  Y = A2 B2^T
 //     dK/dV pass: A1 = K, A2 = V, B1 = Q_i, B2 = dO_i -> X = S^T, Y = dP^T
 //     dQ pass:    A1 = Q, A2 = dO, B1 = K_j, B2 = V_j -> X = S,   Y = dP
-// so TMEM lane = the CTA's own row (key or query) and each softmax thread owns
-// a whole row.  The softmax warps turn X, Y into P and dS (16-bit, written
-// back into TMEM over X and Y), then the MMA warp accumulates
-//     dK/dV pass: dV += P^T dO_i,  dK += dS^T Q_i   (A from TMEM, B = B2, B1 MN-major)
-//     dQ pass:    dQ += dS K_j                      (A from TMEM, B = B1 MN-major)
+// so TMEM lane = the CTA's own row (key or query).  Eight softmax-gradient
+// warps turn X, Y into P and dS (16-bit, written back into TMEM over X and Y);
+// warp w owns TMEM lanes 32(w%4).. and the 32 partner columns 32(w/4)...  The
+// MMA warp then accumulates, with A read from TMEM:
+//     dK/dV pass: dV += P^T dO_i,  dK += dS^T Q_i    (B = B2, B1 read MN-major)
+//     dQ pass:    dQ += dS K_j                       (B = B1 read MN-major)
+// X and Y are double-buffered (two 128-column TMEM buffers), and the MMA
+// warp issues X,Y(i+1) before the accumulation of block i, so the tensor core
+// works on the next block while the warps turn the current one into P and dS.
 #include "fa_kernel_common.cuh"
 
 namespace fa {
@@ -76,37 +80,48 @@ __global__ void __launch_bounds__(256) fa_bwd_preprocess_kernel(const BwdParams 
 
 namespace {
 
-template <int D, bool KV_OUTER>
-struct BwdLayout : TileGeom<D> {
-  using G = TileGeom<D>;
-  static constexpr int kStages = 2;
+constexpr int kPartnerRows = 64;  // rows of a streamed B tile
+constexpr int kBwdThreads = 320;  // 8 softmax-gradient warps, producer, MMA
+
+template <int D>
+struct BwdLayout {
+  using GA = TileGeom<D, 128>;
+  using GB = TileGeom<D, kPartnerRows>;
+  static constexpr int kStages = 4;
   static constexpr int kOffA1 = 0;
-  static constexpr int kOffA2 = kOffA1 + G::kTileBytes;
-  static constexpr int kOffB1 = kOffA2 + G::kTileBytes;                  // [kStages] tiles
-  static constexpr int kOffB2 = kOffB1 + kStages * G::kTileBytes;        // [kStages] tiles
-  static constexpr int kOffRowVec = kOffB2 + kStages * G::kTileBytes;    // [2][2][128] fp32: L2, Delta per column
-  static constexpr int kOffBar = kOffRowVec + 2 * 2 * 128 * 4;
-  // a_full, b_full[S], empty[S], xy_full, p_full, acc_done, drain
-  static constexpr int kNumBars = 1 + 2 * kStages + 4;
+  static constexpr int kOffA2 = kOffA1 + GA::kTileBytes;
+  static constexpr int kOffB1 = kOffA2 + GA::kTileBytes;                // [kStages] tiles
+  static constexpr int kOffB2 = kOffB1 + kStages * GB::kTileBytes;      // [kStages] tiles
+  static constexpr int kOffRowVec = kOffB2 + kStages * GB::kTileBytes;  // [2 buffers][L2, Delta][64] fp32
+  static constexpr int kOffBar = kOffRowVec + 2 * 2 * kPartnerRows * 4;
+  // a_full, b_full[S], empty[S], xy_full[2], p_full[2], acc_final, drain
+  static constexpr int kNumBars = 1 + 2 * kStages + 4 + 2;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemUsed = kOffMisc + 16;
   static constexpr int kSmemBytes = (kSmemUsed + 1024) > 116 * 1024 ? (kSmemUsed + 1024) : 116 * 1024;
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kColX = 0;     // S or S^T; P^T overwrites its first 64 columns
-  static constexpr uint32_t kColY = 128;   // dP or dP^T; dS (dS^T) overwrites its first 64 columns
-  static constexpr uint32_t kColAcc1 = 256;                 // dV (dK/dV pass) or dQ
-  static constexpr uint32_t kColAcc2 = 384;                 // dK (dK/dV pass)
+  // Buffer b: X at column 128 b, Y at 128 b + 64 (64 fp32 columns each).
+  static constexpr uint32_t kColAcc1 = 256;      // dV (dK/dV pass) or dQ
+  static constexpr uint32_t kColAcc2 = 256 + D;  // dK (dK/dV pass)
 };
+
+// TMEM column (relative to a buffer's X or Y) of MMA K-step kk of the 16-bit
+// P or dS block: warp half h wrote partner columns 32h..32h+31 packed into
+// columns 32h..32h+15 of its own 32-column region.
+__device__ __forceinline__ uint32_t packed_col(int kk) { return kk < 2 ? kk * 8 : 32 + (kk - 2) * 8; }
 
 }  // namespace
 
 template <int D, bool BF16, bool KV_OUTER>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_a1, const __grid_constant__ CUtensorMap tm_a2,
                        const __grid_constant__ CUtensorMap tm_b1, const __grid_constant__ CUtensorMap tm_b2,
                        const BwdParams p) {
-  using L = BwdLayout<D, KV_OUTER>;
+  using L = BwdLayout<D>;
+  using GA = typename L::GA;
+  using GB = typename L::GB;
   using elem_t = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+  constexpr int kPN = kPartnerRows;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -114,10 +129,10 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* bar_afull = bars;
   uint64_t* bar_bfull = bars + 1;
   uint64_t* bar_empty = bar_bfull + L::kStages;
-  uint64_t* bar_xyfull = bar_empty + L::kStages;
-  uint64_t* bar_pfull = bar_xyfull + 1;
-  uint64_t* bar_accdone = bar_pfull + 1;
-  uint64_t* bar_drain = bar_accdone + 1;
+  uint64_t* bar_xyfull = bar_empty + L::kStages;  // [2]
+  uint64_t* bar_pfull = bar_xyfull + 2;           // [2]
+  uint64_t* bar_accfinal = bar_pfull + 2;
+  uint64_t* bar_drain = bar_accfinal + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 4);
   float* rowvec = reinterpret_cast<float*>(smem + L::kOffRowVec);
@@ -127,14 +142,15 @@ __global__ void __launch_bounds__(192, 1)
   const int bh = blockIdx.x;
   const int S = p.S;
   const int nt = p.n_tiles;
+  const int np = p.n_partner;
   // Own tile; heavy tiles first under the causal mask (key tile 0 and query
   // tile nt-1 see the most partners).
   const int own = KV_OUTER ? static_cast<int>(blockIdx.y)
                            : (p.causal ? nt - 1 - static_cast<int>(blockIdx.y) : static_cast<int>(blockIdx.y));
-  const int first = (KV_OUTER && p.causal) ? own : 0;
-  const int last_excl = (!KV_OUTER && p.causal) ? own + 1 : nt;
-  const int niter = last_excl - first;
   const int own0 = own * 128;
+  const int first = (KV_OUTER && p.causal) ? own0 / kPN : 0;
+  const int last_excl = (!KV_OUTER && p.causal) ? min(np, (own0 + 127) / kPN + 1) : np;
+  const int niter = last_excl - first;
 
   if (threadIdx.x == 0) {
     mbar_init(bar_afull, 1);
@@ -142,14 +158,16 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&bar_bfull[s], 1);
       mbar_init(&bar_empty[s], 1);
     }
-    mbar_init(bar_xyfull, 1);
-    mbar_init(bar_pfull, 128);
-    mbar_init(bar_accdone, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bar_xyfull[b], 1);
+      mbar_init(&bar_pfull[b], 8);  // one arrival per softmax-gradient warp
+    }
+    mbar_init(bar_accfinal, 1);
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(tmem_slot, L::kTmemCols);
     tmem_relinquish();
   }
@@ -162,184 +180,226 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t sB1 = smem_u32(smem + L::kOffB1);
   const uint32_t sB2 = smem_u32(smem + L::kOffB2);
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       prefetch_tmap(&tm_a1);
       prefetch_tmap(&tm_a2);
       prefetch_tmap(&tm_b1);
       prefetch_tmap(&tm_b2);
-      mbar_arrive_expect_tx(bar_afull, 2 * L::kTileBytes);
+      mbar_arrive_expect_tx(bar_afull, 2 * GA::kTileBytes);
 #pragma unroll
-      for (int ch = 0; ch < L::kChunks; ++ch) {
-        tma_load_3d(smem + L::kOffA1 + ch * L::kChunkBytes, &tm_a1, bar_afull, ch * (L::kRowBytes / 2), own0, bh);
-        tma_load_3d(smem + L::kOffA2 + ch * L::kChunkBytes, &tm_a2, bar_afull, ch * (L::kRowBytes / 2), own0, bh);
+      for (int ch = 0; ch < GA::kChunks; ++ch) {
+        tma_load_3d(smem + L::kOffA1 + ch * GA::kChunkBytes, &tm_a1, bar_afull, ch * (GA::kRowBytes / 2), own0, bh);
+        tma_load_3d(smem + L::kOffA2 + ch * GA::kChunkBytes, &tm_a2, bar_afull, ch * (GA::kRowBytes / 2), own0, bh);
       }
       int it = 0;
       for (; it < niter; ++it) {
         const int st = it % L::kStages;
         const int use = it / L::kStages;
         if (use > 0 && !mbar_wait(&bar_empty[st], (use - 1) & 1, abort_flag, p.err, kErrTimeoutLoad)) break;
-        const int r0 = (first + it) * 128;
-        mbar_arrive_expect_tx(&bar_bfull[st], 2 * L::kTileBytes);
+        const int r0 = (first + it) * kPN;
+        mbar_arrive_expect_tx(&bar_bfull[st], 2 * GB::kTileBytes);
 #pragma unroll
-        for (int ch = 0; ch < L::kChunks; ++ch) {
-          tma_load_3d(smem + L::kOffB1 + st * L::kTileBytes + ch * L::kChunkBytes, &tm_b1, &bar_bfull[st],
-                      ch * (L::kRowBytes / 2), r0, bh);
-          tma_load_3d(smem + L::kOffB2 + st * L::kTileBytes + ch * L::kChunkBytes, &tm_b2, &bar_bfull[st],
-                      ch * (L::kRowBytes / 2), r0, bh);
+        for (int ch = 0; ch < GB::kChunks; ++ch) {
+          tma_load_3d(smem + L::kOffB1 + st * GB::kTileBytes + ch * GB::kChunkBytes, &tm_b1, &bar_bfull[st],
+                      ch * (GB::kRowBytes / 2), r0, bh);
+          tma_load_3d(smem + L::kOffB2 + st * GB::kTileBytes + ch * GB::kChunkBytes, &tm_b2, &bar_bfull[st],
+                      ch * (GB::kRowBytes / 2), r0, bh);
         }
       }
       drain_wait(bar_afull, 0, p.err);
       for (int x = (it > L::kStages ? it - L::kStages : 0); x < it; ++x)
         drain_wait(&bar_bfull[x % L::kStages], (x / L::kStages) & 1, p.err);
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_xy = make_idesc_f16(BF16, 128, 128, false, false);
-      constexpr uint32_t idesc_acc = make_idesc_f16(BF16, 128, D, false, true);
-      bool ok = mbar_wait(bar_afull, 0, abort_flag, p.err, kErrTimeoutMma);
-      for (int it = 0; ok && it < niter; ++it) {
-        const int st = it % L::kStages;
-        ok = mbar_wait(&bar_bfull[st], (it / L::kStages) & 1, abort_flag, p.err, kErrTimeoutMma);
-        // X and Y are overwritten below: the previous iteration's accumulation
-        // (which reads P and dS from them) must be complete.
-        if (ok && it > 0) ok = mbar_wait(bar_accdone, (it - 1) & 1, abort_flag, p.err, kErrTimeoutMma);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t b1 = sB1 + st * L::kTileBytes;
-        const uint32_t b2 = sB2 + st * L::kTileBytes;
+    // The whole warp runs this code converged and one elected lane issues
+    // each MMA; descriptors are built once per stage and advanced by
+    // compile-time offsets, so issue keeps pace with the tensor core.
+    constexpr uint32_t idesc_xy = make_idesc_f16(BF16, 128, kPN, false, false);
+    constexpr uint32_t idesc_acc = make_idesc_f16(BF16, 128, D, false, true);
+    const uint64_t a1_desc = make_sdesc(sA1, 16, 8 * GA::kRowBytes, GA::kSwz);
+    const uint64_t a2_desc = make_sdesc(sA2, 16, 8 * GA::kRowBytes, GA::kSwz);
+    // X, Y of block i into buffer i & 1.  The buffer was last read by the
+    // accumulation of block i - 2, issued earlier by this warp; the tensor
+    // core runs one CTA's MMAs in issue order.
+    auto xy = [&](int i) {
+      const int st = i % L::kStages;
+      const uint32_t tb = tmem + 128u * (i & 1);
+      const uint64_t b1 = make_sdesc(sB1 + st * GB::kTileBytes, 16, 8 * GB::kRowBytes, GB::kSwz);
+      const uint64_t b2 = make_sdesc(sB2 + st * GB::kTileBytes, 16, 8 * GB::kRowBytes, GB::kSwz);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + L::kColX, kmajor_desc<D>(sA1, kk), kmajor_desc<D>(b1, kk), idesc_xy, kk > 0 ? 1u : 0u);
+      for (int kk = 0; kk < D / 16; ++kk)
+        mma_ss_warp(tb, desc_plus(a1_desc, kmajor_step_bytes<D, 128>(kk)), desc_plus(b1, kmajor_step_bytes<D, kPN>(kk)),
+                    idesc_xy, kk > 0 ? 1u : 0u);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + L::kColY, kmajor_desc<D>(sA2, kk), kmajor_desc<D>(b2, kk), idesc_xy, kk > 0 ? 1u : 0u);
-        mma_commit(bar_xyfull);
-        ok = mbar_wait(bar_pfull, it & 1, abort_flag, p.err, kErrTimeoutMma);
-        if (!ok) break;
-        tc_fence_after();
-        if constexpr (KV_OUTER) {
+      for (int kk = 0; kk < D / 16; ++kk)
+        mma_ss_warp(tb + 64, desc_plus(a2_desc, kmajor_step_bytes<D, 128>(kk)),
+                    desc_plus(b2, kmajor_step_bytes<D, kPN>(kk)), idesc_xy, kk > 0 ? 1u : 0u);
+      mma_commit_warp(&bar_xyfull[i & 1]);
+    };
+    auto acc = [&](int x) -> bool {
+      const int st = x % L::kStages;
+      if (!warp_wait(&bar_pfull[x & 1], (x >> 1) & 1, abort_flag, p.err, kErrTimeoutMma)) return false;
+      tc_fence_after();
+      const uint32_t tb = tmem + 128u * (x & 1);
+      const uint64_t b1 = make_sdesc(sB1 + st * GB::kTileBytes, GB::kChunkBytes, 8 * GB::kRowBytes, GB::kSwz);
+      const uint64_t b2 = make_sdesc(sB2 + st * GB::kTileBytes, GB::kChunkBytes, 8 * GB::kRowBytes, GB::kSwz);
+      if constexpr (KV_OUTER) {
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)  // dV += P^T dO_i
-            mma_ts(tmem + L::kColAcc1, tmem + L::kColX + kk * 8, mnmajor_desc<D>(b2, kk), idesc_acc,
-                   (it > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < kPN / 16; ++kk)  // dV += P^T dO_i
+          mma_ts_warp(tmem + L::kColAcc1, tb + packed_col(kk), desc_plus(b2, mnmajor_step_bytes<D>(kk)), idesc_acc,
+                      (x > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)  // dK += dS^T Q_i
-            mma_ts(tmem + L::kColAcc2, tmem + L::kColY + kk * 8, mnmajor_desc<D>(b1, kk), idesc_acc,
-                   (it > 0 || kk > 0) ? 1u : 0u);
-        } else {
+        for (int kk = 0; kk < kPN / 16; ++kk)  // dK += dS^T Q_i
+          mma_ts_warp(tmem + L::kColAcc2, tb + 64 + packed_col(kk), desc_plus(b1, mnmajor_step_bytes<D>(kk)),
+                      idesc_acc, (x > 0 || kk > 0) ? 1u : 0u);
+      } else {
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)  // dQ += dS K_j
-            mma_ts(tmem + L::kColAcc1, tmem + L::kColY + kk * 8, mnmajor_desc<D>(b1, kk), idesc_acc,
-                   (it > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(&bar_empty[st]);
-        mma_commit(bar_accdone);
+        for (int kk = 0; kk < kPN / 16; ++kk)  // dQ += dS K_j
+          mma_ts_warp(tmem + L::kColAcc1, tb + 64 + packed_col(kk), desc_plus(b1, mnmajor_step_bytes<D>(kk)),
+                      idesc_acc, (x > 0 || kk > 0) ? 1u : 0u);
       }
-      mma_commit(bar_drain);
-      drain_wait(bar_drain, 0, p.err);
+      mma_commit_warp(&bar_empty[st]);
+      return true;
+    };
+    bool ok = warp_wait(bar_afull, 0, abort_flag, p.err, kErrTimeoutMma);
+    for (int i = 0; ok && i < niter; ++i) {
+      ok = warp_wait(&bar_bfull[i % L::kStages], (i / L::kStages) & 1, abort_flag, p.err, kErrTimeoutMma);
+      if (!ok) break;
+      tc_fence_after();
+      xy(i);
+      if (i >= 1) ok = acc(i - 1);
     }
-    __syncwarp();
+    if (ok && acc(niter - 1)) mma_commit_warp(bar_accfinal);
+    mma_commit_warp(bar_drain);
+    drain_wait(bar_drain, 0, p.err);
   } else {
-    // ------------------------------------------------------------ softmax-gradient warps 0-3
-    const int r = threadIdx.x;
-    const int my = own0 + r;  // key index (dK/dV pass) or query index (dQ pass)
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t tX = tmem + lane_base + L::kColX;
-    const uint32_t tY = tmem + lane_base + L::kColY;
+    // ------------------------------------------------------------ softmax-gradient warps 0-7
+    const int q4 = warp & 3;      // TMEM lane quarter
+    const int hf = warp >> 2;     // which 32 of the 64 partner columns
+    const int col0 = 32 * hf;
+    const int my = own0 + q4 * 32 + lane;  // key index (dK/dV pass) or query index (dQ pass)
+    const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
     const float sl2 = p.scale_log2;
+    const float2 c2 = make_float2(sl2, sl2);
     constexpr float kLog2e = 1.4426950408889634f;
     const int64_t rowbase = static_cast<int64_t>(bh) * S;
-    // dQ pass: this thread's query row owns its L2 = L * log2 e and Delta.
+    // dQ pass: this thread's query row owns its L2 = L * log2 e and Delta
+    // (rows past S: L2 = +inf, so their probabilities are exactly 0).
     float my_l2 = INFINITY, my_delta = 0.f;
     if (!KV_OUTER && my < S) {
       my_l2 = p.lse[rowbase + my] * kLog2e;
       my_delta = p.delta[rowbase + my];
     }
+    // dK/dV pass: threads 0-63 fetch L2 of the block's 64 query columns and
+    // threads 64-127 their Delta, one block ahead, so the global-load latency
+    // overlaps the previous block's work.  Queries past S get L2 = +inf.
+    auto fetch_colvec = [&](int i) -> float {
+      const int q = (first + i) * kPN + (threadIdx.x & (kPN - 1));
+      if (i >= niter || q >= S) return threadIdx.x < kPN ? INFINITY : 0.f;
+      return threadIdx.x < kPN ? p.lse[rowbase + q] * kLog2e : p.delta[rowbase + q];
+    };
+    float colv = 0.f;
+    if (KV_OUTER && threadIdx.x < 2 * kPN) colv = fetch_colvec(0);
     bool alive = true;
-    for (int it = 0; it < niter; ++it) {
-      const int other0 = (first + it) * 128;
-      float* l2v = rowvec + (it & 1) * 256;
-      float* dlv = l2v + 128;
+    for (int i = 0; i < niter; ++i) {
+      const int b = i & 1;
+      const int partner0 = (first + i) * kPN;
+      float* l2v = rowvec + b * 2 * kPN;
+      float* dlv = l2v + kPN;
       if constexpr (KV_OUTER) {
-        // Per-column (query) L2 and Delta for this query tile; queries past S
-        // get L2 = +inf, so their probabilities are exactly 0.
-        const int q = other0 + r;
-        l2v[r] = q < S ? p.lse[rowbase + q] * kLog2e : INFINITY;
-        dlv[r] = q < S ? p.delta[rowbase + q] : 0.f;
+        // Buffer b was last read two blocks ago, before the previous block's barrier.
+        if (threadIdx.x < 2 * kPN) {
+          l2v[threadIdx.x] = colv;  // l2v and dlv are contiguous: [L2 x 64][Delta x 64]
+          colv = fetch_colvec(i + 1);
+        }
       }
-      // One barrier over the 128 threads publishes the column vectors and
+      // One barrier over the 256 threads publishes the column vectors and
       // makes the outcome of the wait uniform, so no thread is ever left
       // waiting at a barrier that the others have abandoned.
-      const bool got = mbar_wait(bar_xyfull, it & 1, abort_flag, p.err, kErrTimeoutSoftmax);
-      if (!named_sync_and(1, 128, got)) {
+      const bool got = mbar_wait(&bar_xyfull[b], (i >> 1) & 1, abort_flag, p.err, kErrTimeoutSoftmax);
+      if (!named_sync_and(1, 256, got)) {
         alive = false;
         break;
       }
       tc_fence_after();
-      // Masked tiles: the diagonal under the causal mask, and a tile of
-      // partner rows that runs past S (keys past S in the dQ pass).
-      const bool diag = p.causal && (other0 == own0);
-      const bool tail = !KV_OUTER && (other0 + 128 > S);
+      const uint32_t tX = tmem + lane_base + 128u * b + col0;
+      const uint32_t tY = tX + 64;
+      uint32_t xs[32], ys[32];
+      tmem_ld32(tX, xs);
+      tmem_ld32(tY, ys);
+      // Masked blocks: partner rows that cross the diagonal under the causal
+      // mask, and blocks that run past S.
+      const bool masked = (partner0 + kPN > S) ||
+                          (p.causal && (KV_OUTER ? partner0 < own0 + 128 : partner0 + kPN - 1 > own0));
+      uint32_t pk[16], dk[16];
 #pragma unroll
-      for (int c0 = 0; c0 < 128; c0 += 32) {
-        uint32_t xs[32], ys[32];
-        tmem_ld32(tX + c0, xs);
-        tmem_ld32(tY + c0, ys);
-        uint32_t pk[16], dk[16];
-#pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          float pr[2], ds[2];
+      for (int c = 0; c < 32; c += 2) {
+        float2 l2, dl;
+        if constexpr (KV_OUTER) {
+          l2 = make_float2(l2v[col0 + c], l2v[col0 + c + 1]);
+          dl = make_float2(dlv[col0 + c], dlv[col0 + c + 1]);
+        } else {
+          l2 = make_float2(my_l2, my_l2);
+          dl = make_float2(my_delta, my_delta);
+        }
+        const float2 y = __ffma2_rn(make_float2(__uint_as_float(xs[c]), __uint_as_float(xs[c + 1])), c2,
+                                    make_float2(-l2.x, -l2.y));
+        float2 pr = make_float2(ex2(y.x), ex2(y.y));
+        if (masked) {
+          const int other = partner0 + col0 + c;
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
-            const int col = c0 + c + u;
-            const float l2 = KV_OUTER ? l2v[col] : my_l2;
-            const float dl = KV_OUTER ? dlv[col] : my_delta;
-            float pv = ex2(fmaf(__uint_as_float(xs[c + u]), sl2, -l2));
-            if (diag || tail) {
-              const int key = KV_OUTER ? my : other0 + col;
-              const int qry = KV_OUTER ? other0 + col : my;
-              if ((p.causal && key > qry) || key >= S) pv = 0.f;
-            }
-            pr[u] = pv;
-            ds[u] = pv * (__uint_as_float(ys[c + u]) - dl);
+            const int key = KV_OUTER ? my : other + u;
+            const int qry = KV_OUTER ? other + u : my;
+            if ((p.causal && key > qry) || key >= S || qry >= S) (u == 0 ? pr.x : pr.y) = 0.f;
           }
-          pk[c / 2] = pack2<BF16>(pr[0], pr[1]);
-          dk[c / 2] = pack2<BF16>(ds[0], ds[1]);
         }
-        // 16-bit P (dK/dV pass only) and dS go over columns already consumed.
-        if constexpr (KV_OUTER) tmem_st16(tX + c0 / 2, pk);
-        tmem_st16(tY + c0 / 2, dk);
+        const float2 g = __fadd2_rn(make_float2(__uint_as_float(ys[c]), __uint_as_float(ys[c + 1])),
+                                    make_float2(-dl.x, -dl.y));
+        const float2 ds = __fmul2_rn(pr, g);
+        pk[c / 2] = pack2<BF16>(pr.x, pr.y);
+        dk[c / 2] = pack2<BF16>(ds.x, ds.y);
       }
+      // 16-bit P (dK/dV pass only) and dS go over the first 16 columns of this
+      // warp's own 32-column slice of X and Y.
+      if constexpr (KV_OUTER) tmem_st16(tX, pk);
+      tmem_st16(tY, dk);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar_pfull);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_pfull[b]);
     }
     // ------------------------------------------------------------ epilogue
-    const bool done = alive && mbar_wait(bar_accdone, (niter - 1) & 1, abort_flag, p.err, kErrTimeoutSoftmax);
-    if (__all_sync(0xffffffffu, done)) {
+    const bool done = alive && mbar_wait(bar_accfinal, 0, abort_flag, p.err, kErrTimeoutSoftmax);
+    // Each warp stores half of the accumulator columns of its 32 rows (all of
+    // them when D = 16, from the warps of half 0).
+    constexpr int kEpiCols = D / 2 >= 16 ? D / 2 : D;
+    const int c_begin = D / 2 >= 16 ? hf * kEpiCols : 0;
+    if (__all_sync(0xffffffffu, done) && (D / 2 >= 16 || hf == 0)) {
       tc_fence_after();
       const bool row_ok = my < S;
       const size_t off = (static_cast<size_t>(rowbase) + (row_ok ? my : 0)) * D;
+      const uint32_t t_acc = tmem + lane_base;
       if constexpr (KV_OUTER) {
         elem_t* dv_row = reinterpret_cast<elem_t*>(p.dv) + off;
         elem_t* dk_row = reinterpret_cast<elem_t*>(p.dk) + off;
 #pragma unroll
-        for (int c = 0; c < D; c += 16) {
+        for (int c = c_begin; c < c_begin + kEpiCols; c += 16) {
           uint32_t v16[16];
-          tmem_ld16(tmem + lane_base + L::kColAcc1 + c, v16);
+          tmem_ld16(t_acc + L::kColAcc1 + c, v16);
           if (row_ok) store_row16<BF16>(dv_row + c, v16, 1.f);
-          tmem_ld16(tmem + lane_base + L::kColAcc2 + c, v16);
+          tmem_ld16(t_acc + L::kColAcc2 + c, v16);
           if (row_ok) store_row16<BF16>(dk_row + c, v16, p.scale);
         }
       } else {
         elem_t* dq_row = reinterpret_cast<elem_t*>(p.dq) + off;
 #pragma unroll
-        for (int c = 0; c < D; c += 16) {
+        for (int c = c_begin; c < c_begin + kEpiCols; c += 16) {
           uint32_t v16[16];
-          tmem_ld16(tmem + lane_base + L::kColAcc1 + c, v16);
+          tmem_ld16(t_acc + L::kColAcc1 + c, v16);
           if (row_ok) store_row16<BF16>(dq_row + c, v16, p.scale);
         }
       }
@@ -348,7 +408,7 @@ __global__ void __launch_bounds__(192, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, L::kTmemCols);
   }
@@ -369,24 +429,24 @@ cudaError_t launch_pre_t(const BwdParams& p, cudaStream_t stream) {
 template <int D, bool BF16, bool KV_OUTER>
 cudaError_t launch_main_t(const CUtensorMap& a1, const CUtensorMap& a2, const CUtensorMap& b1,
                           const CUtensorMap& b2, const BwdParams& p, cudaStream_t stream) {
-  using L = BwdLayout<D, KV_OUTER>;
+  using L = BwdLayout<D>;
   auto kern = fa_bwd_main_kernel<D, BF16, KV_OUTER>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
   if (e != cudaSuccess) return e;
   dim3 grid(p.BH, p.n_tiles);
-  kern<<<grid, 192, L::kSmemBytes, stream>>>(a1, a2, b1, b2, p);
+  kern<<<grid, kBwdThreads, L::kSmemBytes, stream>>>(a1, a2, b1, b2, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-#define FA_BWD_DISPATCH(CALL)                              \
-  switch (D) {                                             \
-    case 16: return bf16 ? CALL(16, true) : CALL(16, false);   \
-    case 32: return bf16 ? CALL(32, true) : CALL(32, false);   \
-    case 64: return bf16 ? CALL(64, true) : CALL(64, false);   \
+#define FA_BWD_DISPATCH(CALL)                                   \
+  switch (D) {                                                  \
+    case 16: return bf16 ? CALL(16, true) : CALL(16, false);    \
+    case 32: return bf16 ? CALL(32, true) : CALL(32, false);    \
+    case 64: return bf16 ? CALL(64, true) : CALL(64, false);    \
     case 128: return bf16 ? CALL(128, true) : CALL(128, false); \
-    default: return cudaErrorInvalidValue;                 \
+    default: return cudaErrorInvalidValue;                      \
   }
 
 cudaError_t launch_bwd_preprocess(int D, bool bf16, const BwdParams& p, cudaStream_t stream) {
@@ -395,16 +455,14 @@ cudaError_t launch_bwd_preprocess(int D, bool bf16, const BwdParams& p, cudaStre
 #undef FA_PRE
 }
 
-cudaError_t launch_bwd_dkdv(int D, bool bf16, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream) {
-#define FA_DKDV(DD, BB) launch_main_t<DD, BB, true>(tk, tv, tq, tdo, p, stream)
+cudaError_t launch_bwd_dkdv(int D, bool bf16, const BwdMaps& m, const BwdParams& p, cudaStream_t stream) {
+#define FA_DKDV(DD, BB) launch_main_t<DD, BB, true>(m.k128, m.v128, m.q64, m.do64, p, stream)
   FA_BWD_DISPATCH(FA_DKDV)
 #undef FA_DKDV
 }
 
-cudaError_t launch_bwd_dq(int D, bool bf16, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                          const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream) {
-#define FA_DQ(DD, BB) launch_main_t<DD, BB, false>(tq, tdo, tk, tv, p, stream)
+cudaError_t launch_bwd_dq(int D, bool bf16, const BwdMaps& m, const BwdParams& p, cudaStream_t stream) {
+#define FA_DQ(DD, BB) launch_main_t<DD, BB, false>(m.q128, m.do128, m.k64, m.v64, p, stream)
   FA_BWD_DISPATCH(FA_DQ)
 #undef FA_DQ
 }

@@ -9,18 +9,23 @@
 //              row max and row sum need no cross-thread reduction (the split-Q
 //              partition of "Inside FlashAttention" §4.3);
 //   warp 8     TMA producer: both Q tiles once, then K and V blocks through a
-//              ring of shared-memory stages (warps 10-11 idle; warps 8-11 give
+//              ring of shared-memory stages (warp 11 idle; warps 8-11 give
 //              their registers to the softmax warpgroups with setmaxnreg);
-//   warp 9     MMA issuer.  Per key block j it issues, in this order,
-//              O0 += P0(j-1) V(j-1), S0 = Q0 K(j)^T, O1 += P1(j-1) V(j-1),
-//              S1 = Q1 K(j)^T, so while one warpgroup runs the softmax of its
-//              tile the tensor core works on the other tile (the warp
-//              specialisation and matmul/softmax overlap of "Inside
-//              FlashAttention" §5.1-5.2).
-// TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D), O1 after it.
-// P (16-bit) is written over the first 64 columns of its tile's S and read
-// by the P V MMA straight from TMEM.  The tensor core runs one CTA's MMAs in
-// issue order, so S(j+1) is written only after P(j) V(j) has read P(j).
+//   warps 9-10 MMA issuers, one per tile.
+// The two tiles' softmax work overlaps the tensor core's work on the other
+// tile (the warp specialisation and matmul/softmax overlap of "Inside
+// FlashAttention" §5.1-5.2).
+//
+// TMEM (512 columns) for D <= 64: S0 [0,128), S1 [128,256), P0 [256,320),
+// P1 [320,384), O0 [384,384+D), O1 after it.  P (16-bit) has its own columns,
+// so a warpgroup releases S_t(j) as soon as it has loaded it into registers
+// and the MMA warp computes S_t(j+1) while the softmax of block j still runs.
+// Per key block j the MMA warp issues S0 = Q0 K(j)^T, S1 = Q1 K(j)^T, then
+// O0 += P0(j-1) V(j-1), O1 += P1(j-1) V(j-1).
+// For D = 128 (O0, O1 take 256 columns) P is written over the first 64
+// columns of its S and the order is O0 += P0 V, S0 = Q0 K^T, O1 += P1 V,
+// S1 = Q1 K^T; the tensor core runs one CTA's MMAs in issue order, so S(j+1)
+// is written only after P(j) V(j) has read P(j).
 //
 // Per key block j, per row, in the base-2 domain (c = scale * log2 e):
 //   m_blk = c * rowmax(S_j)                        ("T5 讲解" §④; "fa-triton" Step 2)
@@ -44,30 +49,35 @@ namespace {
 constexpr int kFwdThreads = 384;
 // Register split (per thread): the launch gives every thread kLaunchRegs; the
 // producer/MMA warpgroup drops to kRegsLow and both softmax warpgroups rise
-// to kRegsHigh.  2 * 128 * kRegsHigh + 128 * kRegsLow == 384 * kLaunchRegs.
+// to kRegsHigh; the shares may not exceed the launch total 384 * kLaunchRegs.
 constexpr int kLaunchRegs = 168;
 constexpr uint32_t kRegsHigh = 224;
 constexpr uint32_t kRegsLow = 56;
-static_assert(2 * 128 * kRegsHigh + 128 * kRegsLow == kFwdThreads * kLaunchRegs, "register split");
+static_assert(2 * 128 * kRegsHigh + 128 * kRegsLow <= kFwdThreads * kLaunchRegs, "register split");
 constexpr float kTau = 8.0f;  // stale-max threshold (log2 units)
 
 template <int D>
 struct FwdLayout : TileGeom<D> {
   using G = TileGeom<D>;
+  static constexpr bool kSepP = D <= 64;  // P in its own TMEM columns
   static constexpr int kStages = D <= 64 ? 3 : 2;
   static constexpr int kOffQ = 0;  // two query tiles
   static constexpr int kOffK = kOffQ + 2 * G::kTileBytes;
   static constexpr int kOffV = kOffK + kStages * G::kTileBytes;
   static constexpr int kOffBar = kOffV + kStages * G::kTileBytes;
-  // q, kfull[S], vfull[S], empty[S], sfull[2], pfull[2], ofinal[2], drain
-  static constexpr int kNumBars = 1 + 3 * kStages + 6 + 1;
+  // q, kfull[S], vfull[S], empty[S], sfull[2], sfree[2], pfull[2], pvdone[2], ofinal[2], drain[2]
+  static constexpr int kNumBars = 1 + 3 * kStages + 10 + 2;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemUsed = kOffMisc + 16;
   // Tensor memory is allocated whole (512 columns), so at most one CTA may
   // live on an SM: the request is padded above half of the SM's shared memory.
   static constexpr int kSmemBytes = (kSmemUsed + 1024) > 116 * 1024 ? (kSmemUsed + 1024) : 116 * 1024;
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kColO = 256;  // O0 at 256, O1 at 256 + D
+  static constexpr uint32_t kColS = 0;                   // S_t at 128 t
+  static constexpr uint32_t kColP = kSepP ? 256 : 0;     // P_t at kColP + (kSepP ? 64 : 128) t
+  static constexpr uint32_t kStrideP = kSepP ? 64 : 128;
+  static constexpr uint32_t kColO = kSepP ? 384 : 256;   // O_t at kColO + D t
+  static_assert(kColO + 2 * D <= kTmemCols, "TMEM layout");
 };
 
 __device__ __forceinline__ float max3(float a, float b, float c) {
@@ -81,8 +91,18 @@ __device__ __forceinline__ float min3(float a, float b, float c) {
   return d;
 }
 
+// Warp-collective: after this warp's tcgen05 stores/loads are complete, one
+// elected lane arrives on `bar` (whose count is the number of arriving warps).
+__device__ __forceinline__ void warp_arrive(uint64_t* bar) {
+  tc_fence_before();
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 }  // namespace
 
+// tm_q: 128-row boxes (a CTA's own query tiles); tm_k, tm_v: 64-row boxes
+// (each K/V block arrives as two half-block copies).
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -97,10 +117,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   uint64_t* bar_kfull = bars + 1;
   uint64_t* bar_vfull = bar_kfull + L::kStages;
   uint64_t* bar_empty = bar_vfull + L::kStages;
-  uint64_t* bar_sfull = bar_empty + L::kStages;  // [2] per tile
-  uint64_t* bar_pfull = bar_sfull + 2;           // [2]
-  uint64_t* bar_ofinal = bar_pfull + 2;          // [2]
-  uint64_t* bar_drain = bar_ofinal + 2;
+  uint64_t* bar_sfull = bar_empty + L::kStages;  // [2] per tile: S_t(j) computed
+  uint64_t* bar_sfree = bar_sfull + 2;           // [2] S_t(j) loaded by its warpgroup (separate-P layout)
+  uint64_t* bar_pfull = bar_sfree + 2;           // [2] P_t(j) stored, O_t rescaled
+  uint64_t* bar_pvdone = bar_pfull + 2;          // [2] O_t += P_t(j) V(j) done (separate-P layout)
+  uint64_t* bar_ofinal = bar_pvdone + 2;         // [2] last P V of tile t done
+  uint64_t* bar_drain = bar_ofinal + 2;          // [2] one per MMA warp
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 4);
 
@@ -108,26 +130,34 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int lane = threadIdx.x & 31;
   const int bh = blockIdx.x;
   const int S = p.S;
-  const int cta = p.causal ? (p.n_m_tiles - 1 - static_cast<int>(blockIdx.y)) : static_cast<int>(blockIdx.y);
+  // Under the causal mask the heaviest CTAs are launched first.
+  const int cta = p.causal ? p.n_m_tiles - 1 - static_cast<int>(blockIdx.y) : static_cast<int>(blockIdx.y);
   const int row0 = cta * 2 * kBlockM;
   const int n_kv = (S + kBlockN - 1) / kBlockN;
-  // Key blocks visited by each tile (tile 1 sees at most one more under the mask).
-  const int nb0 = p.causal ? min(n_kv, (row0 + kBlockM + kBlockN - 1) / kBlockN) : n_kv;
-  const int nb1 = p.causal ? min(n_kv, (row0 + 2 * kBlockM + kBlockN - 1) / kBlockN) : n_kv;
+  // Key blocks visited by the 128-row tile starting at row r (0 past S).
+  auto blocks_for = [&](int r) {
+    return r >= S ? 0 : (p.causal ? min(n_kv, (r + kBlockM + kBlockN - 1) / kBlockN) : n_kv);
+  };
+  const int nb0 = blocks_for(row0);
+  const int nb1 = blocks_for(row0 + kBlockM);
+  const int nbp = max(nb0, nb1);  // blocks the CTA loads
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
     for (int s = 0; s < L::kStages; ++s) {
       mbar_init(&bar_kfull[s], 1);
       mbar_init(&bar_vfull[s], 1);
-      mbar_init(&bar_empty[s], 1);
+      mbar_init(&bar_empty[s], 2);  // released by both MMA warps
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bar_sfull[t], 1);
-      mbar_init(&bar_pfull[t], 128);
+      mbar_init(&bar_sfree[t], 4);  // one arrival per softmax warp
+      mbar_init(&bar_pfull[t], 4);
+      mbar_init(&bar_pvdone[t], 1);
       mbar_init(&bar_ofinal[t], 1);
     }
-    mbar_init(bar_drain, 1);
+    mbar_init(&bar_drain[0], 1);
+    mbar_init(&bar_drain[1], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -152,27 +182,33 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
         mbar_arrive_expect_tx(bar_q, 2 * L::kTileBytes);
-  #pragma unroll
+#pragma unroll
         for (int t = 0; t < 2; ++t)
-  #pragma unroll
+#pragma unroll
           for (int ch = 0; ch < L::kChunks; ++ch)
             tma_load_3d(smem + L::kOffQ + t * L::kTileBytes + ch * L::kChunkBytes, &tm_q, bar_q,
                         ch * (L::kRowBytes / 2), row0 + t * kBlockM, bh);
+        // K and V blocks, each as two 64-row half-block copies.
+        constexpr int kHalfBytes = (kBlockN / 2) * L::kRowBytes;
         int it = 0;
-        for (; it < nb1; ++it) {
+        for (; it < nbp; ++it) {
           const int st = it % L::kStages;
           const int use = it / L::kStages;
           if (use > 0 && !mbar_wait(&bar_empty[st], (use - 1) & 1, abort_flag, p.err, kErrTimeoutLoad)) break;
           mbar_arrive_expect_tx(&bar_kfull[st], L::kTileBytes);
-  #pragma unroll
+#pragma unroll
           for (int ch = 0; ch < L::kChunks; ++ch)
-            tma_load_3d(smem + L::kOffK + st * L::kTileBytes + ch * L::kChunkBytes, &tm_k, &bar_kfull[st],
-                        ch * (L::kRowBytes / 2), it * kBlockN, bh);
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+              tma_load_3d(smem + L::kOffK + st * L::kTileBytes + ch * L::kChunkBytes + h * kHalfBytes, &tm_k,
+                          &bar_kfull[st], ch * (L::kRowBytes / 2), it * kBlockN + h * (kBlockN / 2), bh);
           mbar_arrive_expect_tx(&bar_vfull[st], L::kTileBytes);
-  #pragma unroll
+#pragma unroll
           for (int ch = 0; ch < L::kChunks; ++ch)
-            tma_load_3d(smem + L::kOffV + st * L::kTileBytes + ch * L::kChunkBytes, &tm_v, &bar_vfull[st],
-                        ch * (L::kRowBytes / 2), it * kBlockN, bh);
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+              tma_load_3d(smem + L::kOffV + st * L::kTileBytes + ch * L::kChunkBytes + h * kHalfBytes, &tm_v,
+                          &bar_vfull[st], ch * (L::kRowBytes / 2), it * kBlockN + h * (kBlockN / 2), bh);
         }
         // Teardown: every copy this thread started must land before the CTA exits.
         drain_wait(bar_q, 0, p.err);
@@ -182,59 +218,74 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           drain_wait(&bar_vfull[st], (x / L::kStages) & 1, p.err);
         }
       }
-    } else if (warp == 9) {
-      // ------------------------------------------------------------ MMA issuer
-      if (lane == 0) {
-        constexpr uint32_t idesc_qk = make_idesc_f16(BF16, 128, kBlockN, false, false);
-        constexpr uint32_t idesc_pv = make_idesc_f16(BF16, 128, D, false, true);
-        auto qk = [&](int t, int j) {
-          const uint32_t k_addr = sK + (j % L::kStages) * L::kTileBytes;
-          const uint32_t q_addr = sQ + t * L::kTileBytes;
-  #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(tmem + 128u * t, kmajor_desc<D>(q_addr, kk), kmajor_desc<D>(k_addr, kk), idesc_qk,
-                   kk > 0 ? 1u : 0u);
-          mma_commit(&bar_sfull[t]);
-        };
-        auto pv = [&](int t, int j) -> bool {
-          const int st = j % L::kStages;
-          if (!mbar_wait(&bar_pfull[t], j & 1, abort_flag, p.err, kErrTimeoutMma)) return false;
-          if (!mbar_wait(&bar_vfull[st], (j / L::kStages) & 1, abort_flag, p.err, kErrTimeoutMma)) return false;
-          tc_fence_after();
-          const uint32_t v_addr = sV + st * L::kTileBytes;
-  #pragma unroll
-          for (int kk = 0; kk < kBlockN / 16; ++kk)
-            mma_ts(tmem + L::kColO + D * t, tmem + 128u * t + kk * 8, mnmajor_desc<D>(v_addr, kk), idesc_pv,
-                   (j > 0 || kk > 0) ? 1u : 0u);
-          return true;
-        };
-        bool ok = mbar_wait(bar_q, 0, abort_flag, p.err, kErrTimeoutMma);
-        for (int j = 0; ok && j < nb1; ++j) {
-          const int st = j % L::kStages;
-          ok = mbar_wait(&bar_kfull[st], (j / L::kStages) & 1, abort_flag, p.err, kErrTimeoutMma);
-          if (!ok) break;
-          tc_fence_after();
-          if (j >= 1 && j - 1 < nb0) {
-            if (!(ok = pv(0, j - 1))) break;
-            if (j - 1 == nb0 - 1) mma_commit(&bar_ofinal[0]);
-          }
-          if (j < nb0) qk(0, j);
-          if (j >= 1) {
-            if (!(ok = pv(1, j - 1))) break;
-            mma_commit(&bar_empty[(j - 1) % L::kStages]);
-          }
-          qk(1, j);
+    } else if (warp == 9 || warp == 10) {
+      // ------------------------------------------------------------ MMA issuers
+      // Warp 9 issues tile 0's MMAs, warp 10 tile 1's, so one warp's commits
+      // and barrier waits overlap the other's MMAs.  Each warp runs its code
+      // converged and one elected lane issues each MMA; descriptors are built
+      // once per stage and advanced by compile-time offsets.
+      const int t = warp - 9;
+      const int nbt = t == 0 ? nb0 : nb1;
+      constexpr uint32_t idesc_qk = make_idesc_f16(BF16, 128, kBlockN, false, false);
+      constexpr uint32_t idesc_pv = make_idesc_f16(BF16, 128, D, false, true);
+      const uint64_t q_desc = make_sdesc(sQ + t * L::kTileBytes, 16, 8 * L::kRowBytes, L::kSwz);
+      // S_t = Q_t K(j)^T; with separate P, first wait until the warpgroup has loaded S_t(j-1).
+      auto qk = [&](int j) -> bool {
+        if (L::kSepP && j > 0 && !warp_wait(&bar_sfree[t], (j - 1) & 1, abort_flag, p.err, kErrTimeoutMma))
+          return false;
+        tc_fence_after();
+        const uint64_t k_desc =
+            make_sdesc(sK + (j % L::kStages) * L::kTileBytes, 16, 8 * L::kRowBytes, L::kSwz);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss_warp(tmem + L::kColS + 128u * t, desc_plus(q_desc, kmajor_step_bytes<D>(kk)),
+                      desc_plus(k_desc, kmajor_step_bytes<D>(kk)), idesc_qk, kk > 0 ? 1u : 0u);
+        mma_commit_warp(&bar_sfull[t]);
+        return true;
+      };
+      // O_t += P_t(j) V(j) once P_t(j) is stored and O_t rescaled.
+      auto pv = [&](int j) -> bool {
+        const int st = j % L::kStages;
+        if (!warp_wait(&bar_pfull[t], j & 1, abort_flag, p.err, kErrTimeoutMma)) return false;
+        if (!warp_wait(&bar_vfull[st], (j / L::kStages) & 1, abort_flag, p.err, kErrTimeoutMma)) return false;
+        tc_fence_after();
+        const uint64_t v_desc = make_sdesc(sV + st * L::kTileBytes, L::kChunkBytes, 8 * L::kRowBytes, L::kSwz);
+        const uint32_t t_p = tmem + L::kColP + L::kStrideP * t;
+#pragma unroll
+        for (int kk = 0; kk < kBlockN / 16; ++kk)
+          mma_ts_warp(tmem + L::kColO + D * t, t_p + kk * 8, desc_plus(v_desc, mnmajor_step_bytes<D>(kk)), idesc_pv,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+        if (L::kSepP) mma_commit_warp(&bar_pvdone[t]);
+        if (j == nbt - 1) mma_commit_warp(&bar_ofinal[t]);
+        return true;
+      };
+      // This warp is done with block x once V(x) has landed and its MMAs on
+      // K(x), V(x) are issued: it releases the stage.
+      auto release = [&](int x) -> bool {
+        const int st = x % L::kStages;
+        if (!warp_wait(&bar_vfull[st], (x / L::kStages) & 1, abort_flag, p.err, kErrTimeoutMma)) return false;
+        mma_commit_warp(&bar_empty[st]);
+        return true;
+      };
+      bool ok = warp_wait(bar_q, 0, abort_flag, p.err, kErrTimeoutMma);
+      for (int j = 0; ok && j < nbp; ++j) {
+        ok = warp_wait(&bar_kfull[j % L::kStages], (j / L::kStages) & 1, abort_flag, p.err, kErrTimeoutMma);
+        if (!ok) break;
+        tc_fence_after();
+        if (L::kSepP) {  // S_t(j) first, then O_t += P_t(j-1) V(j-1)
+          if (j < nbt && !(ok = qk(j))) break;
+          if (j >= 1 && j - 1 < nbt && !(ok = pv(j - 1))) break;
+        } else {  // P_t(j-1) lives in S_t: its P V must precede S_t(j)
+          if (j >= 1 && j - 1 < nbt && !(ok = pv(j - 1))) break;
+          if (j < nbt && !(ok = qk(j))) break;
         }
-        if (ok && nb0 == nb1) {
-          ok = pv(0, nb0 - 1);
-          if (ok) mma_commit(&bar_ofinal[0]);
-        }
-        if (ok && pv(1, nb1 - 1)) mma_commit(&bar_ofinal[1]);
-        // Teardown: wait for every MMA this thread issued.
-        mma_commit(bar_drain);
-        drain_wait(bar_drain, 0, p.err);
+        if (j >= 1 && !(ok = release(j - 1))) break;
       }
-      __syncwarp();
+      if (ok && nbp - 1 < nbt) ok = pv(nbp - 1);
+      if (ok) release(nbp - 1);
+      // Teardown: wait for every MMA this warp issued.
+      mma_commit_warp(&bar_drain[t]);
+      drain_wait(&bar_drain[t], 0, p.err);
     }
   } else {
     regs_increase<kRegsHigh>();
@@ -245,130 +296,131 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const int row_g = tile_row0 + r;
     const int nb = t == 0 ? nb0 : nb1;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t t_s = tmem + lane_base + 128u * t;
+    const uint32_t t_s = tmem + lane_base + L::kColS + 128u * t;
+    const uint32_t t_p = tmem + lane_base + L::kColP + L::kStrideP * t;
     const uint32_t t_o = tmem + lane_base + L::kColO + D * t;
     const float sl2 = p.scale_log2;
     const float2 c2 = make_float2(sl2, sl2);
-    // last visible key of this row
-    const int last = p.causal ? min(S - 1, row_g) : S - 1;
+    const int last = p.causal ? min(S - 1, row_g) : S - 1;  // last visible key of this row
     float m = -INFINITY;  // running (possibly stale) maximum, base-2 scaled
     float l = 0.f;
     bool alive = true;
-    for (int j = 0; j < nb; ++j) {
-      if (!warp_wait(&bar_sfull[t], j & 1, abort_flag, p.err, kErrTimeoutSoftmax)) {
-        alive = false;
-        break;
-      }
-      tc_fence_after();
+    for (int j = 0; j < nb && alive; ++j) {
       uint32_t sr[kBlockN];
-      tmem_ld128(t_s, sr);
-      const int kv0 = j * kBlockN;
-      // Masked blocks: the diagonal block under the causal mask, and a
-      // ragged last key block.
-      const bool masked = (kv0 + kBlockN > S) || (p.causal && kv0 + kBlockN - 1 > tile_row0);
-      float mx;
-      if (!masked) {
-        float a = __uint_as_float(sr[0]), b = __uint_as_float(sr[1]);
-        if (sl2 >= 0.f) {
-#pragma unroll
-          for (int c = 2; c < kBlockN - 2; c += 4) {
-            a = max3(a, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
-            b = max3(b, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
-          }
-          mx = max3(a, b, fmaxf(__uint_as_float(sr[kBlockN - 2]), __uint_as_float(sr[kBlockN - 1])));
-        } else {  // a negative scale turns the largest scaled score into the smallest raw one
-#pragma unroll
-          for (int c = 2; c < kBlockN - 2; c += 4) {
-            a = min3(a, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
-            b = min3(b, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
-          }
-          mx = min3(a, b, fminf(__uint_as_float(sr[kBlockN - 2]), __uint_as_float(sr[kBlockN - 1])));
-        }
-      } else {
-        mx = sl2 >= 0.f ? -INFINITY : INFINITY;
-#pragma unroll
-        for (int c = 0; c < kBlockN; ++c) {
-          const float x = __uint_as_float(sr[c]);
-          if (kv0 + c <= last) mx = sl2 >= 0.f ? fmaxf(mx, x) : fminf(mx, x);
-        }
-      }
-      // A block with no visible key for this row (only rows past S) contributes nothing.
-      const float m_blk = (kv0 > last) ? -INFINITY : mx * sl2;
-      float alpha = 1.f;
+      bool masked = false;
       bool upd = false;
-      if (j == 0) {
-        m = m_blk;
-      } else if (m_blk > m + kTau) {
-        alpha = ex2(m - m_blk);
-        m = m_blk;
-        upd = true;
-      }
-      if (__any_sync(0xffffffffu, upd)) {
-        // O holds the blocks before j, relative to the old m.  The commit
-        // that signalled S(j) also covers the earlier P V MMA, so O is final.
-        l *= alpha;
+      float alpha = 1.f;
+      if (alive && !warp_wait(&bar_sfull[t], j & 1, abort_flag, p.err, kErrTimeoutSoftmax)) alive = false;
+      if (alive) {
+        tc_fence_after();
+        tmem_ld128(t_s, sr);
+        if (L::kSepP) warp_arrive(&bar_sfree[t]);  // S_t(j) is in registers: the MMA may overwrite it
+        const int kv0 = j * kBlockN;
+        // Masked blocks: the diagonal block under the causal mask, and a
+        // ragged last key block.
+        masked = (kv0 + kBlockN > S) || (p.causal && kv0 + kBlockN - 1 > tile_row0);
+        float mx;
+        if (!masked) {
+          // Eight independent chains of 3-input max/min keep the dependency depth short.
+          float mc[8];
+          if (sl2 >= 0.f) {
 #pragma unroll
-        for (int c = 0; c < D; c += 16) {
-          uint32_t o16[16];
-          tmem_ld16(t_o + c, o16);
+            for (int k = 0; k < 8; ++k) {
+              const uint32_t* v = sr + 16 * k;
+              float a = max3(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
 #pragma unroll
-          for (int i = 0; i < 16; i += 2) {
-            const float2 v = __fmul2_rn(make_float2(__uint_as_float(o16[i]), __uint_as_float(o16[i + 1])),
-                                        make_float2(alpha, alpha));
-            o16[i] = __float_as_uint(v.x);
-            o16[i + 1] = __float_as_uint(v.y);
+              for (int c = 3; c < 15; c += 2) a = max3(a, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
+              mc[k] = fmaxf(a, __uint_as_float(v[15]));
+            }
+            mx = max3(max3(mc[0], mc[1], mc[2]), max3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7]));
+          } else {  // a negative scale turns the largest scaled score into the smallest raw one
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const uint32_t* v = sr + 16 * k;
+              float a = min3(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
+#pragma unroll
+              for (int c = 3; c < 15; c += 2) a = min3(a, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
+              mc[k] = fminf(a, __uint_as_float(v[15]));
+            }
+            mx = min3(min3(mc[0], mc[1], mc[2]), min3(mc[3], mc[4], mc[5]), fminf(mc[6], mc[7]));
           }
-          tmem_st16(t_o + c, o16);
+        } else {
+          mx = sl2 >= 0.f ? -INFINITY : INFINITY;
+#pragma unroll
+          for (int c = 0; c < kBlockN; ++c) {
+            const float x = __uint_as_float(sr[c]);
+            if (kv0 + c <= last) mx = sl2 >= 0.f ? fmaxf(mx, x) : fminf(mx, x);
+          }
+        }
+        // A block with no visible key for this row (only rows past S) contributes nothing.
+        const float m_blk = (kv0 > last) ? -INFINITY : mx * sl2;
+        if (j == 0) {
+          m = m_blk;
+        } else if (m_blk > m + kTau) {
+          alpha = ex2(m - m_blk);
+          m = m_blk;
+          upd = true;
         }
       }
-      const float m_use = (m == -INFINITY) ? 0.f : m;
-      const float2 negm = make_float2(-m_use, -m_use);
-      float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-      // P (16-bit) overwrites the first 64 columns of this tile's S, 16 columns
-      // (32 scores) at a time, so only the S row itself stays live in registers.
-      if (!masked) {
+      if (alive) {
+        const int kv0 = j * kBlockN;
+        const float m_use = (m == -INFINITY) ? 0.f : m;
+        const float2 negm = make_float2(-m_use, -m_use);
+        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                         make_float2(0.f, 0.f)};
+        uint32_t pk[kBlockN / 2];
+        if (!masked) {
 #pragma unroll
-        for (int c0 = 0; c0 < kBlockN; c0 += 32) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int c = c0; c < c0 + 32; c += 4) {
-            const float2 y0 =
-                __ffma2_rn(make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), c2, negm);
-            const float2 y1 =
-                __ffma2_rn(make_float2(__uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3])), c2, negm);
-            const float2 e0 = make_float2(ex2(y0.x), ex2(y0.y));
-            const float2 e1 = make_float2(ex2(y1.x), ex2(y1.y));
-            acc0 = __fadd2_rn(acc0, e0);
-            acc1 = __fadd2_rn(acc1, e1);
-            pk[(c - c0) / 2] = pack2<BF16>(e0.x, e0.y);
-            pk[(c - c0) / 2 + 1] = pack2<BF16>(e1.x, e1.y);
+          for (int c = 0; c < kBlockN; c += 2) {
+            const float2 y = __ffma2_rn(make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), c2, negm);
+            const float2 e = make_float2(ex2(y.x), ex2(y.y));
+            acc[(c / 2) & 3] = __fadd2_rn(acc[(c / 2) & 3], e);
+            pk[c / 2] = pack2<BF16>(e.x, e.y);
           }
-          tmem_st16(t_s + c0 / 2, pk);
-        }
-      } else {
+        } else {
 #pragma unroll
-        for (int c0 = 0; c0 < kBlockN; c0 += 32) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int c = c0; c < c0 + 32; c += 2) {
-            const float2 y =
-                __ffma2_rn(make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), c2, negm);
+          for (int c = 0; c < kBlockN; c += 2) {
+            const float2 y = __ffma2_rn(make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), c2, negm);
             const float e0 = (kv0 + c <= last) ? ex2(y.x) : 0.f;
             const float e1 = (kv0 + c + 1 <= last) ? ex2(y.y) : 0.f;
-            acc0 = __fadd2_rn(acc0, make_float2(e0, e1));
-            pk[(c - c0) / 2] = pack2<BF16>(e0, e1);
+            acc[(c / 2) & 3] = __fadd2_rn(acc[(c / 2) & 3], make_float2(e0, e1));
+            pk[c / 2] = pack2<BF16>(e0, e1);
           }
-          tmem_st16(t_s + c0 / 2, pk);
         }
+        const float2 accs = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+        l = l * alpha + (accs.x + accs.y);
+        // With separate P, P_t(j-1) V(j-1) must be done before P_t is rewritten
+        // and before O_t is rescaled.  (With P over S, S_t(j) being ready already
+        // implies it: its commit covers the earlier P V.)
+        if (L::kSepP && j > 0 && !warp_wait(&bar_pvdone[t], (j - 1) & 1, abort_flag, p.err, kErrTimeoutSoftmax)) {
+          alive = false;
+          break;
+        }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, upd)) {
+          // O holds the blocks before j relative to the old m: rescale this warp's rows.
+#pragma unroll
+          for (int c = 0; c < D; c += 16) {
+            uint32_t o16[16];
+            tmem_ld16(t_o + c, o16);
+#pragma unroll
+            for (int i = 0; i < 16; i += 2) {
+              const float2 v = __fmul2_rn(make_float2(__uint_as_float(o16[i]), __uint_as_float(o16[i + 1])),
+                                          make_float2(alpha, alpha));
+              o16[i] = __float_as_uint(v.x);
+              o16[i + 1] = __float_as_uint(v.y);
+            }
+            tmem_st16(t_o + c, o16);
+          }
+        }
+        tmem_st32(t_p, pk);
+        tmem_st32(t_p + 32, pk + 32);
+        tmem_st_wait();
+        warp_arrive(&bar_pfull[t]);
       }
-      const float2 acc = __fadd2_rn(acc0, acc1);
-      l += acc.x + acc.y;
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&bar_pfull[t]);
     }
     // ------------------------------------------------------------ epilogue
-    if (alive && warp_wait(&bar_ofinal[t], 0, abort_flag, p.err, kErrTimeoutSoftmax)) {
+    if (alive && nb > 0 && warp_wait(&bar_ofinal[t], 0, abort_flag, p.err, kErrTimeoutSoftmax)) {
       tc_fence_after();
       const float inv_l = 1.f / l;
       const bool row_ok = row_g < S;

@@ -30,17 +30,19 @@ struct BwdParams {
   void* dv;            // [BH, S, D]
   int S;
   int BH;
-  int n_tiles;         // ceil(S / 128)
+  int n_tiles;         // ceil(S / 128): own tiles per (b, h)
+  int n_partner;       // ceil(S / 64): streamed partner blocks per (b, h)
   int causal;
   float scale;         // softmax scale (dQ, dK factor)
   float scale_log2;    // scale * log2(e)
   int* err;            // device error word
 };
 
-// Tensor maps for one [BH, S, D] 16-bit tensor viewed as 3-D {D, S, BH},
-// box {row_bytes / 2, 128, 1} with the swizzle matching row_bytes.
-struct TensorMaps3 {
-  CUtensorMap a, b, c;
+// Tensor maps of the backward's four inputs, each viewed as 3-D {D, S, BH}:
+// 128-row boxes for a CTA's resident tiles, 64-row boxes for streamed blocks.
+struct BwdMaps {
+  CUtensorMap q128, k128, v128, do128;
+  CUtensorMap q64, k64, v64, do64;
 };
 
 // Launchers (one per kernel family); they dispatch on D and dtype.
@@ -48,10 +50,8 @@ cudaError_t launch_fwd(int D, bool bf16, const CUtensorMap& tq, const CUtensorMa
                        const FwdParams& p, int BH, cudaStream_t stream);
 
 cudaError_t launch_bwd_preprocess(int D, bool bf16, const BwdParams& p, cudaStream_t stream);
-cudaError_t launch_bwd_dkdv(int D, bool bf16, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream);
-cudaError_t launch_bwd_dq(int D, bool bf16, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                          const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream);
+cudaError_t launch_bwd_dkdv(int D, bool bf16, const BwdMaps& maps, const BwdParams& p, cudaStream_t stream);
+cudaError_t launch_bwd_dq(int D, bool bf16, const BwdMaps& maps, const BwdParams& p, cudaStream_t stream);
 
 // Address of this process's device error word on the current device.
 int* device_error_word();

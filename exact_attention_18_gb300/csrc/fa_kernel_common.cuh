@@ -10,22 +10,22 @@
 
 namespace fa {
 
-// A [128, D] tile of 16-bit elements as TMA writes it: `kChunks` column
-// chunks of 128 rows x kRowBytes, each swizzled at kRowBytes granularity.
-template <int D>
+// A [ROWS, D] tile of 16-bit elements as TMA writes it: `kChunks` column
+// chunks of ROWS rows x kRowBytes, each swizzled at kRowBytes granularity.
+template <int D, int ROWS = 128>
 struct TileGeom {
   static constexpr int kRowBytes = D * 2 < 128 ? D * 2 : 128;
   static constexpr int kChunks = D * 2 / kRowBytes;
-  static constexpr int kChunkBytes = 128 * kRowBytes;
-  static constexpr int kTileBytes = 128 * D * 2;
+  static constexpr int kChunkBytes = ROWS * kRowBytes;
+  static constexpr int kTileBytes = ROWS * D * 2;
   static constexpr uint32_t kSwz = ptx::swizzle_code_for(kRowBytes);
 };
 
 // Operand descriptor for K-step kk (16 elements along D) of a tile read
 // K-major (rows = M or N, D contiguous).
-template <int D>
+template <int D, int ROWS = 128>
 __device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile_addr, int kk) {
-  using G = TileGeom<D>;
+  using G = TileGeom<D, ROWS>;
   const int off = kk * 32;
   return ptx::make_sdesc(tile_addr + (off / G::kRowBytes) * G::kChunkBytes + (off % G::kRowBytes), 16,
                          8 * G::kRowBytes, G::kSwz);
@@ -33,11 +33,26 @@ __device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile_addr, int kk) {
 
 // Operand descriptor for K-step kk (tile rows 16kk..16kk+15) of a tile read
 // MN-major (the tile's D columns are the N dimension, its rows the K dimension).
-template <int D>
+template <int D, int ROWS = 128>
 __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile_addr, int kk) {
-  using G = TileGeom<D>;
+  using G = TileGeom<D, ROWS>;
   return ptx::make_sdesc(tile_addr + kk * 16 * G::kRowBytes, G::kChunkBytes, 8 * G::kRowBytes, G::kSwz);
 }
+
+// Byte offset of K-step kk inside a K-major tile (added to a base descriptor's
+// start-address field as offset >> 4).
+template <int D, int ROWS = 128>
+__host__ __device__ constexpr uint32_t kmajor_step_bytes(int kk) {
+  using G = TileGeom<D, ROWS>;
+  return static_cast<uint32_t>(((kk * 32) / G::kRowBytes) * G::kChunkBytes + (kk * 32) % G::kRowBytes);
+}
+// Byte offset of K-step kk (16 tile rows) inside an MN-major tile.
+template <int D>
+__host__ __device__ constexpr uint32_t mnmajor_step_bytes(int kk) {
+  return static_cast<uint32_t>(kk * 16 * TileGeom<D>::kRowBytes);
+}
+// A descriptor advanced by `bytes` (start address is in 16-byte units in the low bits).
+__device__ __forceinline__ uint64_t desc_plus(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
 
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
@@ -73,6 +88,11 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, int* 
 // Named barrier among the `nthreads` threads (a multiple of 32) that use `id`.
 __device__ __forceinline__ void named_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Arrive at named barrier `id` (counted among `nthreads`) without waiting.
+__device__ __forceinline__ void named_arrive(int id, int nthreads) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // Barrier over `nthreads` threads with id `id` that also returns the AND of
