@@ -24,15 +24,19 @@
 //   X = A1 B1^T,  Y = A2 B2^T
 //     dK/dV pass: A1 = K, A2 = V, B1 = Q_i, B2 = dO_i -> X = S^T, Y = dP^T
 //     dQ pass:    A1 = Q, A2 = dO, B1 = K_j, B2 = V_j -> X = S,   Y = dP
-// so TMEM lane = the CTA's own row (key or query).  Eight softmax-gradient
-// warps turn X, Y into P and dS (16-bit, written back into TMEM over X and Y);
-// warp w owns TMEM lanes 32(w%4).. and the 32 partner columns 32(w/4)...  The
-// MMA warp then accumulates, with A read from TMEM:
+// so TMEM lane = the CTA's own row (key or query).  Sixteen softmax-gradient
+// warps in two groups of eight turn X, Y into P and dS (16-bit, written back
+// into TMEM over X and Y); group g takes the blocks i with i mod 2 = g, and in
+// a group warp w owns TMEM lanes 32(w%4).. and partner columns 32((w/4)%2)...
+// The MMA warp then accumulates, with A read from TMEM:
 //     dK/dV pass: dV += P^T dO_i,  dK += dS^T Q_i    (B = B2, B1 read MN-major)
 //     dQ pass:    dQ += dS K_j                       (B = B1 read MN-major)
-// X and Y are double-buffered (two 128-column TMEM buffers), and the MMA
-// warp issues X,Y(i+1) before the accumulation of block i, so the tensor core
-// works on the next block while the warps turn the current one into P and dS.
+// Each group has its own 128-column TMEM buffer for X and Y, and the MMA warp
+// issues X,Y(i+1) before the accumulation of block i, so while one group
+// works on block i the other works on block i+1 and the tensor core on the
+// products of a third.  In the dK/dV pass the producer warp also copies the
+// block's L and Delta (one value per partner query) into the stage with
+// cp.async, completing on the same barrier as the block's tiles.
 #include "fa_kernel_common.cuh"
 
 namespace fa {
@@ -81,7 +85,10 @@ __global__ void __launch_bounds__(256) fa_bwd_preprocess_kernel(const BwdParams 
 namespace {
 
 constexpr int kPartnerRows = 64;  // rows of a streamed B tile
-constexpr int kBwdThreads = 320;  // 8 softmax-gradient warps, producer, MMA
+constexpr int kBwdGroups = 2;     // softmax-gradient groups of 8 warps; group g takes blocks i = g mod 2
+constexpr int kProducerWarp = 8 * kBwdGroups;
+constexpr int kMmaWarp = kProducerWarp + 1;
+constexpr int kBwdThreads = (kMmaWarp + 1) * 32;
 
 template <int D>
 struct BwdLayout {
@@ -90,17 +97,17 @@ struct BwdLayout {
   static constexpr int kStages = 4;
   static constexpr int kOffA1 = 0;
   static constexpr int kOffA2 = kOffA1 + GA::kTileBytes;
-  static constexpr int kOffB1 = kOffA2 + GA::kTileBytes;                // [kStages] tiles
-  static constexpr int kOffB2 = kOffB1 + kStages * GB::kTileBytes;      // [kStages] tiles
-  static constexpr int kOffRowVec = kOffB2 + kStages * GB::kTileBytes;  // [2 buffers][L2, Delta][64] fp32
-  static constexpr int kOffBar = kOffRowVec + 2 * 2 * kPartnerRows * 4;
+  static constexpr int kOffB1 = kOffA2 + GA::kTileBytes;             // [kStages] tiles
+  static constexpr int kOffB2 = kOffB1 + kStages * GB::kTileBytes;   // [kStages] tiles
+  static constexpr int kOffVec = kOffB2 + kStages * GB::kTileBytes;  // [kStages][L, Delta][64] fp32
+  static constexpr int kOffBar = kOffVec + kStages * 2 * kPartnerRows * 4;
   // a_full, b_full[S], empty[S], xy_full[2], p_full[2], acc_final, drain
   static constexpr int kNumBars = 1 + 2 * kStages + 4 + 2;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemUsed = kOffMisc + 16;
   static constexpr int kSmemBytes = (kSmemUsed + 1024) > 116 * 1024 ? (kSmemUsed + 1024) : 116 * 1024;
   static constexpr uint32_t kTmemCols = 512;
-  // Buffer b: X at column 128 b, Y at 128 b + 64 (64 fp32 columns each).
+  // Group g's buffer: X at column 128 g, Y at 128 g + 64 (64 fp32 columns each).
   static constexpr uint32_t kColAcc1 = 256;      // dV (dK/dV pass) or dQ
   static constexpr uint32_t kColAcc2 = 256 + D;  // dK (dK/dV pass)
 };
@@ -122,6 +129,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   using GB = typename L::GB;
   using elem_t = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
   constexpr int kPN = kPartnerRows;
+  constexpr float kLog2e = 1.4426950408889634f;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -135,7 +143,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint64_t* bar_drain = bar_accfinal + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 4);
-  float* rowvec = reinterpret_cast<float*>(smem + L::kOffRowVec);
+  float* vecs = reinterpret_cast<float*>(smem + L::kOffVec);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -143,6 +151,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int S = p.S;
   const int nt = p.n_tiles;
   const int np = p.n_partner;
+  const int64_t rowbase = static_cast<int64_t>(bh) * S;
   // Own tile; heavy tiles first under the causal mask (key tile 0 and query
   // tile nt-1 see the most partners).
   const int own = KV_OUTER ? static_cast<int>(blockIdx.y)
@@ -155,19 +164,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(bar_afull, 1);
     for (int s = 0; s < L::kStages; ++s) {
-      mbar_init(&bar_bfull[s], 1);
+      // dK/dV pass: the producer's TMA arrival plus one cp.async arrival per
+      // producer lane for the block's L and Delta vectors.
+      mbar_init(&bar_bfull[s], KV_OUTER ? 33 : 1);
       mbar_init(&bar_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bar_xyfull[b], 1);
-      mbar_init(&bar_pfull[b], 8);  // one arrival per softmax-gradient warp
+      mbar_init(&bar_pfull[b], 8);  // one arrival per warp of the group
     }
     mbar_init(bar_accfinal, 1);
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == kMmaWarp) {
     tmem_alloc(tmem_slot, L::kTmemCols);
     tmem_relinquish();
   }
@@ -180,8 +191,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t sB1 = smem_u32(smem + L::kOffB1);
   const uint32_t sB2 = smem_u32(smem + L::kOffB2);
 
-  if (warp == 8) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
+    // Lane 0 issues the TMA copies; in the dK/dV pass every lane also copies
+    // two entries of the block's L and Delta vectors (queries past S read 0:
+    // their Q and dO rows are zero-filled, so P dO and dS vanish there).
     if (lane == 0) {
       prefetch_tmap(&tm_a1);
       prefetch_tmap(&tm_a2);
@@ -193,12 +207,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tma_load_3d(smem + L::kOffA1 + ch * GA::kChunkBytes, &tm_a1, bar_afull, ch * (GA::kRowBytes / 2), own0, bh);
         tma_load_3d(smem + L::kOffA2 + ch * GA::kChunkBytes, &tm_a2, bar_afull, ch * (GA::kRowBytes / 2), own0, bh);
       }
-      int it = 0;
-      for (; it < niter; ++it) {
-        const int st = it % L::kStages;
-        const int use = it / L::kStages;
-        if (use > 0 && !mbar_wait(&bar_empty[st], (use - 1) & 1, abort_flag, p.err, kErrTimeoutLoad)) break;
-        const int r0 = (first + it) * kPN;
+    }
+    int it = 0;
+    for (; it < niter; ++it) {
+      const int st = it % L::kStages;
+      const int use = it / L::kStages;
+      if (use > 0 && !warp_wait(&bar_empty[st], (use - 1) & 1, abort_flag, p.err, kErrTimeoutLoad)) break;
+      const int r0 = (first + it) * kPN;
+      if (lane == 0) {
         mbar_arrive_expect_tx(&bar_bfull[st], 2 * GB::kTileBytes);
 #pragma unroll
         for (int ch = 0; ch < GB::kChunks; ++ch) {
@@ -208,11 +224,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                       ch * (GB::kRowBytes / 2), r0, bh);
         }
       }
-      drain_wait(bar_afull, 0, p.err);
-      for (int x = (it > L::kStages ? it - L::kStages : 0); x < it; ++x)
-        drain_wait(&bar_bfull[x % L::kStages], (x / L::kStages) & 1, p.err);
+      if constexpr (KV_OUTER) {
+        float* v = vecs + st * 2 * kPN;
+#pragma unroll
+        for (int h = 0; h < kPN; h += 32) {
+          const int q = r0 + h + lane;
+          const int64_t src = rowbase + (q < S ? q : S - 1);
+          cp_async_4(v + h + lane, p.lse + src, q < S);
+          cp_async_4(v + kPN + h + lane, p.delta + src, q < S);
+        }
+        cp_async_mbar_arrive(&bar_bfull[st]);
+      }
     }
-  } else if (warp == 9) {
+    // Teardown: every copy issued must land before the CTA exits.
+    if (lane == 0) drain_wait(bar_afull, 0, p.err);
+    for (int x = (it > L::kStages ? it - L::kStages : 0); x < it; ++x)
+      drain_wait(&bar_bfull[x % L::kStages], (x / L::kStages) & 1, p.err);
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     // The whole warp runs this code converged and one elected lane issues
     // each MMA; descriptors are built once per stage and advanced by
@@ -221,9 +249,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     constexpr uint32_t idesc_acc = make_idesc_f16(BF16, 128, D, false, true);
     const uint64_t a1_desc = make_sdesc(sA1, 16, 8 * GA::kRowBytes, GA::kSwz);
     const uint64_t a2_desc = make_sdesc(sA2, 16, 8 * GA::kRowBytes, GA::kSwz);
-    // X, Y of block i into buffer i & 1.  The buffer was last read by the
-    // accumulation of block i - 2, issued earlier by this warp; the tensor
-    // core runs one CTA's MMAs in issue order.
+    // X, Y of block i into buffer i & 1 (group i & 1's).  The buffer was last
+    // read by the accumulation of block i - 2, issued earlier by this warp;
+    // the tensor core runs one CTA's MMAs in issue order.
     auto xy = [&](int i) {
       const int st = i % L::kStages;
       const uint32_t tb = tmem + 128u * (i & 1);
@@ -276,16 +304,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mma_commit_warp(bar_drain);
     drain_wait(bar_drain, 0, p.err);
   } else {
-    // ------------------------------------------------------------ softmax-gradient warps 0-7
-    const int q4 = warp & 3;      // TMEM lane quarter
-    const int hf = warp >> 2;     // which 32 of the 64 partner columns
+    // ------------------------------------------------------------ softmax-gradient warps 0-15
+    // Group g = warp / 8 turns blocks g, g + 2, ... into P and dS, so two
+    // blocks are in this stage at once while the tensor core works on a
+    // third.  In a group, warp w owns TMEM lanes 32 (w % 4).. and partner
+    // columns 32 ((w / 4) % 2)...
+    const int g = warp >> 3;
+    const int q4 = warp & 3;
+    const int hf = (warp >> 2) & 1;
     const int col0 = 32 * hf;
     const int my = own0 + q4 * 32 + lane;  // key index (dK/dV pass) or query index (dQ pass)
     const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
     const float sl2 = p.scale_log2;
     const float2 c2 = make_float2(sl2, sl2);
-    constexpr float kLog2e = 1.4426950408889634f;
-    const int64_t rowbase = static_cast<int64_t>(bh) * S;
     // dQ pass: this thread's query row owns its L2 = L * log2 e and Delta
     // (rows past S: L2 = +inf, so their probabilities are exactly 0).
     float my_l2 = INFINITY, my_delta = 0.f;
@@ -293,93 +324,76 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       my_l2 = p.lse[rowbase + my] * kLog2e;
       my_delta = p.delta[rowbase + my];
     }
-    // dK/dV pass: threads 0-63 fetch L2 of the block's 64 query columns and
-    // threads 64-127 their Delta, one block ahead, so the global-load latency
-    // overlaps the previous block's work.  Queries past S get L2 = +inf.
-    auto fetch_colvec = [&](int i) -> float {
-      const int q = (first + i) * kPN + (threadIdx.x & (kPN - 1));
-      if (i >= niter || q >= S) return threadIdx.x < kPN ? INFINITY : 0.f;
-      return threadIdx.x < kPN ? p.lse[rowbase + q] * kLog2e : p.delta[rowbase + q];
-    };
-    float colv = 0.f;
-    if (KV_OUTER && threadIdx.x < 2 * kPN) colv = fetch_colvec(0);
     bool alive = true;
-    for (int i = 0; i < niter; ++i) {
-      const int b = i & 1;
+    for (int i = g; i < niter; i += kBwdGroups) {
+      const int st = i % L::kStages;
       const int partner0 = (first + i) * kPN;
-      float* l2v = rowvec + b * 2 * kPN;
-      float* dlv = l2v + kPN;
-      if constexpr (KV_OUTER) {
-        // Buffer b was last read two blocks ago, before the previous block's barrier.
-        if (threadIdx.x < 2 * kPN) {
-          l2v[threadIdx.x] = colv;  // l2v and dlv are contiguous: [L2 x 64][Delta x 64]
-          colv = fetch_colvec(i + 1);
-        }
-      }
-      // One barrier over the 256 threads publishes the column vectors and
-      // makes the outcome of the wait uniform, so no thread is ever left
-      // waiting at a barrier that the others have abandoned.
-      const bool got = mbar_wait(&bar_xyfull[b], (i >> 1) & 1, abort_flag, p.err, kErrTimeoutSoftmax);
-      if (!named_sync_and(1, 256, got)) {
+      bool ok = true;
+      if constexpr (KV_OUTER) ok = warp_wait(&bar_bfull[st], (i / L::kStages) & 1, abort_flag, p.err, kErrTimeoutSoftmax);
+      ok = ok && warp_wait(&bar_xyfull[g], (i >> 1) & 1, abort_flag, p.err, kErrTimeoutSoftmax);
+      if (!ok) {
         alive = false;
         break;
       }
       tc_fence_after();
-      const uint32_t tX = tmem + lane_base + 128u * b + col0;
+      const uint32_t tX = tmem + lane_base + 128u * g + col0;
       const uint32_t tY = tX + 64;
-      uint32_t xs[32], ys[32];
-      tmem_ld32(tX, xs);
-      tmem_ld32(tY, ys);
-      // Masked blocks: partner rows that cross the diagonal under the causal
-      // mask, and blocks that run past S.
-      const bool masked = (partner0 + kPN > S) ||
-                          (p.causal && (KV_OUTER ? partner0 < own0 + 128 : partner0 + kPN - 1 > own0));
-      uint32_t pk[16], dk[16];
+      const float* lv = vecs + st * 2 * kPN + col0;  // L of this warp's 32 partner queries (dK/dV pass)
+      const float* dv = lv + kPN;                    // and their Delta
+      // Diagonal blocks under the causal mask: the dK/dV pass zeroes partner
+      // column c where query partner0 + col0 + c < key `my`, the dQ pass where
+      // key partner0 + col0 + c > query `my`.  Rows and columns past S need no
+      // mask: their zero-filled operands make their terms vanish (see above).
+      const bool diag = p.causal && (KV_OUTER ? partner0 < own0 + 128 : partner0 + kPN - 1 > own0);
+      const int lim = my - partner0 - col0;
 #pragma unroll
-      for (int c = 0; c < 32; c += 2) {
-        float2 l2, dl;
-        if constexpr (KV_OUTER) {
-          l2 = make_float2(l2v[col0 + c], l2v[col0 + c + 1]);
-          dl = make_float2(dlv[col0 + c], dlv[col0 + c + 1]);
-        } else {
-          l2 = make_float2(my_l2, my_l2);
-          dl = make_float2(my_delta, my_delta);
-        }
-        const float2 y = __ffma2_rn(make_float2(__uint_as_float(xs[c]), __uint_as_float(xs[c + 1])), c2,
-                                    make_float2(-l2.x, -l2.y));
-        float2 pr = make_float2(ex2(y.x), ex2(y.y));
-        if (masked) {
-          const int other = partner0 + col0 + c;
+      for (int h = 0; h < 2; ++h) {
+        uint32_t xs[16], ys[16];
+        tmem_ld16x2(tX + 16 * h, xs, tY + 16 * h, ys);
+        uint32_t pk[8], dk[8];
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int key = KV_OUTER ? my : other + u;
-            const int qry = KV_OUTER ? other + u : my;
-            if ((p.causal && key > qry) || key >= S || qry >= S) (u == 0 ? pr.x : pr.y) = 0.f;
+        for (int c = 0; c < 16; c += 2) {
+          const int cc = 16 * h + c;
+          float2 nl2, dl;
+          if constexpr (KV_OUTER) {
+            nl2 = __fmul2_rn(make_float2(lv[cc], lv[cc + 1]), make_float2(-kLog2e, -kLog2e));
+            dl = make_float2(dv[cc], dv[cc + 1]);
+          } else {
+            nl2 = make_float2(-my_l2, -my_l2);
+            dl = make_float2(my_delta, my_delta);
           }
+          const float2 y = __ffma2_rn(make_float2(__uint_as_float(xs[c]), __uint_as_float(xs[c + 1])), c2, nl2);
+          float2 pr = make_float2(ex2(y.x), ex2(y.y));
+          if (diag) {
+            if (KV_OUTER ? cc < lim : cc > lim) pr.x = 0.f;
+            if (KV_OUTER ? cc + 1 < lim : cc + 1 > lim) pr.y = 0.f;
+          }
+          const float2 gr = __fadd2_rn(make_float2(__uint_as_float(ys[c]), __uint_as_float(ys[c + 1])),
+                                       make_float2(-dl.x, -dl.y));
+          const float2 ds = __fmul2_rn(pr, gr);
+          pk[c / 2] = pack2<BF16>(pr.x, pr.y);
+          dk[c / 2] = pack2<BF16>(ds.x, ds.y);
         }
-        const float2 g = __fadd2_rn(make_float2(__uint_as_float(ys[c]), __uint_as_float(ys[c + 1])),
-                                    make_float2(-dl.x, -dl.y));
-        const float2 ds = __fmul2_rn(pr, g);
-        pk[c / 2] = pack2<BF16>(pr.x, pr.y);
-        dk[c / 2] = pack2<BF16>(ds.x, ds.y);
+        // 16-bit P (dK/dV pass only) and dS of these 16 columns go to columns
+        // 8h..8h+7 of this warp's region of X and Y, already read.
+        if constexpr (KV_OUTER) tmem_st8(tX + 8 * h, pk);
+        tmem_st8(tY + 8 * h, dk);
       }
-      // 16-bit P (dK/dV pass only) and dS go over the first 16 columns of this
-      // warp's own 32-column slice of X and Y.
-      if constexpr (KV_OUTER) tmem_st16(tX, pk);
-      tmem_st16(tY, dk);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_pfull[b]);
+      if (lane == 0) mbar_arrive(&bar_pfull[g]);
     }
     // ------------------------------------------------------------ epilogue
     const bool done = alive && mbar_wait(bar_accfinal, 0, abort_flag, p.err, kErrTimeoutSoftmax);
-    // Each warp stores half of the accumulator columns of its 32 rows (all of
-    // them when D = 16, from the warps of half 0).
-    constexpr int kEpiCols = D / 2 >= 16 ? D / 2 : D;
-    const int c_begin = D / 2 >= 16 ? hf * kEpiCols : 0;
-    if (__all_sync(0xffffffffu, done) && (D / 2 >= 16 || hf == 0)) {
+    // The 16 warps split the accumulator columns of their 32 rows into up to
+    // four parts of at least 16 columns.
+    constexpr int kParts = D >= 64 ? 4 : D / 16;
+    constexpr int kEpiCols = D / kParts;
+    const int part = warp >> 2;
+    if (__all_sync(0xffffffffu, done) && part < kParts) {
       tc_fence_after();
+      const int c_begin = part * kEpiCols;
       const bool row_ok = my < S;
       const size_t off = (static_cast<size_t>(rowbase) + (row_ok ? my : 0)) * D;
       const uint32_t t_acc = tmem + lane_base;
@@ -408,7 +422,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, L::kTmemCols);
   }
