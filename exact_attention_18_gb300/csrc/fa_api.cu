@@ -165,8 +165,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
       (st = check_ptr(o, "o")) || (st = check_ptr(lse, "lse")))
     return st;
   const bool bf16 = dtype == FA_BF16;
-  // Q in 128-row boxes (a CTA's own tiles); K and V in 64-row boxes (each CTA
-  // of a cluster pair loads half of every block for both).
+  // Q in 128-row boxes (a CTA's own tiles); K and V in 64-row boxes.
   CUtensorMap tq, tk, tv;
   if ((st = encode_qkv_map(&tq, q, bf16, D, S, BH, "q")) || (st = encode_qkv_map(&tk, k, bf16, D, S, BH, "k", 64)) ||
       (st = encode_qkv_map(&tv, v, bf16, D, S, BH, "v", 64)))
@@ -175,7 +174,8 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   p.o = o;
   p.lse = lse;
   p.S = static_cast<int>(S);
-  p.n_m_tiles = static_cast<int>((S + 2 * fa::kBlockM - 1) / (2 * fa::kBlockM));  // CTAs per head: 256 rows each
+  const int rows_per_cta = fa::fwd_rows_per_cta(static_cast<int>(D));
+  p.n_m_tiles = static_cast<int>((S + rows_per_cta - 1) / rows_per_cta);  // CTAs per (b, h)
   p.causal = causal ? 1 : 0;
   p.scale_log2 = scale * kLog2e;
   p.err = fa::device_error_word();

@@ -39,7 +39,7 @@
 // Causal: tile t of query rows visits key blocks up to its diagonal block
 // ("T5 讲解" §⑤); masking is element-wise only on the diagonal block and on a
 // ragged last key block ("fa-triton" §Causal Mask 的处理：off-band 与 on-band).
-#include "fa_kernel_common.cuh"
+#include "fa_softmax.cuh"
 
 namespace fa {
 using namespace ptx;
@@ -54,7 +54,12 @@ constexpr int kLaunchRegs = 168;
 constexpr uint32_t kRegsHigh = 224;
 constexpr uint32_t kRegsLow = 56;
 static_assert(2 * 128 * kRegsHigh + 128 * kRegsLow <= kFwdThreads * kLaunchRegs, "register split");
-constexpr float kTau = 8.0f;  // stale-max threshold (log2 units)
+// A block's P~ = exp2(c s - m) is accepted with a stale maximum m while the
+// block's sum stays <= 2^8 (so every P~ <= 2^8, far inside the 16-bit range).
+constexpr float kSumLimit = 256.0f;
+// The two tiles' softmax warps of one SM sub-partition alternate at the
+// exponentials of each key block.
+constexpr bool kTurns = true;
 
 template <int D>
 struct FwdLayout : TileGeom<D> {
@@ -65,8 +70,8 @@ struct FwdLayout : TileGeom<D> {
   static constexpr int kOffK = kOffQ + 2 * G::kTileBytes;
   static constexpr int kOffV = kOffK + kStages * G::kTileBytes;
   static constexpr int kOffBar = kOffV + kStages * G::kTileBytes;
-  // q, kfull[S], vfull[S], empty[S], sfull[2], sfree[2], pfull[2], pvdone[2], ofinal[2], drain[2]
-  static constexpr int kNumBars = 1 + 3 * kStages + 10 + 2;
+  // q, kfull[S], vfull[S], empty[S], sfull[2], sfree[2], pfull[2], pvdone[2], ofinal[2], drain[2], turn[8]
+  static constexpr int kNumBars = 1 + 3 * kStages + 10 + 2 + 8;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemUsed = kOffMisc + 16;
   // Tensor memory is allocated whole (512 columns), so at most one CTA may
@@ -80,23 +85,24 @@ struct FwdLayout : TileGeom<D> {
   static_assert(kColO + 2 * D <= kTmemCols, "TMEM layout");
 };
 
-__device__ __forceinline__ float max3(float a, float b, float c) {
-  float d;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
-}
-__device__ __forceinline__ float min3(float a, float b, float c) {
-  float d;
-  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
-}
-
-// Warp-collective: after this warp's tcgen05 stores/loads are complete, one
-// elected lane arrives on `bar` (whose count is the number of arriving warps).
-__device__ __forceinline__ void warp_arrive(uint64_t* bar) {
-  tc_fence_before();
-  __syncwarp();
-  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+// P~ = exp2(c2 * s - m) for the block's 128 scores, packed as 16-bit pairs
+// into pk; with `masked`, columns past lim are exactly 0.  Returns the fp32
+// sum of the unrounded P~ (the block's share of the running sum l).
+template <bool BF16>
+__device__ __forceinline__ float exp_block(const uint32_t* sr, float2 c2, float m, bool masked, int lim,
+                                           uint32_t* pk) {
+  const float m_use = (m == -INFINITY) ? 0.f : m;  // rows with no visible key so far
+  const float2 negm = make_float2(-m_use, -m_use);
+  float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+  if (masked) {
+#pragma unroll
+    for (int k0 = 0; k0 < kBlockN; k0 += 16) exp16<BF16, true>(sr, k0, c2, negm, lim, acc, pk + k0 / 2);
+  } else {
+#pragma unroll
+    for (int k0 = 0; k0 < kBlockN; k0 += 16) exp16<BF16, false>(sr, k0, c2, negm, lim, acc, pk + k0 / 2);
+  }
+  const float2 a = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+  return a.x + a.y;
 }
 
 }  // namespace
@@ -123,6 +129,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   uint64_t* bar_pvdone = bar_pfull + 2;          // [2] O_t += P_t(j) V(j) done (separate-P layout)
   uint64_t* bar_ofinal = bar_pvdone + 2;         // [2] last P V of tile t done
   uint64_t* bar_drain = bar_ofinal + 2;          // [2] one per MMA warp
+  uint64_t* bar_turn = bar_drain + 2;            // [2][4] tile t's warps q may start their exponentials
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 4);
 
@@ -158,6 +165,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
     mbar_init(&bar_drain[0], 1);
     mbar_init(&bar_drain[1], 1);
+    for (int i = 0; i < 8; ++i) mbar_init(&bar_turn[i], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -291,133 +299,95 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     regs_increase<kRegsHigh>();
     // ------------------------------------------------------------ softmax warpgroups
     const int t = warp >> 2;            // tile
+    const int q4 = warp & 3;            // lane quarter (and SM sub-partition) of this warp
     const int r = threadIdx.x & 127;    // row within the tile == TMEM lane
     const int tile_row0 = row0 + t * kBlockM;
     const int row_g = tile_row0 + r;
     const int nb = t == 0 ? nb0 : nb1;
-    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int nb_other = t == 0 ? nb1 : nb0;
+    const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
     const uint32_t t_s = tmem + lane_base + L::kColS + 128u * t;
     const uint32_t t_p = tmem + lane_base + L::kColP + L::kStrideP * t;
     const uint32_t t_o = tmem + lane_base + L::kColO + D * t;
     const float sl2 = p.scale_log2;
     const float2 c2 = make_float2(sl2, sl2);
+    const bool neg_scale = sl2 < 0.f;
     const int last = p.causal ? min(S - 1, row_g) : S - 1;  // last visible key of this row
     float m = -INFINITY;  // running (possibly stale) maximum, base-2 scaled
     float l = 0.f;
     bool alive = true;
     for (int j = 0; j < nb && alive; ++j) {
       uint32_t sr[kBlockN];
-      bool masked = false;
-      bool upd = false;
+      if (!warp_wait(&bar_sfull[t], j & 1, abort_flag, p.err, kErrTimeoutSoftmax)) {
+        alive = false;
+        break;
+      }
+      tc_fence_after();
+      tmem_ld128(t_s, sr);
+      if (L::kSepP) warp_arrive(&bar_sfree[t]);  // S_t(j) is in registers: the MMA may overwrite it
+      const int kv0 = j * kBlockN;
+      const int lim = last - kv0;  // columns c <= lim are visible to this row
+      // Masked blocks: the diagonal block under the causal mask, and a ragged
+      // last key block.
+      const bool masked = (kv0 + kBlockN > S) || (p.causal && kv0 + kBlockN - 1 > tile_row0);
+      if (j == 0) m = block_max_scaled<kBlockN>(sr, masked, lim, sl2, neg_scale);
+      // The two tiles' warps of one sub-partition take turns at the
+      // exponentials, so one's loads, stores and waits overlap the other's.
+      if (kTurns && (t == 0 ? j >= 1 && j - 1 < nb_other : j < nb_other) &&
+          !warp_wait(&bar_turn[t * 4 + q4], (t == 0 ? j - 1 : j) & 1, abort_flag, p.err, kErrTimeoutSoftmax)) {
+        alive = false;
+        break;
+      }
+      uint32_t pk[kBlockN / 2];
       float alpha = 1.f;
-      if (alive && !warp_wait(&bar_sfull[t], j & 1, abort_flag, p.err, kErrTimeoutSoftmax)) alive = false;
-      if (alive) {
-        tc_fence_after();
-        tmem_ld128(t_s, sr);
-        if (L::kSepP) warp_arrive(&bar_sfree[t]);  // S_t(j) is in registers: the MMA may overwrite it
-        const int kv0 = j * kBlockN;
-        // Masked blocks: the diagonal block under the causal mask, and a
-        // ragged last key block.
-        masked = (kv0 + kBlockN > S) || (p.causal && kv0 + kBlockN - 1 > tile_row0);
-        float mx;
-        if (!masked) {
-          // Eight independent chains of 3-input max/min keep the dependency depth short.
-          float mc[8];
-          if (sl2 >= 0.f) {
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const uint32_t* v = sr + 16 * k;
-              float a = max3(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
-#pragma unroll
-              for (int c = 3; c < 15; c += 2) a = max3(a, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
-              mc[k] = fmaxf(a, __uint_as_float(v[15]));
-            }
-            mx = max3(max3(mc[0], mc[1], mc[2]), max3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7]));
-          } else {  // a negative scale turns the largest scaled score into the smallest raw one
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const uint32_t* v = sr + 16 * k;
-              float a = min3(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
-#pragma unroll
-              for (int c = 3; c < 15; c += 2) a = min3(a, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
-              mc[k] = fminf(a, __uint_as_float(v[15]));
-            }
-            mx = min3(min3(mc[0], mc[1], mc[2]), min3(mc[3], mc[4], mc[5]), fminf(mc[6], mc[7]));
-          }
-        } else {
-          mx = sl2 >= 0.f ? -INFINITY : INFINITY;
-#pragma unroll
-          for (int c = 0; c < kBlockN; ++c) {
-            const float x = __uint_as_float(sr[c]);
-            if (kv0 + c <= last) mx = sl2 >= 0.f ? fmaxf(mx, x) : fminf(mx, x);
-          }
-        }
-        // A block with no visible key for this row (only rows past S) contributes nothing.
-        const float m_blk = (kv0 > last) ? -INFINITY : mx * sl2;
-        if (j == 0) {
-          m = m_blk;
-        } else if (m_blk > m + kTau) {
+      bool upd = false;
+      float blk = exp_block<BF16>(sr, c2, m, masked, lim, pk);
+      // Every P~ <= 2^8 holds if the block's sum does.  Otherwise (or on NaN)
+      // this block's maximum is too far above the stale m: move m to it,
+      // rescale, and redo the block ("T5 讲解" §④ online update).
+      const bool need = !(blk <= kSumLimit);
+      if (__any_sync(0xffffffffu, need)) {
+        const float m_blk = block_max_scaled<kBlockN>(sr, masked, lim, sl2, neg_scale);
+        if (need && m_blk > m) {
           alpha = ex2(m - m_blk);
           m = m_blk;
           upd = true;
         }
+        if (__any_sync(0xffffffffu, upd)) blk = exp_block<BF16>(sr, c2, m, masked, lim, pk);
       }
-      if (alive) {
-        const int kv0 = j * kBlockN;
-        const float m_use = (m == -INFINITY) ? 0.f : m;
-        const float2 negm = make_float2(-m_use, -m_use);
-        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                         make_float2(0.f, 0.f)};
-        uint32_t pk[kBlockN / 2];
-        if (!masked) {
-#pragma unroll
-          for (int c = 0; c < kBlockN; c += 2) {
-            const float2 y = __ffma2_rn(make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), c2, negm);
-            const float2 e = make_float2(ex2(y.x), ex2(y.y));
-            acc[(c / 2) & 3] = __fadd2_rn(acc[(c / 2) & 3], e);
-            pk[c / 2] = pack2<BF16>(e.x, e.y);
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < kBlockN; c += 2) {
-            const float2 y = __ffma2_rn(make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), c2, negm);
-            const float e0 = (kv0 + c <= last) ? ex2(y.x) : 0.f;
-            const float e1 = (kv0 + c + 1 <= last) ? ex2(y.y) : 0.f;
-            acc[(c / 2) & 3] = __fadd2_rn(acc[(c / 2) & 3], make_float2(e0, e1));
-            pk[c / 2] = pack2<BF16>(e0, e1);
-          }
-        }
-        const float2 accs = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
-        l = l * alpha + (accs.x + accs.y);
-        // With separate P, P_t(j-1) V(j-1) must be done before P_t is rewritten
-        // and before O_t is rescaled.  (With P over S, S_t(j) being ready already
-        // implies it: its commit covers the earlier P V.)
-        if (L::kSepP && j > 0 && !warp_wait(&bar_pvdone[t], (j - 1) & 1, abort_flag, p.err, kErrTimeoutSoftmax)) {
-          alive = false;
-          break;
-        }
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, upd)) {
-          // O holds the blocks before j relative to the old m: rescale this warp's rows.
-#pragma unroll
-          for (int c = 0; c < D; c += 16) {
-            uint32_t o16[16];
-            tmem_ld16(t_o + c, o16);
-#pragma unroll
-            for (int i = 0; i < 16; i += 2) {
-              const float2 v = __fmul2_rn(make_float2(__uint_as_float(o16[i]), __uint_as_float(o16[i + 1])),
-                                          make_float2(alpha, alpha));
-              o16[i] = __float_as_uint(v.x);
-              o16[i + 1] = __float_as_uint(v.y);
-            }
-            tmem_st16(t_o + c, o16);
-          }
-        }
-        tmem_st32(t_p, pk);
-        tmem_st32(t_p + 32, pk + 32);
-        tmem_st_wait();
-        warp_arrive(&bar_pfull[t]);
+      if (kTurns && (t == 0 ? j < nb_other : j + 1 < nb_other)) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_turn[(1 - t) * 4 + q4]);
       }
+      l = l * alpha + blk;
+      // With separate P, P_t(j-1) V(j-1) must be done before P_t is rewritten
+      // and before O_t is rescaled.  (With P over S, S_t(j) being ready already
+      // implies it: its commit covers the earlier P V.)
+      if (L::kSepP && j > 0 && !warp_wait(&bar_pvdone[t], (j - 1) & 1, abort_flag, p.err, kErrTimeoutSoftmax)) {
+        alive = false;
+        break;
+      }
+      tc_fence_after();
+      if (__any_sync(0xffffffffu, upd)) {
+        // O holds the blocks before j relative to the old m: rescale this warp's rows.
+#pragma unroll
+        for (int c = 0; c < D; c += 16) {
+          uint32_t o16[16];
+          tmem_ld16(t_o + c, o16);
+#pragma unroll
+          for (int i = 0; i < 16; i += 2) {
+            const float2 v = __fmul2_rn(make_float2(__uint_as_float(o16[i]), __uint_as_float(o16[i + 1])),
+                                        make_float2(alpha, alpha));
+            o16[i] = __float_as_uint(v.x);
+            o16[i + 1] = __float_as_uint(v.y);
+          }
+          tmem_st16(t_o + c, o16);
+        }
+      }
+      tmem_st32(t_p, pk);
+      tmem_st32(t_p + 32, pk + 32);
+      tmem_st_wait();
+      warp_arrive(&bar_pfull[t]);
     }
     // ------------------------------------------------------------ epilogue
     if (alive && nb > 0 && warp_wait(&bar_ofinal[t], 0, abort_flag, p.err, kErrTimeoutSoftmax)) {
@@ -470,9 +440,10 @@ cudaError_t launch_fwd(int D, bool bf16, const CUtensorMap& tq, const CUtensorMa
     return bf16 ? launch_fwd_t<DD, true>(tq, tk, tv, p, BH, stream)      \
                 : launch_fwd_t<DD, false>(tq, tk, tv, p, BH, stream);
   switch (D) {
-    FA_FWD_CASE(16)
-    FA_FWD_CASE(32)
-    FA_FWD_CASE(64)
+    case 16:
+    case 32:
+    case 64:
+      return launch_fwd4(D, bf16, tq, tk, tv, p, BH, stream);
     FA_FWD_CASE(128)
     default:
       return cudaErrorInvalidValue;

@@ -14,7 +14,7 @@ struct FwdParams {
   void* o;             // [BH, S, D] output
   float* lse;          // [BH, S] natural-log logsumexp
   int S;               // sequence length
-  int n_m_tiles;       // CTAs per (b, h): ceil(S / (2 * kBlockM))
+  int n_m_tiles;       // CTAs per (b, h): ceil(S / fwd_rows_per_cta(D))
   int causal;          // nonzero: key j visible to query i iff j <= i
   float scale_log2;    // scale * log2(e): scores enter exp2 in base 2
   int* err;            // device error word (set when a pipeline wait times out)
@@ -45,7 +45,14 @@ struct BwdMaps {
   CUtensorMap q64, k64, v64, do64;
 };
 
+// Query rows one forward CTA covers for head dimension D.
+int fwd_rows_per_cta(int D);
+
 // Launchers (one per kernel family); they dispatch on D and dtype.
+// launch_fwd4: the four-tile forward for D <= 64; launch_fwd: any D (passes
+// D <= 64 on to launch_fwd4).
+cudaError_t launch_fwd4(int D, bool bf16, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                        const FwdParams& p, int BH, cudaStream_t stream);
 cudaError_t launch_fwd(int D, bool bf16, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdParams& p, int BH, cudaStream_t stream);
 
