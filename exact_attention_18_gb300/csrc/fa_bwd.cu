@@ -247,6 +247,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // compile-time offsets, so issue keeps pace with the tensor core.
     constexpr uint32_t idesc_xy = make_idesc_f16(BF16, 128, kPN, false, false);
     constexpr uint32_t idesc_acc = make_idesc_f16(BF16, 128, D, false, true);
+    const AccFlags accf = runtime_flags(S);
     const uint64_t a1_desc = make_sdesc(sA1, 16, 8 * GA::kRowBytes, GA::kSwz);
     const uint64_t a2_desc = make_sdesc(sA2, 16, 8 * GA::kRowBytes, GA::kSwz);
     // X, Y of block i into buffer i & 1 (group i & 1's).  The buffer was last
@@ -260,11 +261,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
         mma_ss_warp(tb, desc_plus(a1_desc, kmajor_step_bytes<D, 128>(kk)), desc_plus(b1, kmajor_step_bytes<D, kPN>(kk)),
-                    idesc_xy, kk > 0 ? 1u : 0u);
+                    idesc_xy, kk > 0 ? accf.on : accf.off);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
         mma_ss_warp(tb + 64, desc_plus(a2_desc, kmajor_step_bytes<D, 128>(kk)),
-                    desc_plus(b2, kmajor_step_bytes<D, kPN>(kk)), idesc_xy, kk > 0 ? 1u : 0u);
+                    desc_plus(b2, kmajor_step_bytes<D, kPN>(kk)), idesc_xy, kk > 0 ? accf.on : accf.off);
       mma_commit_warp(&bar_xyfull[i & 1]);
     };
     auto acc = [&](int x) -> bool {
@@ -278,16 +279,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < kPN / 16; ++kk)  // dV += P^T dO_i
           mma_ts_warp(tmem + L::kColAcc1, tb + packed_col(kk), desc_plus(b2, mnmajor_step_bytes<D>(kk)), idesc_acc,
-                      (x > 0 || kk > 0) ? 1u : 0u);
+                      (x > 0 || kk > 0) ? accf.on : accf.off);
 #pragma unroll
         for (int kk = 0; kk < kPN / 16; ++kk)  // dK += dS^T Q_i
           mma_ts_warp(tmem + L::kColAcc2, tb + 64 + packed_col(kk), desc_plus(b1, mnmajor_step_bytes<D>(kk)),
-                      idesc_acc, (x > 0 || kk > 0) ? 1u : 0u);
+                      idesc_acc, (x > 0 || kk > 0) ? accf.on : accf.off);
       } else {
 #pragma unroll
         for (int kk = 0; kk < kPN / 16; ++kk)  // dQ += dS K_j
           mma_ts_warp(tmem + L::kColAcc1, tb + 64 + packed_col(kk), desc_plus(b1, mnmajor_step_bytes<D>(kk)),
-                      idesc_acc, (x > 0 || kk > 0) ? 1u : 0u);
+                      idesc_acc, (x > 0 || kk > 0) ? accf.on : accf.off);
       }
       mma_commit_warp(&bar_empty[st]);
       return true;

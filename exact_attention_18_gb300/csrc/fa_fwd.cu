@@ -236,6 +236,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const int nbt = t == 0 ? nb0 : nb1;
       constexpr uint32_t idesc_qk = make_idesc_f16(BF16, 128, kBlockN, false, false);
       constexpr uint32_t idesc_pv = make_idesc_f16(BF16, 128, D, false, true);
+      const AccFlags acc = runtime_flags(S);
       const uint64_t q_desc = make_sdesc(sQ + t * L::kTileBytes, 16, 8 * L::kRowBytes, L::kSwz);
       // S_t = Q_t K(j)^T; with separate P, first wait until the warpgroup has loaded S_t(j-1).
       auto qk = [&](int j) -> bool {
@@ -247,7 +248,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           mma_ss_warp(tmem + L::kColS + 128u * t, desc_plus(q_desc, kmajor_step_bytes<D>(kk)),
-                      desc_plus(k_desc, kmajor_step_bytes<D>(kk)), idesc_qk, kk > 0 ? 1u : 0u);
+                      desc_plus(k_desc, kmajor_step_bytes<D>(kk)), idesc_qk, kk > 0 ? acc.on : acc.off);
         mma_commit_warp(&bar_sfull[t]);
         return true;
       };
@@ -262,7 +263,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < kBlockN / 16; ++kk)
           mma_ts_warp(tmem + L::kColO + D * t, t_p + kk * 8, desc_plus(v_desc, mnmajor_step_bytes<D>(kk)), idesc_pv,
-                      (j > 0 || kk > 0) ? 1u : 0u);
+                      (j > 0 || kk > 0) ? acc.on : acc.off);
         if (L::kSepP) mma_commit_warp(&bar_pvdone[t]);
         if (j == nbt - 1) mma_commit_warp(&bar_ofinal[t]);
         return true;

@@ -8,12 +8,12 @@
 // own softmax warpgroup (thread = query row = TMEM lane, the split-Q partition
 // of "Inside FlashAttention" §4.3), so every SM sub-partition holds four
 // softmax warps whose loads, stores and waits hide behind each other's
-// exponentials.  Key/value blocks are 64 rows.  Warp roles (640 threads):
+// exponentials.  Key/value blocks are 64 rows.  Warp roles (768 threads):
 //   warps 0-15  softmax: warp w serves tile w/4, TMEM lanes 32(w%4)..+31;
 //   warp 16     TMA producer: the four Q tiles once, then K and V blocks
 //               through a ring of shared-memory stages;
-//   warps 17-18 MMA issuers, for tiles {0, 2} and {1, 3};
-//   warp 19     idle (warps 16-19 give registers to the softmax warps).
+//   warps 17-20 MMA issuers, one per tile;
+//   warps 21-23 idle (warps 16-23 give registers to the softmax warps).
 //
 // TMEM (512 columns): tile t owns columns [128t, 128t+128): S_t in the first
 // 64 (fp32 scores of one block), O_t in the next D.  The 16-bit P_t(j) is
@@ -44,19 +44,34 @@ using namespace ptx;
 
 namespace {
 
-constexpr int kF4Threads = 640;
 constexpr int kF4Tiles = 4;
 constexpr int kF4BlockN = 64;     // keys per block
 constexpr int kF4RowsPerCta = kF4Tiles * kBlockM;
 constexpr int kF4Producer = 16;
-constexpr int kF4MmaWarp0 = 17;   // tiles 0 and 2; warp 18: tiles 1 and 3
-// Register split: the launch gives every thread kF4LaunchRegs; warps 16-19
-// drop to kF4RegsLow and the softmax warps rise to kF4RegsHigh.
-constexpr int kF4LaunchRegs = 96;
-constexpr uint32_t kF4RegsHigh = 104;
-constexpr uint32_t kF4RegsLow = 64;
-static_assert(16 * 32 * kF4RegsHigh + 4 * 32 * kF4RegsLow <= kF4Threads * kF4LaunchRegs, "register split");
+constexpr int kF4MmaWarp0 = 17;
+// MMA issuers: warp kF4MmaWarp0 + w serves tiles w * kF4TilesPerMma, ...  One
+// warp cannot issue the small (N = 64) products of several tiles fast enough.
+constexpr int kF4MmaWarps = 2;
+constexpr int kF4TilesPerMma = kF4Tiles / kF4MmaWarps;
+// Whole warpgroups after the 16 softmax warps: producer + MMA warps + idle.
+constexpr int kF4Threads = 512 + 128 * ((1 + kF4MmaWarps + 3) / 4);
+// Register split: the launch gives every thread kF4LaunchRegs; the warps
+// after the softmax warps drop to kF4RegsLow and the softmax warps rise to
+// kF4RegsHigh.
+constexpr int kF4LaunchRegs = kF4Threads == 640 ? 96 : 80;
+constexpr uint32_t kF4RegsHigh = kF4Threads == 640 ? 104 : 96;
+constexpr uint32_t kF4RegsLow = kF4Threads == 640 ? 64 : 48;
+static_assert(512 * kF4RegsHigh + (kF4Threads - 512) * kF4RegsLow <= kF4Threads * kF4LaunchRegs, "register split");
 constexpr float kF4SumLimit = 256.0f;
+// The softmax warps of one SM sub-partition can take turns at the
+// exponentials in groups of kF4TurnGroup tiles (group order within each key
+// block), so one group's exponentials run while the tensor core works on the
+// other group's products (the ping-pong of "Inside FlashAttention" §5.2).
+// Measured on GB300 at D = 64, forced turns (groups of 1 or 2 tiles) were
+// 25-50% slower than free-running warps, so kF4TurnGroup = 4: no turns.
+constexpr int kF4TurnGroup = 4;
+constexpr int kF4TurnGroups = kF4Tiles / kF4TurnGroup;
+constexpr bool kF4Turns = kF4TurnGroups > 1;
 
 template <int D>
 struct F4Layout {
@@ -68,8 +83,8 @@ struct F4Layout {
   static constexpr int kOffK = kOffQ + kF4Tiles * GQ::kTileBytes;
   static constexpr int kOffV = kOffK + kStages * GK::kTileBytes;
   static constexpr int kOffBar = kOffV + kStages * GK::kTileBytes;
-  // q, kfull[S], vfull[S], empty[S], sfull[4], pfull[4], ofinal[4], drain[2]
-  static constexpr int kNumBars = 1 + 3 * kStages + 12 + 2;
+  // q, kfull[S], vfull[S], empty[S], sfull[4], pfull[4], ofinal[4], drain[MMA warps], turn[groups][4]
+  static constexpr int kNumBars = 1 + 3 * kStages + 12 + kF4MmaWarps + 4 * kF4TurnGroups;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemUsed = kOffMisc + 16;
   // TMEM is allocated whole (512 columns): the shared-memory request keeps it
@@ -103,7 +118,8 @@ __global__ void __launch_bounds__(kF4Threads, 1)
   uint64_t* bar_sfull = bar_empty + L::kStages;  // [4] S_t(j) computed (and P_t(j-1) V(j-1) done)
   uint64_t* bar_pfull = bar_sfull + kF4Tiles;     // [4] P_t(j) stored, O_t rescaled
   uint64_t* bar_ofinal = bar_pfull + kF4Tiles;    // [4] last P V of tile t done
-  uint64_t* bar_drain = bar_ofinal + kF4Tiles;    // [2] one per MMA warp
+  uint64_t* bar_drain = bar_ofinal + kF4Tiles;    // one per MMA warp
+  uint64_t* bar_turn = bar_drain + kF4MmaWarps;   // [group][lane quarter]: that group's warps may start
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 4);
 
@@ -128,15 +144,15 @@ __global__ void __launch_bounds__(kF4Threads, 1)
     for (int s = 0; s < L::kStages; ++s) {
       mbar_init(&bar_kfull[s], 1);
       mbar_init(&bar_vfull[s], 1);
-      mbar_init(&bar_empty[s], 2);  // released by both MMA warps
+      mbar_init(&bar_empty[s], kF4MmaWarps);  // released by every MMA warp
     }
     for (int t = 0; t < kF4Tiles; ++t) {
       mbar_init(&bar_sfull[t], 1);
       mbar_init(&bar_pfull[t], 4);  // one arrival per softmax warp of the tile
       mbar_init(&bar_ofinal[t], 1);
     }
-    mbar_init(&bar_drain[0], 1);
-    mbar_init(&bar_drain[1], 1);
+    for (int w = 0; w < kF4MmaWarps; ++w) mbar_init(&bar_drain[w], 1);
+    for (int i = 0; i < 4 * kF4TurnGroups; ++i) mbar_init(&bar_turn[i], kF4TurnGroup);  // the group's warps
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -182,17 +198,21 @@ __global__ void __launch_bounds__(kF4Threads, 1)
           drain_wait(&bar_vfull[st], (x / L::kStages) & 1, p.err);
         }
       }
-    } else if (warp == kF4MmaWarp0 || warp == kF4MmaWarp0 + 1) {
+    } else if (warp >= kF4MmaWarp0 && warp < kF4MmaWarp0 + kF4MmaWarps) {
       // ------------------------------------------------------------ MMA issuers
-      // Warp 17 serves tiles 0 and 2, warp 18 tiles 1 and 3.  Each runs
-      // converged and one elected lane issues every MMA.
+      // Warp kF4MmaWarp0 + w serves tiles w * kF4TilesPerMma, ... (one turn
+      // group).  Each runs converged and one elected lane issues every MMA.
       const int w = warp - kF4MmaWarp0;
-      const int ta = w, tb = w + 2;
-      const int nba = blocks_for(row0 + ta * kBlockM);
-      const int nbb = blocks_for(row0 + tb * kBlockM);
-      const int nbw = max(nba, nbb);
+      int nbt[kF4TilesPerMma];
+      int nbw = 0;
+#pragma unroll
+      for (int h = 0; h < kF4TilesPerMma; ++h) {
+        nbt[h] = blocks_for(row0 + (w * kF4TilesPerMma + h) * kBlockM);
+        nbw = max(nbw, nbt[h]);
+      }
       constexpr uint32_t idesc_qk = make_idesc_f16(BF16, 128, kBN, false, false);
       constexpr uint32_t idesc_pv = make_idesc_f16(BF16, 128, D, false, true);
+      const AccFlags acc = runtime_flags(S);
       // S_t = Q_t K(j)^T into tile t's S columns.
       auto qk = [&](int t, int j) {
         const uint64_t q_desc = make_sdesc(sQ + t * GQ::kTileBytes, 16, 8 * GQ::kRowBytes, GQ::kSwz);
@@ -200,7 +220,7 @@ __global__ void __launch_bounds__(kF4Threads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           mma_ss_warp(tmem + 128u * t, desc_plus(q_desc, kmajor_step_bytes<D, 128>(kk)),
-                      desc_plus(k_desc, kmajor_step_bytes<D, kBN>(kk)), idesc_qk, kk > 0 ? 1u : 0u);
+                      desc_plus(k_desc, kmajor_step_bytes<D, kBN>(kk)), idesc_qk, kk > 0 ? acc.on : acc.off);
       };
       // O_t += P_t(j) V(j), P from tile t's S columns.
       auto pv = [&](int t, int j) {
@@ -209,40 +229,38 @@ __global__ void __launch_bounds__(kF4Threads, 1)
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
           mma_ts_warp(tmem + 128u * t + L::kColO, tmem + 128u * t + kk * 8,
-                      desc_plus(v_desc, mnmajor_step_bytes<D>(kk)), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+                      desc_plus(v_desc, mnmajor_step_bytes<D>(kk)), idesc_pv, (j > 0 || kk > 0) ? acc.on : acc.off);
       };
       bool ok = warp_wait(bar_q, 0, abort_flag, p.err, kErrTimeoutMma);
       if (ok && nbw > 0) ok = warp_wait(&bar_kfull[0], 0, abort_flag, p.err, kErrTimeoutMma);
       if (ok) {
         tc_fence_after();
-        if (nba > 0) {
-          qk(ta, 0);
-          mma_commit_warp(&bar_sfull[ta]);
-        }
-        if (nbb > 0) {
-          qk(tb, 0);
-          mma_commit_warp(&bar_sfull[tb]);
+#pragma unroll
+        for (int h = 0; h < kF4TilesPerMma; ++h) {
+          if (nbt[h] == 0) continue;
+          const int t = w * kF4TilesPerMma + h;
+          qk(t, 0);
+          mma_commit_warp(&bar_sfull[t]);
         }
       }
       int j = 0;
       for (; ok && j < nbw; ++j) {
         const int st = j % L::kStages;
         ok = warp_wait(&bar_vfull[st], (j / L::kStages) & 1, abort_flag, p.err, kErrTimeoutMma);
-        // K(j+1) for the next score products (if either tile goes on).
-        const bool more = j + 1 < nbw;
-        if (ok && more)
+        // K(j+1) for the next score products (if a tile of this warp goes on).
+        if (ok && j + 1 < nbw)
           ok = warp_wait(&bar_kfull[(j + 1) % L::kStages], ((j + 1) / L::kStages) & 1, abort_flag, p.err,
                          kErrTimeoutMma);
 #pragma unroll
-        for (int h = 0; h < 2 && ok; ++h) {
-          const int t = h == 0 ? ta : tb;
-          const int nbt = h == 0 ? nba : nbb;
-          if (j >= nbt) continue;
+        for (int h = 0; h < kF4TilesPerMma; ++h) {
+          if (!ok) break;
+          if (j >= nbt[h]) continue;
+          const int t = w * kF4TilesPerMma + h;
           ok = warp_wait(&bar_pfull[t], j & 1, abort_flag, p.err, kErrTimeoutMma);
           if (!ok) break;
           tc_fence_after();
           pv(t, j);
-          if (j + 1 < nbt) {
+          if (j + 1 < nbt[h]) {
             qk(t, j + 1);
             mma_commit_warp(&bar_sfull[t]);
           } else {
@@ -251,8 +269,8 @@ __global__ void __launch_bounds__(kF4Threads, 1)
         }
         if (ok) mma_commit_warp(&bar_empty[st]);  // this warp's MMAs on K(j), V(j) are issued
       }
-      // Blocks the CTA loads but neither of this warp's tiles uses: release
-      // each once it has landed (so its arrival counts toward the right phase).
+      // Blocks the CTA loads but no tile of this warp uses: release each once
+      // it has landed (so the arrival counts toward the right phase).
       for (; ok && j < nbp; ++j) {
         const int st = j % L::kStages;
         ok = warp_wait(&bar_vfull[st], (j / L::kStages) & 1, abort_flag, p.err, kErrTimeoutMma) &&
@@ -282,6 +300,44 @@ __global__ void __launch_bounds__(kF4Threads, 1)
     float m = -INFINITY;  // running (possibly stale) maximum, base-2 scaled
     float l = 0.f;
     bool alive = true;
+    // Turn order on this sub-partition: key block by key block, and within a
+    // block the groups that visit it in group order.  A group takes part in
+    // block j while any of its tiles does; a warp whose tile has finished
+    // keeps passing the turn on for its group (after its epilogue).
+    const int g = t / kF4TurnGroup;
+    int ng[kF4TurnGroups];
+#pragma unroll
+    for (int u = 0; u < kF4TurnGroups; ++u) {
+      ng[u] = 0;
+#pragma unroll
+      for (int v = 0; v < kF4TurnGroup; ++v) ng[u] = max(ng[u], blocks_for(row0 + (u * kF4TurnGroup + v) * kBlockM));
+    }
+    int first = kF4TurnGroups;
+#pragma unroll
+    for (int u = kF4TurnGroups - 1; u >= 0; --u)
+      if (ng[u] > 0) first = u;
+    // The group whose turn follows (g, j), or -1 if the sequence ends there.
+    auto successor = [&](int j) {
+#pragma unroll
+      for (int u = 0; u < kF4TurnGroups; ++u)
+        if (u > g && ng[u] > j) return u;
+#pragma unroll
+      for (int u = 0; u < kF4TurnGroups; ++u)
+        if (ng[u] > j + 1) return u;
+      return -1;
+    };
+    auto wait_turn = [&](int j, int& waited) -> bool {
+      if (g == first && j == 0) return true;
+      const bool ok = warp_wait(&bar_turn[g * 4 + q4], waited & 1, abort_flag, p.err, kErrTimeoutSoftmax);
+      ++waited;
+      return ok;
+    };
+    auto pass_turn = [&](int j) {
+      const int nxt = successor(j);
+      __syncwarp();
+      if (nxt >= 0 && lane == 0) mbar_arrive(&bar_turn[nxt * 4 + q4]);
+    };
+    int turns_waited = 0;
     for (int j = 0; j < nb; ++j) {
       if (!warp_wait(&bar_sfull[t], j & 1, abort_flag, p.err, kErrTimeoutSoftmax)) {
         alive = false;
@@ -323,7 +379,12 @@ __global__ void __launch_bounds__(kF4Threads, 1)
         const float2 a = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
         return a.x + a.y;
       };
+      if (kF4Turns && !wait_turn(j, turns_waited)) {
+        alive = false;
+        break;
+      }
       blk = exps();
+      if (kF4Turns) pass_turn(j);
       // Every P~ <= 2^8 holds if the block's sum does.  Otherwise (or on NaN)
       // the stale m is too far below this block's maximum: move m, rescale,
       // and redo the block.
@@ -373,6 +434,12 @@ __global__ void __launch_bounds__(kF4Threads, 1)
       }
       if (row_ok) p.lse[static_cast<size_t>(bh) * S + row_g] = (m + log2f(l)) * 0.69314718055994530942f;
     }
+    // Blocks this tile does not visit but its group does: pass the turn on.
+    if (kF4Turns && alive)
+      for (int j = nb; j < ng[g]; ++j) {
+        if (!wait_turn(j, turns_waited)) break;
+        pass_turn(j);
+      }
   }
 
   tc_fence_before();

@@ -71,6 +71,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, but a thread whose phase is not complete is suspended
+// until it completes or `hint_ns` nanoseconds pass, so waiting warps do not
+// take issue slots from the warps they wait for.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+constexpr uint32_t kSleepHintNs = 20000;  // 20 us per suspended try
+
 // Wait until the phase with the given parity has completed.  Returns false
 // (after recording `code`) if that takes longer than kWaitLimitNs, or at once
 // if another thread of the CTA has already given up (*abort != 0).
@@ -79,9 +96,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
   while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
     if (*abort) return false;
     if (globaltimer() - t0 > kWaitLimitNs) {
       *abort = 1;
@@ -186,6 +201,16 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
+// Accumulate flags the compiler cannot fold: {off, on} = {0, 1} derived from
+// a kernel argument (`nonzero` must be nonzero at run time).
+struct AccFlags {
+  uint32_t off, on;
+};
+__device__ __forceinline__ AccFlags runtime_flags(int nonzero) {
+  const uint32_t on = nonzero != 0 ? 1u : 0u;
+  return AccFlags{on ^ 1u, on};
+}
+
 // Arrive once on `bar` when every tcgen05 MMA this thread issued so far is done.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -207,6 +232,9 @@ __device__ __forceinline__ void mma_commit_multicast(uint64_t* bar, uint16_t cta
 // (converged, so descriptors stay warp-uniform) and elect.sync lets exactly
 // one lane issue.  Issuing from converged code is what keeps the MMA issue
 // rate at the tensor core's own rate for small shapes.
+// `accumulate` must be a run-time value (see runtime_flags below): measured
+// on sm_103a, an MMA whose accumulate predicate the compiler can fold to a
+// constant issues at about half the tensor core's rate.
 __device__ __forceinline__ void mma_ss_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                             uint32_t accumulate) {
   asm volatile(
