@@ -37,7 +37,8 @@ sys.path.insert(0, ROOT)
 METRIC = "attention fwd/bwd TFLOPS and % of GB300 FP16 tensor peak (B4 H16 S4096 D64 causal)"
 WORKLOAD = "c2"
 FLUSH_BYTES = 256 << 20  # > 129 MB L2
-KERNEL_SOURCES = ["exact_attention_18_gb300/csrc/fa_fwd.cu", "exact_attention_18_gb300/csrc/fa_bwd.cu",
+KERNEL_SOURCES = ["exact_attention_18_gb300/csrc/fa_fwd.cu", "exact_attention_18_gb300/csrc/fa_fwd4.cu",
+                  "exact_attention_18_gb300/csrc/fa_bwd.cu", "exact_attention_18_gb300/csrc/fa_softmax.cuh",
                   "exact_attention_18_gb300/csrc/fa_kernel_common.cuh", "exact_attention_18_gb300/csrc/sm103_ptx.cuh"]
 
 
@@ -49,12 +50,17 @@ def conv_flops(w):
     return f, 2.5 * f
 
 
+def fwd_kernel_name(w):
+    """The forward kernel the library launches for this head dimension."""
+    return "fa_fwd4_kernel" if w.D <= 64 else "fa_fwd_kernel"
+
+
 def kernel_work(w):
     """Algorithmic work per launch of each kernel (FLOPs of its tensor-core GEMMs, or HBM bytes)."""
     units = w.B * w.H * w.S * w.S * w.D / (2.0 if w.causal else 1.0)
     rows = w.B * w.H * w.S
     return {
-        "fa_fwd_kernel": ("tensor", 4.0 * units),            # S = QK^T, O += PV
+        fwd_kernel_name(w): ("tensor", 4.0 * units),        # S = QK^T, O += PV
         "fa_bwd_preprocess_kernel": ("hbm", rows * w.D * 2 * 2 + rows * 4),  # read O, dO; write Delta
         "fa_bwd_dkdv_kernel": ("tensor", 8.0 * units),       # S^T, dP^T, dV, dK
         "fa_bwd_dq_kernel": ("tensor", 6.0 * units),         # S, dP, dQ
@@ -92,7 +98,7 @@ def load_traffic():
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling every 200 ms while the benchmark runs."""
+    """nvidia-smi clock / throttle sampling every 100 ms while the benchmark runs."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -104,7 +110,7 @@ class ClockSampler:
         self.marks = []
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
-                                          "-lms", "200", "-i", gpu_id], stdout=subprocess.PIPE,
+                                          "-lms", "100", "-i", gpu_id], stdout=subprocess.PIPE,
                                          stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -288,7 +294,7 @@ def main():
     if fa.fa_check_device_errors(sp) != 0:
         raise RuntimeError("device error during the timed steps: " + fa.fa_last_error_detail())
 
-    names = ["fa_fwd_kernel", "fa_bwd_preprocess_kernel", "fa_bwd_dkdv_kernel", "fa_bwd_dq_kernel"]
+    names = [fwd_kernel_name(w), "fa_bwd_preprocess_kernel", "fa_bwd_dkdv_kernel", "fa_bwd_dq_kernel"]
     per = {n: [] for n in names}
     step_ms = []
     for e in evs:
@@ -304,7 +310,7 @@ def main():
         total_ms = float(t.item())
     f_fwd, f_bwd = conv_flops(w)
     value = world * (f_fwd + f_bwd) * args.steps / (total_ms * 1e-3) / 1e12
-    fwd_ms = statistics.mean(per["fa_fwd_kernel"])
+    fwd_ms = statistics.mean(per[names[0]])
     bwd_ms = statistics.mean([a + b + c for a, b, c in zip(per["fa_bwd_preprocess_kernel"],
                                                            per["fa_bwd_dkdv_kernel"], per["fa_bwd_dq_kernel"])])
     peaks = load_peaks()
@@ -371,8 +377,10 @@ def main():
             e2e_ms = float(t.item())
         e2e = {"value": world * (f_fwd + f_bwd) * args.steps / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps}
+    t_wall2 = time.time()
     sampler.stop()
-    clocks = sampler.summary(t_wall0, t_wall1)
+    # Samples from the device-timed steps and the end-to-end steps (both under load).
+    clocks = sampler.summary(t_wall0, t_wall2 if e2e is not None else t_wall1)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -31,10 +31,11 @@
 // The MMA warp then accumulates, with A read from TMEM:
 //     dK/dV pass: dV += P^T dO_i,  dK += dS^T Q_i    (B = B2, B1 read MN-major)
 //     dQ pass:    dQ += dS K_j                       (B = B1 read MN-major)
-// Each group has its own 128-column TMEM buffer for X and Y, and the MMA warp
-// issues X,Y(i+1) before the accumulation of block i, so while one group
-// works on block i the other works on block i+1 and the tensor core on the
-// products of a third.  In the dK/dV pass the producer warp also copies the
+// X and Y of block i live in TMEM buffer i mod kXYBufs (128 columns; three
+// buffers for D <= 64, two for D = 128), and the MMA warp issues X,Y(i + 2)
+// (i + 1 with two buffers) before the accumulation of block i, so a group that
+// finishes block i usually finds block i + 2 already computed, and both groups
+// work while the tensor core runs the products of the blocks around them.  In the dK/dV pass the producer warp also copies the
 // block's L and Delta (one value per partner query) into the stage with
 // cp.async, completing on the same barrier as the block's tiles.
 #include "fa_kernel_common.cuh"
@@ -101,21 +102,72 @@ struct BwdLayout {
   static constexpr int kOffB2 = kOffB1 + kStages * GB::kTileBytes;   // [kStages] tiles
   static constexpr int kOffVec = kOffB2 + kStages * GB::kTileBytes;  // [kStages][L, Delta][64] fp32
   static constexpr int kOffBar = kOffVec + kStages * 2 * kPartnerRows * 4;
-  // a_full, b_full[S], empty[S], xy_full[2], p_full[2], acc_final, drain
-  static constexpr int kNumBars = 1 + 2 * kStages + 4 + 2;
+  // X/Y buffers in TMEM (128 columns each): three when the accumulators
+  // leave room (D <= 64), so the MMA warp can compute X, Y two blocks ahead.
+  static constexpr int kXYBufs = D <= 64 ? 3 : 2;
+  // a_full, b_full[S], empty[S], xy_full[buffers], p_full[2], acc_final, drain
+  static constexpr int kNumBars = 1 + 2 * kStages + kXYBufs + 2 + 2;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemUsed = kOffMisc + 16;
   static constexpr int kSmemBytes = (kSmemUsed + 1024) > 116 * 1024 ? (kSmemUsed + 1024) : 116 * 1024;
   static constexpr uint32_t kTmemCols = 512;
   // Group g's buffer: X at column 128 g, Y at 128 g + 64 (64 fp32 columns each).
-  static constexpr uint32_t kColAcc1 = 256;      // dV (dK/dV pass) or dQ
-  static constexpr uint32_t kColAcc2 = 256 + D;  // dK (dK/dV pass)
+  static constexpr uint32_t kColAcc1 = 128 * kXYBufs;      // dV (dK/dV pass) or dQ
+  static constexpr uint32_t kColAcc2 = 128 * kXYBufs + D;  // dK (dK/dV pass)
+  static_assert(kColAcc2 + D <= kTmemCols, "TMEM layout");
 };
 
 // TMEM column (relative to a buffer's X or Y) of MMA K-step kk of the 16-bit
 // P or dS block: warp half h wrote partner columns 32h..32h+31 packed into
 // columns 32h..32h+15 of its own 32-column region.
 __device__ __forceinline__ uint32_t packed_col(int kk) { return kk < 2 ? kk * 8 : 32 + (kk - 2) * 8; }
+
+
+// One warp's 32 partner columns of a block: from the scores X and the
+// gradient products Y (fp32, TMEM) form P = exp2(c X - L log2 e) and
+// dS = P o (Y - Delta) and write them back as 16-bit pairs over the columns
+// of X (P, dK/dV pass only) and Y (dS) already read.  In the dK/dV pass each
+// column is a partner query whose L and Delta come from lv, dv; in the dQ
+// pass they are the thread's own row's.  With DIAG the causal mask zeroes
+// partner column c where c < lim (dK/dV pass) or c > lim (dQ pass).
+template <bool BF16, bool KV_OUTER, bool DIAG>
+__device__ __forceinline__ void grad_block(uint32_t tX, uint32_t tY, const float* lv, const float* dv, float2 c2,
+                                           float my_l2, float my_delta, int lim) {
+  constexpr float kLog2e = 1.4426950408889634f;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t xs[16], ys[16];
+    tmem_ld16x2(tX + 16 * h, xs, tY + 16 * h, ys);
+    uint32_t pk[8], dk[8];
+#pragma unroll
+    for (int c = 0; c < 16; c += 2) {
+      const int cc = 16 * h + c;
+      float2 nl2, dl;
+      if constexpr (KV_OUTER) {
+        nl2 = __fmul2_rn(make_float2(lv[cc], lv[cc + 1]), make_float2(-kLog2e, -kLog2e));
+        dl = make_float2(dv[cc], dv[cc + 1]);
+      } else {
+        nl2 = make_float2(-my_l2, -my_l2);
+        dl = make_float2(my_delta, my_delta);
+      }
+      const float2 y = __ffma2_rn(make_float2(__uint_as_float(xs[c]), __uint_as_float(xs[c + 1])), c2, nl2);
+      float2 pr = make_float2(ex2(y.x), ex2(y.y));
+      if constexpr (DIAG) {
+        if (KV_OUTER ? cc < lim : cc > lim) pr.x = 0.f;
+        if (KV_OUTER ? cc + 1 < lim : cc + 1 > lim) pr.y = 0.f;
+      }
+      const float2 gr = __fadd2_rn(make_float2(__uint_as_float(ys[c]), __uint_as_float(ys[c + 1])),
+                                   make_float2(-dl.x, -dl.y));
+      const float2 ds = __fmul2_rn(pr, gr);
+      pk[c / 2] = pack2<BF16>(pr.x, pr.y);
+      dk[c / 2] = pack2<BF16>(ds.x, ds.y);
+    }
+    // 16-bit P (dK/dV pass only) and dS of these 16 columns go to columns
+    // 8h..8h+7 of this warp's region of X and Y, already read.
+    if constexpr (KV_OUTER) tmem_st8(tX + 8 * h, pk);
+    tmem_st8(tY + 8 * h, dk);
+  }
+}
 
 }  // namespace
 
@@ -137,8 +189,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint64_t* bar_afull = bars;
   uint64_t* bar_bfull = bars + 1;
   uint64_t* bar_empty = bar_bfull + L::kStages;
-  uint64_t* bar_xyfull = bar_empty + L::kStages;  // [2]
-  uint64_t* bar_pfull = bar_xyfull + 2;           // [2]
+  uint64_t* bar_xyfull = bar_empty + L::kStages;  // [buffers]
+  uint64_t* bar_pfull = bar_xyfull + L::kXYBufs;  // [2] one per group
   uint64_t* bar_accfinal = bar_pfull + 2;
   uint64_t* bar_drain = bar_accfinal + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
@@ -169,8 +221,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(&bar_bfull[s], KV_OUTER ? 33 : 1);
       mbar_init(&bar_empty[s], 1);
     }
+    for (int b = 0; b < L::kXYBufs; ++b) mbar_init(&bar_xyfull[b], 1);
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&bar_xyfull[b], 1);
       mbar_init(&bar_pfull[b], 8);  // one arrival per warp of the group
     }
     mbar_init(bar_accfinal, 1);
@@ -250,12 +302,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const AccFlags accf = runtime_flags(S);
     const uint64_t a1_desc = make_sdesc(sA1, 16, 8 * GA::kRowBytes, GA::kSwz);
     const uint64_t a2_desc = make_sdesc(sA2, 16, 8 * GA::kRowBytes, GA::kSwz);
-    // X, Y of block i into buffer i & 1 (group i & 1's).  The buffer was last
-    // read by the accumulation of block i - 2, issued earlier by this warp;
-    // the tensor core runs one CTA's MMAs in issue order.
+    // X, Y of block i into buffer i % kXYBufs.  The buffer was last read by the
+    // accumulation of block i - kXYBufs, issued earlier by this warp; the
+    // tensor core runs one CTA's MMAs in issue order.
     auto xy = [&](int i) {
       const int st = i % L::kStages;
-      const uint32_t tb = tmem + 128u * (i & 1);
+      const uint32_t tb = tmem + 128u * (i % L::kXYBufs);
       const uint64_t b1 = make_sdesc(sB1 + st * GB::kTileBytes, 16, 8 * GB::kRowBytes, GB::kSwz);
       const uint64_t b2 = make_sdesc(sB2 + st * GB::kTileBytes, 16, 8 * GB::kRowBytes, GB::kSwz);
 #pragma unroll
@@ -266,13 +318,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int kk = 0; kk < D / 16; ++kk)
         mma_ss_warp(tb + 64, desc_plus(a2_desc, kmajor_step_bytes<D, 128>(kk)),
                     desc_plus(b2, kmajor_step_bytes<D, kPN>(kk)), idesc_xy, kk > 0 ? accf.on : accf.off);
-      mma_commit_warp(&bar_xyfull[i & 1]);
+      mma_commit_warp(&bar_xyfull[i % L::kXYBufs]);
     };
     auto acc = [&](int x) -> bool {
       const int st = x % L::kStages;
       if (!warp_wait(&bar_pfull[x & 1], (x >> 1) & 1, abort_flag, p.err, kErrTimeoutMma)) return false;
       tc_fence_after();
-      const uint32_t tb = tmem + 128u * (x & 1);
+      const uint32_t tb = tmem + 128u * (x % L::kXYBufs);
       const uint64_t b1 = make_sdesc(sB1 + st * GB::kTileBytes, GB::kChunkBytes, 8 * GB::kRowBytes, GB::kSwz);
       const uint64_t b2 = make_sdesc(sB2 + st * GB::kTileBytes, GB::kChunkBytes, 8 * GB::kRowBytes, GB::kSwz);
       if constexpr (KV_OUTER) {
@@ -293,15 +345,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mma_commit_warp(&bar_empty[st]);
       return true;
     };
-    bool ok = warp_wait(bar_afull, 0, abort_flag, p.err, kErrTimeoutMma);
-    for (int i = 0; ok && i < niter; ++i) {
-      ok = warp_wait(&bar_bfull[i % L::kStages], (i / L::kStages) & 1, abort_flag, p.err, kErrTimeoutMma);
-      if (!ok) break;
+    // X, Y run kAhead blocks ahead of the accumulation: X,Y(i + kAhead)
+    // reuses the buffer of block i - 1, whose accumulation was issued in the
+    // previous iteration.
+    constexpr int kAhead = L::kXYBufs - 1;
+    auto issue_xy = [&](int i) -> bool {
+      if (!warp_wait(&bar_bfull[i % L::kStages], (i / L::kStages) & 1, abort_flag, p.err, kErrTimeoutMma))
+        return false;
       tc_fence_after();
       xy(i);
-      if (i >= 1) ok = acc(i - 1);
+      return true;
+    };
+    bool ok = warp_wait(bar_afull, 0, abort_flag, p.err, kErrTimeoutMma);
+    for (int i = 0; ok && i < kAhead && i < niter; ++i) ok = issue_xy(i);
+    for (int i = 0; ok && i < niter; ++i) {
+      if (i + kAhead < niter) ok = issue_xy(i + kAhead);
+      if (ok) ok = acc(i);
     }
-    if (ok && acc(niter - 1)) mma_commit_warp(bar_accfinal);
+    if (ok) mma_commit_warp(bar_accfinal);
     mma_commit_warp(bar_drain);
     drain_wait(bar_drain, 0, p.err);
   } else {
@@ -331,13 +392,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int partner0 = (first + i) * kPN;
       bool ok = true;
       if constexpr (KV_OUTER) ok = warp_wait(&bar_bfull[st], (i / L::kStages) & 1, abort_flag, p.err, kErrTimeoutSoftmax);
-      ok = ok && warp_wait(&bar_xyfull[g], (i >> 1) & 1, abort_flag, p.err, kErrTimeoutSoftmax);
+      ok = ok && warp_wait(&bar_xyfull[i % L::kXYBufs], (i / L::kXYBufs) & 1, abort_flag, p.err, kErrTimeoutSoftmax);
       if (!ok) {
         alive = false;
         break;
       }
       tc_fence_after();
-      const uint32_t tX = tmem + lane_base + 128u * g + col0;
+      const uint32_t tX = tmem + lane_base + 128u * (i % L::kXYBufs) + col0;
       const uint32_t tY = tX + 64;
       const float* lv = vecs + st * 2 * kPN + col0;  // L of this warp's 32 partner queries (dK/dV pass)
       const float* dv = lv + kPN;                    // and their Delta
@@ -347,39 +408,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // mask: their zero-filled operands make their terms vanish (see above).
       const bool diag = p.causal && (KV_OUTER ? partner0 < own0 + 128 : partner0 + kPN - 1 > own0);
       const int lim = my - partner0 - col0;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t xs[16], ys[16];
-        tmem_ld16x2(tX + 16 * h, xs, tY + 16 * h, ys);
-        uint32_t pk[8], dk[8];
-#pragma unroll
-        for (int c = 0; c < 16; c += 2) {
-          const int cc = 16 * h + c;
-          float2 nl2, dl;
-          if constexpr (KV_OUTER) {
-            nl2 = __fmul2_rn(make_float2(lv[cc], lv[cc + 1]), make_float2(-kLog2e, -kLog2e));
-            dl = make_float2(dv[cc], dv[cc + 1]);
-          } else {
-            nl2 = make_float2(-my_l2, -my_l2);
-            dl = make_float2(my_delta, my_delta);
-          }
-          const float2 y = __ffma2_rn(make_float2(__uint_as_float(xs[c]), __uint_as_float(xs[c + 1])), c2, nl2);
-          float2 pr = make_float2(ex2(y.x), ex2(y.y));
-          if (diag) {
-            if (KV_OUTER ? cc < lim : cc > lim) pr.x = 0.f;
-            if (KV_OUTER ? cc + 1 < lim : cc + 1 > lim) pr.y = 0.f;
-          }
-          const float2 gr = __fadd2_rn(make_float2(__uint_as_float(ys[c]), __uint_as_float(ys[c + 1])),
-                                       make_float2(-dl.x, -dl.y));
-          const float2 ds = __fmul2_rn(pr, gr);
-          pk[c / 2] = pack2<BF16>(pr.x, pr.y);
-          dk[c / 2] = pack2<BF16>(ds.x, ds.y);
-        }
-        // 16-bit P (dK/dV pass only) and dS of these 16 columns go to columns
-        // 8h..8h+7 of this warp's region of X and Y, already read.
-        if constexpr (KV_OUTER) tmem_st8(tX + 8 * h, pk);
-        tmem_st8(tY + 8 * h, dk);
-      }
+      // Off-diagonal blocks (all but one or two per tile) take the path with
+      // no per-element compare or select.
+      if (diag)
+        grad_block<BF16, KV_OUTER, true>(tX, tY, lv, dv, c2, my_l2, my_delta, lim);
+      else
+        grad_block<BF16, KV_OUTER, false>(tX, tY, lv, dv, c2, my_l2, my_delta, lim);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();

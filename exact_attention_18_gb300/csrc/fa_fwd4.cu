@@ -8,12 +8,12 @@
 // own softmax warpgroup (thread = query row = TMEM lane, the split-Q partition
 // of "Inside FlashAttention" §4.3), so every SM sub-partition holds four
 // softmax warps whose loads, stores and waits hide behind each other's
-// exponentials.  Key/value blocks are 64 rows.  Warp roles (768 threads):
+// exponentials.  Key/value blocks are 64 rows.  Warp roles (640 threads):
 //   warps 0-15  softmax: warp w serves tile w/4, TMEM lanes 32(w%4)..+31;
 //   warp 16     TMA producer: the four Q tiles once, then K and V blocks
 //               through a ring of shared-memory stages;
-//   warps 17-20 MMA issuers, one per tile;
-//   warps 21-23 idle (warps 16-23 give registers to the softmax warps).
+//   warps 17-18 MMA issuers, for tiles {0, 1} and {2, 3};
+//   warp 19     idle (warps 16-19 give registers to the softmax warps).
 //
 // TMEM (512 columns): tile t owns columns [128t, 128t+128): S_t in the first
 // 64 (fp32 scores of one block), O_t in the next D.  The 16-bit P_t(j) is
@@ -49,8 +49,10 @@ constexpr int kF4BlockN = 64;     // keys per block
 constexpr int kF4RowsPerCta = kF4Tiles * kBlockM;
 constexpr int kF4Producer = 16;
 constexpr int kF4MmaWarp0 = 17;
-// MMA issuers: warp kF4MmaWarp0 + w serves tiles w * kF4TilesPerMma, ...  One
-// warp cannot issue the small (N = 64) products of several tiles fast enough.
+// MMA issuers: warp kF4MmaWarp0 + w serves tiles w * kF4TilesPerMma, ...
+// Measured at D = 64: one warp for all four tiles cannot keep the tensor core
+// fed (each of its MMAs waits behind the last), four (one per tile) cost the
+// softmax warps registers and issue slots; two were fastest.
 constexpr int kF4MmaWarps = 2;
 constexpr int kF4TilesPerMma = kF4Tiles / kF4MmaWarps;
 // Whole warpgroups after the 16 softmax warps: producer + MMA warps + idle.
@@ -63,15 +65,6 @@ constexpr uint32_t kF4RegsHigh = kF4Threads == 640 ? 104 : 96;
 constexpr uint32_t kF4RegsLow = kF4Threads == 640 ? 64 : 48;
 static_assert(512 * kF4RegsHigh + (kF4Threads - 512) * kF4RegsLow <= kF4Threads * kF4LaunchRegs, "register split");
 constexpr float kF4SumLimit = 256.0f;
-// The softmax warps of one SM sub-partition can take turns at the
-// exponentials in groups of kF4TurnGroup tiles (group order within each key
-// block), so one group's exponentials run while the tensor core works on the
-// other group's products (the ping-pong of "Inside FlashAttention" §5.2).
-// Measured on GB300 at D = 64, forced turns (groups of 1 or 2 tiles) were
-// 25-50% slower than free-running warps, so kF4TurnGroup = 4: no turns.
-constexpr int kF4TurnGroup = 4;
-constexpr int kF4TurnGroups = kF4Tiles / kF4TurnGroup;
-constexpr bool kF4Turns = kF4TurnGroups > 1;
 
 template <int D>
 struct F4Layout {
@@ -83,8 +76,8 @@ struct F4Layout {
   static constexpr int kOffK = kOffQ + kF4Tiles * GQ::kTileBytes;
   static constexpr int kOffV = kOffK + kStages * GK::kTileBytes;
   static constexpr int kOffBar = kOffV + kStages * GK::kTileBytes;
-  // q, kfull[S], vfull[S], empty[S], sfull[4], pfull[4], ofinal[4], drain[MMA warps], turn[groups][4]
-  static constexpr int kNumBars = 1 + 3 * kStages + 12 + kF4MmaWarps + 4 * kF4TurnGroups;
+  // q, kfull[S], vfull[S], empty[S], sfull[4], pfull[4], ofinal[4], drain[MMA warps]
+  static constexpr int kNumBars = 1 + 3 * kStages + 12 + kF4MmaWarps;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemUsed = kOffMisc + 16;
   // TMEM is allocated whole (512 columns): the shared-memory request keeps it
@@ -119,7 +112,6 @@ __global__ void __launch_bounds__(kF4Threads, 1)
   uint64_t* bar_pfull = bar_sfull + kF4Tiles;     // [4] P_t(j) stored, O_t rescaled
   uint64_t* bar_ofinal = bar_pfull + kF4Tiles;    // [4] last P V of tile t done
   uint64_t* bar_drain = bar_ofinal + kF4Tiles;    // one per MMA warp
-  uint64_t* bar_turn = bar_drain + kF4MmaWarps;   // [group][lane quarter]: that group's warps may start
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 4);
 
@@ -152,7 +144,6 @@ __global__ void __launch_bounds__(kF4Threads, 1)
       mbar_init(&bar_ofinal[t], 1);
     }
     for (int w = 0; w < kF4MmaWarps; ++w) mbar_init(&bar_drain[w], 1);
-    for (int i = 0; i < 4 * kF4TurnGroups; ++i) mbar_init(&bar_turn[i], kF4TurnGroup);  // the group's warps
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -200,8 +191,8 @@ __global__ void __launch_bounds__(kF4Threads, 1)
       }
     } else if (warp >= kF4MmaWarp0 && warp < kF4MmaWarp0 + kF4MmaWarps) {
       // ------------------------------------------------------------ MMA issuers
-      // Warp kF4MmaWarp0 + w serves tiles w * kF4TilesPerMma, ... (one turn
-      // group).  Each runs converged and one elected lane issues every MMA.
+      // Warp kF4MmaWarp0 + w serves tiles w * kF4TilesPerMma, ... (a contiguous
+      // pair).  Each runs converged and one elected lane issues every MMA.
       const int w = warp - kF4MmaWarp0;
       int nbt[kF4TilesPerMma];
       int nbw = 0;
@@ -300,44 +291,6 @@ __global__ void __launch_bounds__(kF4Threads, 1)
     float m = -INFINITY;  // running (possibly stale) maximum, base-2 scaled
     float l = 0.f;
     bool alive = true;
-    // Turn order on this sub-partition: key block by key block, and within a
-    // block the groups that visit it in group order.  A group takes part in
-    // block j while any of its tiles does; a warp whose tile has finished
-    // keeps passing the turn on for its group (after its epilogue).
-    const int g = t / kF4TurnGroup;
-    int ng[kF4TurnGroups];
-#pragma unroll
-    for (int u = 0; u < kF4TurnGroups; ++u) {
-      ng[u] = 0;
-#pragma unroll
-      for (int v = 0; v < kF4TurnGroup; ++v) ng[u] = max(ng[u], blocks_for(row0 + (u * kF4TurnGroup + v) * kBlockM));
-    }
-    int first = kF4TurnGroups;
-#pragma unroll
-    for (int u = kF4TurnGroups - 1; u >= 0; --u)
-      if (ng[u] > 0) first = u;
-    // The group whose turn follows (g, j), or -1 if the sequence ends there.
-    auto successor = [&](int j) {
-#pragma unroll
-      for (int u = 0; u < kF4TurnGroups; ++u)
-        if (u > g && ng[u] > j) return u;
-#pragma unroll
-      for (int u = 0; u < kF4TurnGroups; ++u)
-        if (ng[u] > j + 1) return u;
-      return -1;
-    };
-    auto wait_turn = [&](int j, int& waited) -> bool {
-      if (g == first && j == 0) return true;
-      const bool ok = warp_wait(&bar_turn[g * 4 + q4], waited & 1, abort_flag, p.err, kErrTimeoutSoftmax);
-      ++waited;
-      return ok;
-    };
-    auto pass_turn = [&](int j) {
-      const int nxt = successor(j);
-      __syncwarp();
-      if (nxt >= 0 && lane == 0) mbar_arrive(&bar_turn[nxt * 4 + q4]);
-    };
-    int turns_waited = 0;
     for (int j = 0; j < nb; ++j) {
       if (!warp_wait(&bar_sfull[t], j & 1, abort_flag, p.err, kErrTimeoutSoftmax)) {
         alive = false;
@@ -379,12 +332,7 @@ __global__ void __launch_bounds__(kF4Threads, 1)
         const float2 a = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
         return a.x + a.y;
       };
-      if (kF4Turns && !wait_turn(j, turns_waited)) {
-        alive = false;
-        break;
-      }
       blk = exps();
-      if (kF4Turns) pass_turn(j);
       // Every P~ <= 2^8 holds if the block's sum does.  Otherwise (or on NaN)
       // the stale m is too far below this block's maximum: move m, rescale,
       // and redo the block.
@@ -434,12 +382,6 @@ __global__ void __launch_bounds__(kF4Threads, 1)
       }
       if (row_ok) p.lse[static_cast<size_t>(bh) * S + row_g] = (m + log2f(l)) * 0.69314718055994530942f;
     }
-    // Blocks this tile does not visit but its group does: pass the turn on.
-    if (kF4Turns && alive)
-      for (int j = nb; j < ng[g]; ++j) {
-        if (!wait_turn(j, turns_waited)) break;
-        pass_turn(j);
-      }
   }
 
   tc_fence_before();
