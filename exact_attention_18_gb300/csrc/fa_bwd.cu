@@ -95,7 +95,9 @@ template <int D>
 struct BwdLayout {
   using GA = TileGeom<D, 128>;
   using GB = TileGeom<D, kPartnerRows>;
-  static constexpr int kStages = 4;
+  // Partner blocks in flight: enough to cover the load latency where shared
+  // memory allows (D <= 64); D = 128 tiles leave room for four.
+  static constexpr int kStages = D <= 64 ? 8 : 4;
   static constexpr int kOffA1 = 0;
   static constexpr int kOffA2 = kOffA1 + GA::kTileBytes;
   static constexpr int kOffB1 = kOffA2 + GA::kTileBytes;             // [kStages] tiles
@@ -166,6 +168,63 @@ __device__ __forceinline__ void grad_block(uint32_t tX, uint32_t tY, const float
     // 8h..8h+7 of this warp's region of X and Y, already read.
     if constexpr (KV_OUTER) tmem_st8(tX + 8 * h, pk);
     tmem_st8(tY + 8 * h, dk);
+  }
+}
+
+
+// The dK/dV pass's version of grad_block, where the partner columns are
+// queries with their own L and Delta.  The 32x32b layout would give every
+// thread all 32 of the warp's columns and so all 32 (L, Delta) pairs from
+// shared memory; with 16x256b loads a thread holds 2 adjacent columns of each
+// of 4 column groups for 4 of the warp's rows (lanes t/4 + 8k), i.e. 8
+// columns, a quarter of the shared-memory reads.  The packed 16-bit results
+// of such a column pair go back with 16x128b stores to packed column
+// (8i + 2(t%4)) / 2 = 4i + t%4, the layout the accumulation MMAs read.
+// lim0: key index of the warp's first row minus its first partner column.
+template <bool BF16, bool DIAG>
+__device__ __forceinline__ void grad_block_kv(uint32_t tX, uint32_t tY, const float* lv, const float* dv, float2 c2,
+                                              int lim0) {
+  constexpr float kLog2e = 1.4426950408889634f;
+  const int lane = threadIdx.x & 31;
+  const int u = lane & 3;   // column pair within each group of 8
+  const int r = lane >> 2;  // first of the thread's rows within 16
+  float2 nl2[4], dl[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 l2 = *reinterpret_cast<const float2*>(lv + 8 * i + 2 * u);
+    nl2[i] = __fmul2_rn(l2, make_float2(-kLog2e, -kLog2e));
+    const float2 d2 = *reinterpret_cast<const float2*>(dv + 8 * i + 2 * u);
+    dl[i] = make_float2(-d2.x, -d2.y);
+  }
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const uint32_t lane_off = static_cast<uint32_t>(16 * half) << 16;
+    uint32_t xs[16], ys[16];
+    tmem_ld16x256b_x4(tX + lane_off, xs);
+    tmem_ld16x256b_x4(tY + lane_off, ys);
+    tmem_ld_wait();
+    uint32_t pk[8], dk[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int e = 4 * i + 2 * k;
+        const float2 y = __ffma2_rn(make_float2(__uint_as_float(xs[e]), __uint_as_float(xs[e + 1])), c2, nl2[i]);
+        float2 pr = make_float2(ex2(y.x), ex2(y.y));
+        if constexpr (DIAG) {
+          const int lim = lim0 + 16 * half + r + 8 * k;  // zero partner columns c < lim (query before key)
+          const int cc = 8 * i + 2 * u;
+          if (cc < lim) pr.x = 0.f;
+          if (cc + 1 < lim) pr.y = 0.f;
+        }
+        const float2 gr = __fadd2_rn(make_float2(__uint_as_float(ys[e]), __uint_as_float(ys[e + 1])), dl[i]);
+        const float2 ds = __fmul2_rn(pr, gr);
+        pk[2 * i + k] = pack2<BF16>(pr.x, pr.y);
+        dk[2 * i + k] = pack2<BF16>(ds.x, ds.y);
+      }
+    }
+    tmem_st16x128b_x4(tX + lane_off, pk);
+    tmem_st16x128b_x4(tY + lane_off, dk);
   }
 }
 
@@ -410,10 +469,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int lim = my - partner0 - col0;
       // Off-diagonal blocks (all but one or two per tile) take the path with
       // no per-element compare or select.
-      if (diag)
-        grad_block<BF16, KV_OUTER, true>(tX, tY, lv, dv, c2, my_l2, my_delta, lim);
-      else
-        grad_block<BF16, KV_OUTER, false>(tX, tY, lv, dv, c2, my_l2, my_delta, lim);
+      if constexpr (KV_OUTER) {
+        const int lim0 = own0 + q4 * 32 - partner0 - col0;
+        if (diag)
+          grad_block_kv<BF16, true>(tX, tY, lv, dv, c2, lim0);
+        else
+          grad_block_kv<BF16, false>(tX, tY, lv, dv, c2, lim0);
+      } else {
+        if (diag)
+          grad_block<BF16, KV_OUTER, true>(tX, tY, lv, dv, c2, my_l2, my_delta, lim);
+        else
+          grad_block<BF16, KV_OUTER, false>(tX, tY, lv, dv, c2, my_l2, my_delta, lim);
+      }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();

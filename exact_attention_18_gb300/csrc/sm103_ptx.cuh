@@ -359,6 +359,30 @@ __device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t* a, uint32_t t
       : "memory");
 }
 
+// 16 lanes x 32 columns as four 16x256b blocks, without the wait: thread t
+// receives, for block i (columns 8i..8i+7) and its lanes t/4 and t/4+8 of the
+// 16, columns 8i + 2(t%4) and 8i + 2(t%4) + 1 as r[4i..4i+3] =
+// (t/4, c), (t/4, c+1), (t/4+8, c), (t/4+8, c+1).
+__device__ __forceinline__ void tmem_ld16x256b_x4(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// 16 lanes x 16 columns as four 16x128b blocks: thread t writes, for block i
+// (columns 4i..4i+3), column 4i + t%4 of lanes t/4 (r[2i]) and t/4+8 (r[2i+1]).
+__device__ __forceinline__ void tmem_st16x128b_x4(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.16x128b.x4.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
