@@ -32,10 +32,10 @@
 //     dK/dV pass: dV += P^T dO_i,  dK += dS^T Q_i    (B = B2, B1 read MN-major)
 //     dQ pass:    dQ += dS K_j                       (B = B1 read MN-major)
 // X and Y of block i live in TMEM buffer i mod kXYBufs (128 columns; three
-// buffers for D <= 64, two for D = 128), and the MMA warp issues X,Y(i + 2)
-// (i + 1 with two buffers) before the accumulation of block i, so a group that
-// finishes block i usually finds block i + 2 already computed, and both groups
-// work while the tensor core runs the products of the blocks around them.  In the dK/dV pass the producer warp also copies the
+// buffers for D <= 64, two for D = 128).  One warp issues X, Y of every block
+// as soon as its tiles and buffer are free, another the accumulations, so a
+// group that finishes block i usually finds block i + 2 already computed, and
+// both groups work while the tensor core runs the products around them.  In the dK/dV pass the producer warp also copies the
 // block's L and Delta (one value per partner query) into the stage with
 // cp.async, completing on the same barrier as the block's tiles.
 #include "fa_kernel_common.cuh"
@@ -88,8 +88,9 @@ namespace {
 constexpr int kPartnerRows = 64;  // rows of a streamed B tile
 constexpr int kBwdGroups = 2;     // softmax-gradient groups of 8 warps; group g takes blocks i = g mod 2
 constexpr int kProducerWarp = 8 * kBwdGroups;
-constexpr int kMmaWarp = kProducerWarp + 1;
-constexpr int kBwdThreads = (kMmaWarp + 1) * 32;
+constexpr int kMmaWarp = kProducerWarp + 1;  // issues the score products X, Y
+constexpr int kAccWarp = kMmaWarp + 1;       // issues the accumulations
+constexpr int kBwdThreads = (kAccWarp + 1) * 32;
 
 template <int D>
 struct BwdLayout {
@@ -107,8 +108,8 @@ struct BwdLayout {
   // X/Y buffers in TMEM (128 columns each): three when the accumulators
   // leave room (D <= 64), so the MMA warp can compute X, Y two blocks ahead.
   static constexpr int kXYBufs = D <= 64 ? 3 : 2;
-  // a_full, b_full[S], empty[S], xy_full[buffers], p_full[2], acc_final, drain
-  static constexpr int kNumBars = 1 + 2 * kStages + kXYBufs + 2 + 2;
+  // a_full, b_full[S], empty[S], xy_full[buffers], acc_issued[buffers], p_full[2], acc_final, drain[2]
+  static constexpr int kNumBars = 1 + 2 * kStages + 2 * kXYBufs + 2 + 1 + 2;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemUsed = kOffMisc + 16;
   static constexpr int kSmemBytes = (kSmemUsed + 1024) > 116 * 1024 ? (kSmemUsed + 1024) : 116 * 1024;
@@ -249,9 +250,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint64_t* bar_bfull = bars + 1;
   uint64_t* bar_empty = bar_bfull + L::kStages;
   uint64_t* bar_xyfull = bar_empty + L::kStages;  // [buffers]
-  uint64_t* bar_pfull = bar_xyfull + L::kXYBufs;  // [2] one per group
+  uint64_t* bar_accissued = bar_xyfull + L::kXYBufs;  // [buffers] accumulation reading it issued
+  uint64_t* bar_pfull = bar_accissued + L::kXYBufs;     // [2] one per group
   uint64_t* bar_accfinal = bar_pfull + 2;
-  uint64_t* bar_drain = bar_accfinal + 1;
+  uint64_t* bar_drain = bar_accfinal + 1;               // [2] one per MMA warp
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 4);
   float* vecs = reinterpret_cast<float*>(smem + L::kOffVec);
@@ -280,12 +282,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(&bar_bfull[s], KV_OUTER ? 33 : 1);
       mbar_init(&bar_empty[s], 1);
     }
-    for (int b = 0; b < L::kXYBufs; ++b) mbar_init(&bar_xyfull[b], 1);
+    for (int b = 0; b < L::kXYBufs; ++b) {
+      mbar_init(&bar_xyfull[b], 1);
+      mbar_init(&bar_accissued[b], 1);
+    }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bar_pfull[b], 8);  // one arrival per warp of the group
     }
     mbar_init(bar_accfinal, 1);
-    mbar_init(bar_drain, 1);
+    mbar_init(&bar_drain[0], 1);
+    mbar_init(&bar_drain[1], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -351,79 +357,82 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (lane == 0) drain_wait(bar_afull, 0, p.err);
     for (int x = (it > L::kStages ? it - L::kStages : 0); x < it; ++x)
       drain_wait(&bar_bfull[x % L::kStages], (x / L::kStages) & 1, p.err);
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer
-    // The whole warp runs this code converged and one elected lane issues
-    // each MMA; descriptors are built once per stage and advanced by
-    // compile-time offsets, so issue keeps pace with the tensor core.
+  } else if (warp == kMmaWarp || warp == kAccWarp) {
+    // ------------------------------------------------------------ MMA issuers
+    // Warp kMmaWarp issues the score products X, Y of every block, warp
+    // kAccWarp the accumulations, so X, Y keep the tensor core busy while the
+    // accumulation of a block waits for its P and dS.  Both run converged and
+    // one elected lane issues each MMA.  X, Y(i) reuse buffer i % kXYBufs,
+    // last read by the accumulation of block i - kXYBufs: kAccWarp signals
+    // acc_issued after issuing it (tcgen05 fences order the two warps' MMAs,
+    // which the tensor core then runs in issue order).
     constexpr uint32_t idesc_xy = make_idesc_f16(BF16, 128, kPN, false, false);
     constexpr uint32_t idesc_acc = make_idesc_f16(BF16, 128, D, false, true);
     const AccFlags accf = runtime_flags(S);
-    const uint64_t a1_desc = make_sdesc(sA1, 16, 8 * GA::kRowBytes, GA::kSwz);
-    const uint64_t a2_desc = make_sdesc(sA2, 16, 8 * GA::kRowBytes, GA::kSwz);
-    // X, Y of block i into buffer i % kXYBufs.  The buffer was last read by the
-    // accumulation of block i - kXYBufs, issued earlier by this warp; the
-    // tensor core runs one CTA's MMAs in issue order.
-    auto xy = [&](int i) {
-      const int st = i % L::kStages;
-      const uint32_t tb = tmem + 128u * (i % L::kXYBufs);
-      const uint64_t b1 = make_sdesc(sB1 + st * GB::kTileBytes, 16, 8 * GB::kRowBytes, GB::kSwz);
-      const uint64_t b2 = make_sdesc(sB2 + st * GB::kTileBytes, 16, 8 * GB::kRowBytes, GB::kSwz);
+    bool ok = true;
+    if (warp == kMmaWarp) {
+      const uint64_t a1_desc = make_sdesc(sA1, 16, 8 * GA::kRowBytes, GA::kSwz);
+      const uint64_t a2_desc = make_sdesc(sA2, 16, 8 * GA::kRowBytes, GA::kSwz);
+      ok = warp_wait(bar_afull, 0, abort_flag, p.err, kErrTimeoutMma);
+      for (int i = 0; ok && i < niter; ++i) {
+        const int st = i % L::kStages;
+        const int b = i % L::kXYBufs;
+        ok = warp_wait(&bar_bfull[st], (i / L::kStages) & 1, abort_flag, p.err, kErrTimeoutMma);
+        if (ok && i >= L::kXYBufs)
+          ok = warp_wait(&bar_accissued[b], ((i / L::kXYBufs) - 1) & 1, abort_flag, p.err, kErrTimeoutMma);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t tb = tmem + 128u * b;
+        const uint64_t b1 = make_sdesc(sB1 + st * GB::kTileBytes, 16, 8 * GB::kRowBytes, GB::kSwz);
+        const uint64_t b2 = make_sdesc(sB2 + st * GB::kTileBytes, 16, 8 * GB::kRowBytes, GB::kSwz);
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk)
-        mma_ss_warp(tb, desc_plus(a1_desc, kmajor_step_bytes<D, 128>(kk)), desc_plus(b1, kmajor_step_bytes<D, kPN>(kk)),
-                    idesc_xy, kk > 0 ? accf.on : accf.off);
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss_warp(tb, desc_plus(a1_desc, kmajor_step_bytes<D, 128>(kk)),
+                      desc_plus(b1, kmajor_step_bytes<D, kPN>(kk)), idesc_xy, kk > 0 ? accf.on : accf.off);
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk)
-        mma_ss_warp(tb + 64, desc_plus(a2_desc, kmajor_step_bytes<D, 128>(kk)),
-                    desc_plus(b2, kmajor_step_bytes<D, kPN>(kk)), idesc_xy, kk > 0 ? accf.on : accf.off);
-      mma_commit_warp(&bar_xyfull[i % L::kXYBufs]);
-    };
-    auto acc = [&](int x) -> bool {
-      const int st = x % L::kStages;
-      if (!warp_wait(&bar_pfull[x & 1], (x >> 1) & 1, abort_flag, p.err, kErrTimeoutMma)) return false;
-      tc_fence_after();
-      const uint32_t tb = tmem + 128u * (x % L::kXYBufs);
-      const uint64_t b1 = make_sdesc(sB1 + st * GB::kTileBytes, GB::kChunkBytes, 8 * GB::kRowBytes, GB::kSwz);
-      const uint64_t b2 = make_sdesc(sB2 + st * GB::kTileBytes, GB::kChunkBytes, 8 * GB::kRowBytes, GB::kSwz);
-      if constexpr (KV_OUTER) {
-#pragma unroll
-        for (int kk = 0; kk < kPN / 16; ++kk)  // dV += P^T dO_i
-          mma_ts_warp(tmem + L::kColAcc1, tb + packed_col(kk), desc_plus(b2, mnmajor_step_bytes<D>(kk)), idesc_acc,
-                      (x > 0 || kk > 0) ? accf.on : accf.off);
-#pragma unroll
-        for (int kk = 0; kk < kPN / 16; ++kk)  // dK += dS^T Q_i
-          mma_ts_warp(tmem + L::kColAcc2, tb + 64 + packed_col(kk), desc_plus(b1, mnmajor_step_bytes<D>(kk)),
-                      idesc_acc, (x > 0 || kk > 0) ? accf.on : accf.off);
-      } else {
-#pragma unroll
-        for (int kk = 0; kk < kPN / 16; ++kk)  // dQ += dS K_j
-          mma_ts_warp(tmem + L::kColAcc1, tb + 64 + packed_col(kk), desc_plus(b1, mnmajor_step_bytes<D>(kk)),
-                      idesc_acc, (x > 0 || kk > 0) ? accf.on : accf.off);
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss_warp(tb + 64, desc_plus(a2_desc, kmajor_step_bytes<D, 128>(kk)),
+                      desc_plus(b2, kmajor_step_bytes<D, kPN>(kk)), idesc_xy, kk > 0 ? accf.on : accf.off);
+        mma_commit_warp(&bar_xyfull[b]);
       }
-      mma_commit_warp(&bar_empty[st]);
-      return true;
-    };
-    // X, Y run kAhead blocks ahead of the accumulation: X,Y(i + kAhead)
-    // reuses the buffer of block i - 1, whose accumulation was issued in the
-    // previous iteration.
-    constexpr int kAhead = L::kXYBufs - 1;
-    auto issue_xy = [&](int i) -> bool {
-      if (!warp_wait(&bar_bfull[i % L::kStages], (i / L::kStages) & 1, abort_flag, p.err, kErrTimeoutMma))
-        return false;
-      tc_fence_after();
-      xy(i);
-      return true;
-    };
-    bool ok = warp_wait(bar_afull, 0, abort_flag, p.err, kErrTimeoutMma);
-    for (int i = 0; ok && i < kAhead && i < niter; ++i) ok = issue_xy(i);
-    for (int i = 0; ok && i < niter; ++i) {
-      if (i + kAhead < niter) ok = issue_xy(i + kAhead);
-      if (ok) ok = acc(i);
+      mma_commit_warp(&bar_drain[0]);
+      drain_wait(&bar_drain[0], 0, p.err);
+    } else {
+      for (int x = 0; ok && x < niter; ++x) {
+        const int st = x % L::kStages;
+        const int b = x % L::kXYBufs;
+        ok = warp_wait(&bar_pfull[x & 1], (x >> 1) & 1, abort_flag, p.err, kErrTimeoutMma);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t tb = tmem + 128u * b;
+        const uint64_t b1 = make_sdesc(sB1 + st * GB::kTileBytes, GB::kChunkBytes, 8 * GB::kRowBytes, GB::kSwz);
+        const uint64_t b2 = make_sdesc(sB2 + st * GB::kTileBytes, GB::kChunkBytes, 8 * GB::kRowBytes, GB::kSwz);
+        if constexpr (KV_OUTER) {
+#pragma unroll
+          for (int kk = 0; kk < kPN / 16; ++kk)  // dV += P^T dO_i
+            mma_ts_warp(tmem + L::kColAcc1, tb + packed_col(kk), desc_plus(b2, mnmajor_step_bytes<D>(kk)), idesc_acc,
+                        (x > 0 || kk > 0) ? accf.on : accf.off);
+#pragma unroll
+          for (int kk = 0; kk < kPN / 16; ++kk)  // dK += dS^T Q_i
+            mma_ts_warp(tmem + L::kColAcc2, tb + 64 + packed_col(kk), desc_plus(b1, mnmajor_step_bytes<D>(kk)),
+                        idesc_acc, (x > 0 || kk > 0) ? accf.on : accf.off);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < kPN / 16; ++kk)  // dQ += dS K_j
+            mma_ts_warp(tmem + L::kColAcc1, tb + 64 + packed_col(kk), desc_plus(b1, mnmajor_step_bytes<D>(kk)),
+                        idesc_acc, (x > 0 || kk > 0) ? accf.on : accf.off);
+        }
+        // The stage's tiles are free once this completes: X, Y(x) finished
+        // before the group could form P and dS.
+        mma_commit_warp(&bar_empty[st]);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_accissued[b]);
+      }
+      if (ok) mma_commit_warp(bar_accfinal);
+      mma_commit_warp(&bar_drain[1]);
+      drain_wait(&bar_drain[1], 0, p.err);
     }
-    if (ok) mma_commit_warp(bar_accfinal);
-    mma_commit_warp(bar_drain);
-    drain_wait(bar_drain, 0, p.err);
   } else {
     // ------------------------------------------------------------ softmax-gradient warps 0-15
     // Group g = warp / 8 turns blocks g, g + 2, ... into P and dS, so two
