@@ -226,6 +226,7 @@ def main():
 
     import torch
     import exact_attention_18_gb300 as fa
+    from exact_attention_18_gb300.sharding import job_throughput, max_over_ranks
     from seeded_inputs import make_inputs
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -303,13 +304,9 @@ def main():
         for n, t in zip(names, ts):
             per[n].append(t)
         step_ms.append(e[0].elapsed_time(e[4]))
-    total_ms = sum(step_ms)
-    if dist is not None:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), dist, dev)
     f_fwd, f_bwd = conv_flops(w)
-    value = world * (f_fwd + f_bwd) * args.steps / (total_ms * 1e-3) / 1e12
+    value = job_throughput(f_fwd + f_bwd, args.steps, world, total_ms) / 1e12
     fwd_ms = statistics.mean(per[names[0]])
     bwd_ms = statistics.mean([a + b + c for a, b, c in zip(per["fa_bwd_preprocess_kernel"],
                                                            per["fa_bwd_dkdv_kernel"], per["fa_bwd_dq_kernel"])])
@@ -370,12 +367,8 @@ def main():
             e2e_step()
         e1.record(stream)
         barrier()
-        e2e_ms = e0.elapsed_time(e1)
-        if dist is not None:
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": world * (f_fwd + f_bwd) * args.steps / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
+        e2e = {"value": job_throughput(f_fwd + f_bwd, args.steps, world, e2e_ms) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps}
     t_wall2 = time.time()
     sampler.stop()
