@@ -118,6 +118,13 @@ struct BwdLayout {
   static constexpr uint32_t kColAcc1 = 128 * kXYBufs;      // dV (dK/dV pass) or dQ
   static constexpr uint32_t kColAcc2 = 128 * kXYBufs + D;  // dK (dK/dV pass)
   static_assert(kColAcc2 + D <= kTmemCols, "TMEM layout");
+  // dQ pass with D <= 64: the resident tiles A1 = Q, A2 = dO are copied into
+  // TMEM (D/2 columns each, after dQ) and the score products read A from
+  // there instead of shared memory (32 instead of 48 cycles per MMA).
+  static constexpr bool kTmemA = D <= 64;
+  static constexpr uint32_t kColA1 = kColAcc1 + D;
+  static constexpr uint32_t kColA2 = kColA1 + D / 2;
+  static_assert(!kTmemA || kColA2 + D / 2 <= kTmemCols, "TMEM layout");
 };
 
 // TMEM column (relative to a buffer's X or Y) of MMA K-step kk of the 16-bit
@@ -374,6 +381,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint64_t a1_desc = make_sdesc(sA1, 16, 8 * GA::kRowBytes, GA::kSwz);
       const uint64_t a2_desc = make_sdesc(sA2, 16, 8 * GA::kRowBytes, GA::kSwz);
       ok = warp_wait(bar_afull, 0, abort_flag, p.err, kErrTimeoutMma);
+      constexpr bool kAFromTmem = !KV_OUTER && L::kTmemA;
+      if (kAFromTmem && ok) {
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          tmem_cp_128x256b_warp(tmem + L::kColA1 + 8 * kk, desc_plus(a1_desc, kmajor_step_bytes<D, 128>(kk)));
+          tmem_cp_128x256b_warp(tmem + L::kColA2 + 8 * kk, desc_plus(a2_desc, kmajor_step_bytes<D, 128>(kk)));
+        }
+      }
       for (int i = 0; ok && i < niter; ++i) {
         const int st = i % L::kStages;
         const int b = i % L::kXYBufs;
@@ -385,14 +401,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t tb = tmem + 128u * b;
         const uint64_t b1 = make_sdesc(sB1 + st * GB::kTileBytes, 16, 8 * GB::kRowBytes, GB::kSwz);
         const uint64_t b2 = make_sdesc(sB2 + st * GB::kTileBytes, 16, 8 * GB::kRowBytes, GB::kSwz);
+        if constexpr (kAFromTmem) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss_warp(tb, desc_plus(a1_desc, kmajor_step_bytes<D, 128>(kk)),
-                      desc_plus(b1, kmajor_step_bytes<D, kPN>(kk)), idesc_xy, kk > 0 ? accf.on : accf.off);
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ts_warp(tb, tmem + L::kColA1 + 8 * kk, desc_plus(b1, kmajor_step_bytes<D, kPN>(kk)), idesc_xy,
+                        kk > 0 ? accf.on : accf.off);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss_warp(tb + 64, desc_plus(a2_desc, kmajor_step_bytes<D, 128>(kk)),
-                      desc_plus(b2, kmajor_step_bytes<D, kPN>(kk)), idesc_xy, kk > 0 ? accf.on : accf.off);
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ts_warp(tb + 64, tmem + L::kColA2 + 8 * kk, desc_plus(b2, kmajor_step_bytes<D, kPN>(kk)), idesc_xy,
+                        kk > 0 ? accf.on : accf.off);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss_warp(tb, desc_plus(a1_desc, kmajor_step_bytes<D, 128>(kk)),
+                        desc_plus(b1, kmajor_step_bytes<D, kPN>(kk)), idesc_xy, kk > 0 ? accf.on : accf.off);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss_warp(tb + 64, desc_plus(a2_desc, kmajor_step_bytes<D, 128>(kk)),
+                        desc_plus(b2, kmajor_step_bytes<D, kPN>(kk)), idesc_xy, kk > 0 ? accf.on : accf.off);
+        }
         mma_commit_warp(&bar_xyfull[b]);
       }
       mma_commit_warp(&bar_drain[0]);

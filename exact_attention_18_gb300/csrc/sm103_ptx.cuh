@@ -211,6 +211,20 @@ __device__ __forceinline__ AccFlags runtime_flags(int nonzero) {
   return AccFlags{on ^ 1u, on};
 }
 
+// Copy a 128-row x 256-bit (16 16-bit elements per row) block, described by a
+// shared-memory matrix descriptor, into TMEM lanes 0-127, 8 columns from
+// `taddr`: row r lands in lane r in element order, the layout an MMA reads as
+// a K-major A operand for one K-step.  Asynchronous; ordered with the
+// tcgen05.mma this thread issues afterwards.  Warp-collective like the MMA
+// issue variants: one elected lane issues it.
+__device__ __forceinline__ void tmem_cp_128x256b_warp(uint32_t taddr, uint64_t s_desc) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t.reg .b32 r;\n\telect.sync r|e, 0xffffffff;\n\t"
+      "@e tcgen05.cp.cta_group::1.128x256b [%0], %1;\n\t}" ::"r"(taddr),
+      "l"(s_desc)
+      : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 MMA this thread issued so far is done.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
