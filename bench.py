@@ -7,7 +7,9 @@ resident in HBM.  Prints ONE JSON line (rank 0):
   value     whole-job TFLOP/s over the timed steps, counting 4*B*H*S^2*D / 2
             (causal) for the forward and 2.5x that for the backward;
   e2e       the same metric through the C ABI with host buffers: every step
-            copies q, k, v, dO from pinned host memory and O, L, dQ, dK, dV back;
+            copies q, k, v, dO from pinned host memory and O, L, dQ, dK, dV back
+            (copy streams and two buffer sets overlap neighbouring steps' copies
+            with the kernels);
   roofline  the dominant kernel's algorithmic FLOPs (or bytes) per launch over
             its CUDA-event duration, against the measured peak;
   cpu_baseline  the fp64 CPU oracle on a bounded sample (rank 0, N = 1).
@@ -337,35 +339,69 @@ def main():
             kernels[n] = {"ms": avg[n], "GB/s": ach, "frac_of_hbm_peak": ach / peaks["hbm_gbs"]}
 
     # ---------------------------------------------------------------- end to end through host buffers
+    # Every step copies its inputs q, k, v, dO from pinned host memory and reads all of its outputs
+    # (O, L, dQ, dK, dV) back, inside the timed region.  Two device buffer sets let the copies of
+    # neighbouring steps (inputs of step i+1 on one copy stream, outputs of step i-1 on another)
+    # overlap step i's kernels, as a training loop would pipeline them.
     e2e = None
     if not args.no_e2e:
         pin = {n: inp[n].pin_memory() for n in ("q", "k", "v", "do")}
-        outs = {"o": torch.empty(o.shape, dtype=o.dtype).pin_memory(),
-                "lse": torch.empty(lse.shape, dtype=lse.dtype).pin_memory(),
-                "dq": torch.empty(q.shape, dtype=q.dtype).pin_memory(),
-                "dk": torch.empty(q.shape, dtype=q.dtype).pin_memory(),
-                "dv": torch.empty(q.shape, dtype=q.dtype).pin_memory()}
+        out_shapes = {"o": (o.shape, o.dtype), "lse": (lse.shape, lse.dtype), "dq": (q.shape, q.dtype),
+                      "dk": (q.shape, q.dtype), "dv": (q.shape, q.dtype)}
+        host_out = [{n: torch.empty(sh, dtype=dt).pin_memory() for n, (sh, dt) in out_shapes.items()}
+                    for _ in range(2)]
+        dev_in = [{"q": q, "k": k, "v": v, "do": do},
+                  {n: torch.empty_like(t) for n, t in (("q", q), ("k", k), ("v", v), ("do", do))}]
+        dev_out = [{"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv},
+                   {n: torch.empty(sh, dtype=dt, device=dev) for n, (sh, dt) in out_shapes.items()}]
         h2d = sum(t.numel() * t.element_size() for t in pin.values())
-        d2h = sum(t.numel() * t.element_size() for t in outs.values())
-        dev_in = {"q": q, "k": k, "v": v, "do": do}
-        dev_out = {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
+        d2h = sum(t.numel() * t.element_size() for t in host_out[0].values())
+        s_h2d, s_d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
-        def e2e_step():
-            for n in pin:
-                dev_in[n].copy_(pin[n], non_blocking=True)
-            step()
-            for n in outs:
-                outs[n].copy_(dev_out[n], non_blocking=True)
+        def run_step(bi, bo):
+            st = fa.fa_fwd(bi["q"].data_ptr(), bi["k"].data_ptr(), bi["v"].data_ptr(), bo["o"].data_ptr(),
+                           bo["lse"].data_ptr(), B, H, S, D, w.causal, w.scale, dt_code, sp)
+            if st:
+                raise RuntimeError(f"fa_fwd: {fa.fa_status_string(st)} {fa.fa_last_error_detail()}")
+            st = fa.fa_bwd(bi["q"].data_ptr(), bi["k"].data_ptr(), bi["v"].data_ptr(), bo["o"].data_ptr(),
+                           bi["do"].data_ptr(), bo["lse"].data_ptr(), bo["dq"].data_ptr(), bo["dk"].data_ptr(),
+                           bo["dv"].data_ptr(), B, H, S, D, w.causal, w.scale, dt_code, ws.data_ptr(), ws_bytes, sp)
+            if st:
+                raise RuntimeError(f"fa_bwd: {fa.fa_status_string(st)} {fa.fa_last_error_detail()}")
 
-        for _ in range(args.warmup):
-            e2e_step()
+        def e2e_run(n):
+            done_compute, done_d2h = [None, None], [None, None]
+            for i in range(n):
+                b = i % 2
+                with torch.cuda.stream(s_h2d):  # inputs of step i (buffer b was last read by step i-2)
+                    if done_compute[b] is not None:
+                        s_h2d.wait_event(done_compute[b])
+                    for name in pin:
+                        dev_in[b][name].copy_(pin[name], non_blocking=True)
+                    h_done = torch.cuda.Event()
+                    h_done.record(s_h2d)
+                stream.wait_event(h_done)
+                if done_d2h[b] is not None:  # outputs of step i-2 have left buffer b
+                    stream.wait_event(done_d2h[b])
+                run_step(dev_in[b], dev_out[b])
+                c_done = torch.cuda.Event()
+                c_done.record(stream)
+                done_compute[b] = c_done
+                with torch.cuda.stream(s_d2h):  # outputs of step i
+                    s_d2h.wait_event(c_done)
+                    for name in host_out[b]:
+                        host_out[b][name].copy_(dev_out[b][name], non_blocking=True)
+                    d_done = torch.cuda.Event()
+                    d_done.record(s_d2h)
+                    done_d2h[b] = d_done
+
+        e2e_run(args.warmup)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier()
-        e0.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
-        e1.record(stream)
+        e0.record(s_h2d)
+        e2e_run(args.steps)
+        e1.record(s_d2h)
         barrier()
         e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
         e2e = {"value": job_throughput(f_fwd + f_bwd, args.steps, world, e2e_ms) / 1e12, "unit": "TFLOP/s",
