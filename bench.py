@@ -17,6 +17,11 @@ resident in HBM.  Prints ONE JSON line (rank 0):
 `--impl reference` times the CPU oracle (the reference arm of this build) on
 the same workload, one (b, h) head per step.
 
+`--workload gqa` / `--workload mqa` run the same measurement on the same shape
+with 2 K/V heads (8 query heads each) or 1 K/V head (grouped-query and
+multi-query attention, fa_fwd_gqa / fa_bwd_gqa); the default is the multi-head
+workload above.
+
 Multi-GPU (torchrun): every rank runs the same workload on its own GPU with no
 data exchange (weak scaling); value = all ranks' FLOPs / max-over-ranks time.
 """
@@ -38,6 +43,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "attention fwd/bwd TFLOPS and % of GB300 FP16 tensor peak (B4 H16 S4096 D64 causal)"
 WORKLOAD = "c2"
+WORKLOADS = ("c2", "gqa", "mqa")
 FLUSH_BYTES = 256 << 20  # > 129 MB L2
 KERNEL_SOURCES = ["exact_attention_18_gb300/csrc/fa_fwd.cu", "exact_attention_18_gb300/csrc/fa_fwd4.cu",
                   "exact_attention_18_gb300/csrc/fa_bwd.cu", "exact_attention_18_gb300/csrc/fa_softmax.cuh",
@@ -155,10 +161,15 @@ class ClockSampler:
 
 
 def cpu_oracle_step(inp, w, heads):
-    """The fp64 oracle forward + backward on the listed (b, h) heads (test infrastructure)."""
+    """The fp64 oracle forward + backward on the listed (b, h) heads (test infrastructure).
+
+    With grouped K/V heads, query head h reads K/V head h // (H / H_kv).
+    """
     import oracle
+    grp = w.H // w.kv_heads
     for b, h in heads:
-        q, k, v, do = (inp[n][b, h] for n in ("q", "k", "v", "do"))
+        q, do = inp["q"][b, h], inp["do"][b, h]
+        k, v = inp["k"][b, h // grp], inp["v"][b, h // grp]
         oracle.forward(q, k, v, w.causal, w.scale)
         oracle.backward(q, k, v, do, w.causal, w.scale)
 
@@ -216,12 +227,16 @@ def main():
     ap.add_argument("--cpu-heads", type=int, default=16, help="heads in the CPU oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--workload", default=WORKLOAD, choices=WORKLOADS)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
+    import dataclasses
     from seeded_inputs import CONFIGS
-    w = CONFIGS[WORKLOAD]
-    w = type(w)(w.name, w.B, w.H, w.S, w.D, w.dtype, w.causal, w.qk_std, True, w.seed)
+    w = dataclasses.replace(CONFIGS[args.workload], backward=True)
+    global METRIC
+    if args.workload != WORKLOAD:
+        METRIC = f"attention fwd/bwd TFLOPS and % of GB300 FP16 tensor peak ({w.describe()})"
     if args.impl == "reference":
         run_reference(args, w)
         return
@@ -250,28 +265,39 @@ def main():
     q, k, v, do = (inp[n].to(dev) for n in ("q", "k", "v", "do"))
     o = torch.empty_like(q)
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
-    ws_bytes = fa.fa_bwd_workspace_size(w.B, w.H, w.S, w.D)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(k)
+    ws_bytes = fa.fa_bwd_gqa_workspace_size(w.B, w.H, w.kv_heads, w.S, w.D)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     sp = stream.cuda_stream
     dt_code = fa.FA_FP16 if w.dtype == "fp16" else fa.FA_BF16
     B, H, S, D = w.B, w.H, w.S, w.D
+    Hkv = w.kv_heads
+
+    def fwd_call(q_, k_, v_, o_, lse_):
+        if Hkv == H:
+            return fa.fa_fwd(q_, k_, v_, o_, lse_, B, H, S, D, w.causal, w.scale, dt_code, sp)
+        return fa.fa_fwd_gqa(q_, k_, v_, o_, lse_, B, H, Hkv, S, D, w.causal, w.scale, dt_code, sp)
+
+    def bwd_call(q_, k_, v_, o_, do_, lse_, dq_, dk_, dv_, marks):
+        if Hkv == H:
+            return fa.fa_bwd_marked(q_, k_, v_, o_, do_, lse_, dq_, dk_, dv_, B, H, S, D, w.causal, w.scale,
+                                    dt_code, ws.data_ptr(), ws_bytes, sp, marks)
+        return fa.fa_bwd_gqa_marked(q_, k_, v_, o_, do_, lse_, dq_, dk_, dv_, B, H, Hkv, S, D, w.causal, w.scale,
+                                    dt_code, ws.data_ptr(), ws_bytes, sp, marks)
 
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        st = fa.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, S, D,
-                       w.causal, w.scale, dt_code, sp)
+        st = fwd_call(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr())
         if st:
-            raise RuntimeError(f"fa_fwd: {fa.fa_status_string(st)} {fa.fa_last_error_detail()}")
+            raise RuntimeError(f"forward: {fa.fa_status_string(st)} {fa.fa_last_error_detail()}")
         marks = None if ev is None else [e.cuda_event for e in ev[1:5]]
-        st = fa.fa_bwd_marked(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
-                              lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, S, D, w.causal,
-                              w.scale, dt_code, ws.data_ptr(), ws_bytes, sp, marks)
+        st = bwd_call(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
+                      dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), marks)
         if st:
-            raise RuntimeError(f"fa_bwd: {fa.fa_status_string(st)} {fa.fa_last_error_detail()}")
+            raise RuntimeError(f"backward: {fa.fa_status_string(st)} {fa.fa_last_error_detail()}")
 
     visible = os.environ.get("CUDA_VISIBLE_DEVICES")
     gpu_id = visible.split(",")[local].strip() if visible else str(local)
@@ -347,7 +373,7 @@ def main():
     if not args.no_e2e:
         pin = {n: inp[n].pin_memory() for n in ("q", "k", "v", "do")}
         out_shapes = {"o": (o.shape, o.dtype), "lse": (lse.shape, lse.dtype), "dq": (q.shape, q.dtype),
-                      "dk": (q.shape, q.dtype), "dv": (q.shape, q.dtype)}
+                      "dk": (k.shape, k.dtype), "dv": (k.shape, k.dtype)}
         host_out = [{n: torch.empty(sh, dtype=dt).pin_memory() for n, (sh, dt) in out_shapes.items()}
                     for _ in range(2)]
         dev_in = [{"q": q, "k": k, "v": v, "do": do},
@@ -359,15 +385,15 @@ def main():
         s_h2d, s_d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
         def run_step(bi, bo):
-            st = fa.fa_fwd(bi["q"].data_ptr(), bi["k"].data_ptr(), bi["v"].data_ptr(), bo["o"].data_ptr(),
-                           bo["lse"].data_ptr(), B, H, S, D, w.causal, w.scale, dt_code, sp)
+            st = fwd_call(bi["q"].data_ptr(), bi["k"].data_ptr(), bi["v"].data_ptr(), bo["o"].data_ptr(),
+                          bo["lse"].data_ptr())
             if st:
-                raise RuntimeError(f"fa_fwd: {fa.fa_status_string(st)} {fa.fa_last_error_detail()}")
-            st = fa.fa_bwd(bi["q"].data_ptr(), bi["k"].data_ptr(), bi["v"].data_ptr(), bo["o"].data_ptr(),
-                           bi["do"].data_ptr(), bo["lse"].data_ptr(), bo["dq"].data_ptr(), bo["dk"].data_ptr(),
-                           bo["dv"].data_ptr(), B, H, S, D, w.causal, w.scale, dt_code, ws.data_ptr(), ws_bytes, sp)
+                raise RuntimeError(f"forward: {fa.fa_status_string(st)} {fa.fa_last_error_detail()}")
+            st = bwd_call(bi["q"].data_ptr(), bi["k"].data_ptr(), bi["v"].data_ptr(), bo["o"].data_ptr(),
+                          bi["do"].data_ptr(), bo["lse"].data_ptr(), bo["dq"].data_ptr(), bo["dk"].data_ptr(),
+                          bo["dv"].data_ptr(), None)
             if st:
-                raise RuntimeError(f"fa_bwd: {fa.fa_status_string(st)} {fa.fa_last_error_detail()}")
+                raise RuntimeError(f"backward: {fa.fa_status_string(st)} {fa.fa_last_error_detail()}")
 
         def e2e_run(n):
             done_compute, done_d2h = [None, None], [None, None]
@@ -420,9 +446,9 @@ def main():
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "fp16", "data": "synthetic",
-            "config": {"workload": w.name, "B": w.B, "H": w.H, "S": w.S, "D": w.D, "causal": w.causal,
-                       "global_batch": w.B * world, "seq_len": w.S, "parallelism": f"independent x{world}",
-                       "step": "fa_fwd + fa_bwd", "l2": "flushed between timed steps (256 MiB write)",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.kv_heads, "S": w.S, "D": w.D,
+                       "causal": w.causal, "global_batch": w.B * world, "seq_len": w.S, "parallelism": f"independent x{world}",
+                       "step": "fa_fwd + fa_bwd" if w.kv_heads == w.H else "fa_fwd_gqa + fa_bwd_gqa", "l2": "flushed between timed steps (256 MiB write)",
                        "flop_convention": "fwd 4*B*H*S^2*D/2 (causal), bwd 2.5x fwd"},
             "fwd": {"ms": fwd_ms, "TFLOP/s": f_fwd / (fwd_ms * 1e-3) / 1e12,
                     "frac_of_tensor_peak": f_fwd / (fwd_ms * 1e-3) / 1e12 / peaks["tensor_tflops"]},

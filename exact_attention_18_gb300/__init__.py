@@ -4,9 +4,12 @@ Argument marshalling only: every step of the attention computation runs in
 the library's CUDA kernels.  PyTorch supplies device memory and streams.
 
 The raw entry points keep the C names and signatures (pointers as ints):
-``fa_fwd``, ``fa_bwd``, ``fa_bwd_marked``, ``fa_bwd_workspace_size``, ``fa_status_string``,
-``fa_last_error_detail``, ``fa_check_device_errors``.  ``forward`` and
-``backward`` wrap them for contiguous [B, H, S, D] CUDA tensors.
+``fa_fwd``, ``fa_fwd_gqa``, ``fa_bwd``, ``fa_bwd_marked``, ``fa_bwd_gqa``,
+``fa_bwd_gqa_marked``, ``fa_bwd_noalloc``, ``fa_bwd_workspace_size``, ``fa_bwd_gqa_workspace_size``,
+``fa_status_string``, ``fa_last_error_detail``, ``fa_check_device_errors``.
+``forward`` and ``backward`` wrap them for contiguous [B, H, S, D] CUDA tensors;
+K and V (and dK, dV) may have fewer heads H_kv dividing H (grouped-query and
+multi-query attention), in which case they call the ``_gqa`` entry points.
 
 The first call loads the compiled library and raises if it has not been built
 (``python -m exact_attention_18_gb300.build``); there is no fallback
@@ -20,7 +23,8 @@ import os
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libfa_gb300.so")
 
-__all__ = ["fa_fwd", "fa_bwd", "fa_bwd_marked", "fa_bwd_noalloc", "fa_bwd_workspace_size", "fa_status_string", "fa_last_error_detail",
+__all__ = ["fa_fwd", "fa_fwd_gqa", "fa_bwd", "fa_bwd_marked", "fa_bwd_gqa", "fa_bwd_gqa_marked", "fa_bwd_noalloc",
+           "fa_bwd_workspace_size", "fa_bwd_gqa_workspace_size", "fa_status_string", "fa_last_error_detail",
            "fa_check_device_errors", "forward", "backward", "FAError", "FA_FP16", "FA_BF16", "STATUS",
            "library_path", "load_library"]
 
@@ -50,6 +54,16 @@ def _load():
     lib.fa_bwd_marked.restype = i32
     lib.fa_bwd_marked.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i32, f32, i32, vp, sz,
                                   vp, ctypes.POINTER(vp)]
+    lib.fa_fwd_gqa.restype = i32
+    lib.fa_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i32, f32, i32, vp]
+    lib.fa_bwd_gqa.restype = i32
+    lib.fa_bwd_gqa.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i32, f32, i32, vp, sz,
+                               vp]
+    lib.fa_bwd_gqa_marked.restype = i32
+    lib.fa_bwd_gqa_marked.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i32, f32, i32, vp,
+                                      sz, vp, ctypes.POINTER(vp)]
+    lib.fa_bwd_gqa_workspace_size.restype = sz
+    lib.fa_bwd_gqa_workspace_size.argtypes = [i64, i64, i64, i64, i64]
     lib.fa_bwd_noalloc.restype = i32
     lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i32, f32, i32, vp]
     lib.fa_status_string.restype = ctypes.c_char_p
@@ -91,6 +105,25 @@ def fa_bwd_marked(q, k, v, o, dout, lse, dq, dk, dv, B, H, S, D, causal, scale, 
                                  int(dtype), workspace, workspace_bytes, stream, arr)
 
 
+def fa_fwd_gqa(q, k, v, o, lse, B, H, H_kv, S, D, causal, scale, dtype, stream) -> int:
+    return _load().fa_fwd_gqa(q, k, v, o, lse, B, H, H_kv, S, D, int(causal), float(scale), int(dtype), stream)
+
+
+def fa_bwd_gqa(q, k, v, o, dout, lse, dq, dk, dv, B, H, H_kv, S, D, causal, scale, dtype, workspace,
+               workspace_bytes, stream) -> int:
+    return _load().fa_bwd_gqa(q, k, v, o, dout, lse, dq, dk, dv, B, H, H_kv, S, D, int(causal), float(scale),
+                              int(dtype), workspace, workspace_bytes, stream)
+
+
+def fa_bwd_gqa_marked(q, k, v, o, dout, lse, dq, dk, dv, B, H, H_kv, S, D, causal, scale, dtype, workspace,
+                      workspace_bytes, stream, marks) -> int:
+    arr = None
+    if marks is not None:
+        arr = (ctypes.c_void_p * 4)(*[m if m else None for m in marks])
+    return _load().fa_bwd_gqa_marked(q, k, v, o, dout, lse, dq, dk, dv, B, H, H_kv, S, D, int(causal),
+                                     float(scale), int(dtype), workspace, workspace_bytes, stream, arr)
+
+
 def fa_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, B, H, S, D, causal, scale, dtype, stream) -> int:
     """fa_bwd for callers that cannot allocate: its scratch is a fixed array inside the library."""
     return _load().fa_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, B, H, S, D, int(causal), float(scale),
@@ -99,6 +132,10 @@ def fa_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, B, H, S, D, causal, scale,
 
 def fa_bwd_workspace_size(B, H, S, D) -> int:
     return _load().fa_bwd_workspace_size(B, H, S, D)
+
+
+def fa_bwd_gqa_workspace_size(B, H, H_kv, S, D) -> int:
+    return _load().fa_bwd_gqa_workspace_size(B, H, H_kv, S, D)
 
 
 def fa_status_string(status: int) -> str:
@@ -148,20 +185,37 @@ def _bhsd(x, name):
     return x
 
 
+def _kv_heads(q, k, v):
+    """H_kv of K, V [B, H_kv, S, D] against Q [B, H, S, D]; H must be a multiple of H_kv."""
+    B, H, S, D = q.shape
+    hk = k.shape[1]
+    grouped = hk == H == 0 or (hk >= 1 and H % hk == 0)
+    if k.shape != (B, hk, S, D) or v.shape != k.shape or k.dtype != q.dtype or v.dtype != q.dtype or not grouped:
+        raise ValueError("k and v must be [B, H_kv, S, D] with H_kv dividing H, in q's dtype")
+    return hk
+
+
 def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None, stream=None):
-    """O and fp32 natural-log LSE of exact attention; tensors [B, H, S, D] (or [B, S, D])."""
+    """O and fp32 natural-log LSE of exact attention; tensors [B, H, S, D] (or [B, S, D]).
+
+    K and V may have H_kv heads with H a multiple of H_kv (grouped-query
+    attention; query head h reads K/V head h // (H // H_kv)).
+    """
     import torch
     squeeze = q.dim() == 3
     q, k, v = _bhsd(q, "q"), _bhsd(k, "k"), _bhsd(v, "v")
-    if k.shape != q.shape or v.shape != q.shape or k.dtype != q.dtype or v.dtype != q.dtype:
-        raise ValueError("q, k, v must share shape and dtype")
     B, H, S, D = q.shape
+    hk = _kv_heads(q, k, v)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     o = torch.empty_like(q) if out is None else out.view(q.shape)
     l = torch.empty((B, H, S), dtype=torch.float32, device=q.device) if lse is None else lse.view(B, H, S)
-    _check(fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), l.data_ptr(), B, H, S, D, causal,
-                  scale, _dtype_code(q), _stream_ptr(stream)), "fa_fwd")
+    if hk == H:
+        _check(fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), l.data_ptr(), B, H, S, D, causal,
+                      scale, _dtype_code(q), _stream_ptr(stream)), "fa_fwd")
+    else:
+        _check(fa_fwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), l.data_ptr(), B, H, hk, S, D,
+                          causal, scale, _dtype_code(q), _stream_ptr(stream)), "fa_fwd_gqa")
     if squeeze:
         return o.squeeze(1), l.squeeze(1)
     return o, l
@@ -169,24 +223,34 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
 
 def backward(q, k, v, o, do, lse, causal: bool = False, scale: float | None = None, dq=None, dk=None, dv=None,
              workspace=None, stream=None):
-    """dQ, dK, dV of exact attention from the forward's O and LSE (recompute backward)."""
+    """dQ, dK, dV of exact attention from the forward's O and LSE (recompute backward).
+
+    With K, V of H_kv < H heads, dK and dV have H_kv heads and sum over each
+    K/V head's group of query heads.
+    """
     import torch
     squeeze = q.dim() == 3
     q, k, v, o, do = (_bhsd(x, n) for x, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (do, "do")))
     B, H, S, D = q.shape
+    hk = _kv_heads(q, k, v)
+    if o.shape != q.shape or do.shape != q.shape:
+        raise ValueError("o and do must have q's shape")
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     lse = lse.reshape(B, H, S)
     dq = torch.empty_like(q) if dq is None else dq.view(q.shape)
-    dk = torch.empty_like(q) if dk is None else dk.view(q.shape)
-    dv = torch.empty_like(q) if dv is None else dv.view(q.shape)
-    need = fa_bwd_workspace_size(B, H, S, D)
+    dk = torch.empty_like(k) if dk is None else dk.view(k.shape)
+    dv = torch.empty_like(k) if dv is None else dv.view(k.shape)
+    need = fa_bwd_gqa_workspace_size(B, H, hk, S, D) if hk else 0
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
-    _check(fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
-                  dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, S, D, causal, scale, _dtype_code(q),
-                  workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_ptr(stream)),
-           "fa_bwd")
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
+            dq.data_ptr(), dk.data_ptr(), dv.data_ptr())
+    ws = (workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_ptr(stream))
+    if hk == H:
+        _check(fa_bwd(*args, B, H, S, D, causal, scale, _dtype_code(q), *ws), "fa_bwd")
+    else:
+        _check(fa_bwd_gqa(*args, B, H, hk, S, D, causal, scale, _dtype_code(q), *ws), "fa_bwd_gqa")
     if squeeze:
         return dq.squeeze(1), dk.squeeze(1), dv.squeeze(1)
     return dq, dk, dv

@@ -150,15 +150,23 @@ fa_status from_cuda(cudaError_t e, const char* what) {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
-}  // namespace
+// Grouped heads: H_kv K/V heads, each shared by H / H_kv consecutive query
+// heads.  H_kv = H is ordinary multi-head attention.
+fa_status check_heads(int64_t H, int64_t H_kv) {
+  if (H_kv < 0 || H_kv > H) return fail(FA_ERR_INVALID_ARG, "H_kv=%lld must lie in [0, H=%lld]",
+                                        (long long)H_kv, (long long)H);
+  if (H > 0 && (H_kv == 0 || H % H_kv != 0))
+    return fail(FA_ERR_INVALID_ARG, "H=%lld is not a multiple of H_kv=%lld", (long long)H, (long long)H_kv);
+  if (H == 0 && H_kv != 0) return fail(FA_ERR_INVALID_ARG, "H_kv=%lld with H=0", (long long)H_kv);
+  return FA_OK;
+}
 
-extern "C" {
-
-fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H, int64_t S,
-                 int64_t D, int causal, float scale, fa_dtype dtype, void* stream) {
+fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
+                   int64_t H_kv, int64_t S, int64_t D, int causal, float scale, fa_dtype dtype, void* stream) {
   g_detail[0] = 0;
   fa_status st = check_common(B, H, S, D, scale, dtype);
   if (st != FA_OK) return st;
+  if ((st = check_heads(H, H_kv))) return st;
   const int64_t BH = B * H;
   if (BH == 0 || S == 0) return FA_OK;  // empty: nothing is read or written, pointers may be NULL
   if ((st = check_ptr(q, "q")) || (st = check_ptr(k, "k")) || (st = check_ptr(v, "v")) ||
@@ -167,8 +175,10 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   const bool bf16 = dtype == FA_BF16;
   // Q in 128-row boxes (a CTA's own tiles); K and V in 64-row boxes.
   CUtensorMap tq, tk, tv;
-  if ((st = encode_qkv_map(&tq, q, bf16, D, S, BH, "q")) || (st = encode_qkv_map(&tk, k, bf16, D, S, BH, "k", 64)) ||
-      (st = encode_qkv_map(&tv, v, bf16, D, S, BH, "v", 64)))
+  const int64_t BHkv = B * H_kv;
+  if ((st = encode_qkv_map(&tq, q, bf16, D, S, BH, "q")) ||
+      (st = encode_qkv_map(&tk, k, bf16, D, S, BHkv, "k", 64)) ||
+      (st = encode_qkv_map(&tv, v, bf16, D, S, BHkv, "v", 64)))
     return st;
   fa::FwdParams p;
   p.o = o;
@@ -177,6 +187,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   const int rows_per_cta = fa::fwd_rows_per_cta(static_cast<int>(D));
   p.n_m_tiles = static_cast<int>((S + rows_per_cta - 1) / rows_per_cta);  // CTAs per (b, h)
   p.causal = causal ? 1 : 0;
+  p.group = static_cast<int>(H / H_kv);
   p.scale_log2 = scale * kLog2e;
   p.err = fa::device_error_word();
   if (!p.err) return fail(FA_ERR_CUDA, "cannot resolve the device error word on the current device");
@@ -185,11 +196,53 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                    "forward launch");
 }
 
+fa_status bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                   void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t H_kv, int64_t S, int64_t D,
+                   int causal, float scale, fa_dtype dtype, void* workspace, size_t workspace_bytes,
+                   void* stream, void* const* marks);
+
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Backward workspace: the fp32 row vector Delta of every query row, then, when
+// the dK/dV pass splits a K/V head's query heads over several CTAs, their fp32
+// partial [dV | dK] rows.  Sizes must already be validated (H_kv divides H).
+size_t bwd_workspace_layout(int64_t B, int64_t H, int64_t H_kv, int64_t S, int64_t D, int* splits,
+                            size_t* delta_bytes) {
+  *splits = 1;
+  *delta_bytes = 0;
+  if (B <= 0 || H <= 0 || S <= 0 || H_kv <= 0) return 0;
+  *delta_bytes = round256(static_cast<size_t>(B) * static_cast<size_t>(H) * static_cast<size_t>(S) * sizeof(float));
+  *splits = fa::bwd_kv_splits(B * H_kv, (S + 127) / 128, static_cast<int>(H / H_kv));
+  if (*splits == 1) return *delta_bytes;
+  return *delta_bytes + round256(static_cast<size_t>(*splits) * static_cast<size_t>(B * H_kv) *
+                                 static_cast<size_t>(S) * static_cast<size_t>(2 * D) * sizeof(float));
+}
+
+}  // namespace
+
+extern "C" {
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H, int64_t S,
+                 int64_t D, int causal, float scale, fa_dtype dtype, void* stream) {
+  return fwd_impl(q, k, v, o, lse, B, H, H, S, D, causal, scale, dtype, stream);
+}
+
+fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
+                     int64_t H_kv, int64_t S, int64_t D, int causal, float scale, fa_dtype dtype, void* stream) {
+  return fwd_impl(q, k, v, o, lse, B, H, H_kv, S, D, causal, scale, dtype, stream);
+}
+
 size_t fa_bwd_workspace_size(int64_t B, int64_t H, int64_t S, int64_t D) {
-  (void)D;
-  if (B <= 0 || H <= 0 || S <= 0) return 0;
-  const size_t bytes = static_cast<size_t>(B) * static_cast<size_t>(H) * static_cast<size_t>(S) * sizeof(float);
-  return (bytes + 255) & ~static_cast<size_t>(255);
+  int splits = 1;
+  size_t delta_bytes = 0;
+  return bwd_workspace_layout(B, H, H, S, D, &splits, &delta_bytes);
+}
+
+size_t fa_bwd_gqa_workspace_size(int64_t B, int64_t H, int64_t H_kv, int64_t S, int64_t D) {
+  if (H_kv <= 0 || H <= 0 || H % H_kv != 0) return 0;
+  int splits = 1;
+  size_t delta_bytes = 0;
+  return bwd_workspace_layout(B, H, H_kv, S, D, &splits, &delta_bytes);
 }
 
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
@@ -203,16 +256,48 @@ fa_status fa_bwd_marked(const void* q, const void* k, const void* v, const void*
                         const float* lse, void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t S, int64_t D,
                         int causal, float scale, fa_dtype dtype, void* workspace, size_t workspace_bytes,
                         void* stream, void* const* marks) {
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, B, H, H, S, D, causal, scale, dtype, workspace,
+                  workspace_bytes, stream, marks);
+}
+
+fa_status fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                     void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t H_kv, int64_t S, int64_t D,
+                     int causal, float scale, fa_dtype dtype, void* workspace, size_t workspace_bytes,
+                     void* stream) {
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, B, H, H_kv, S, D, causal, scale, dtype, workspace,
+                  workspace_bytes, stream, nullptr);
+}
+
+fa_status fa_bwd_gqa_marked(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                            const float* lse, void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t H_kv,
+                            int64_t S, int64_t D, int causal, float scale, fa_dtype dtype, void* workspace,
+                            size_t workspace_bytes, void* stream, void* const* marks) {
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, B, H, H_kv, S, D, causal, scale, dtype, workspace,
+                  workspace_bytes, stream, marks);
+}
+
+}  // extern "C"
+
+namespace {
+
+fa_status bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                   void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t H_kv, int64_t S, int64_t D,
+                   int causal, float scale, fa_dtype dtype, void* workspace, size_t workspace_bytes,
+                   void* stream, void* const* marks) {
   g_detail[0] = 0;
   fa_status st = check_common(B, H, S, D, scale, dtype);
   if (st != FA_OK) return st;
+  if ((st = check_heads(H, H_kv))) return st;
   const int64_t BH = B * H;
+  const int64_t BHkv = B * H_kv;
   if (BH == 0 || S == 0) return FA_OK;  // empty: nothing is read or written, pointers may be NULL
   if ((st = check_ptr(q, "q")) || (st = check_ptr(k, "k")) || (st = check_ptr(v, "v")) ||
       (st = check_ptr(o, "o")) || (st = check_ptr(dout, "dout")) || (st = check_ptr(lse, "lse")) ||
       (st = check_ptr(dq, "dq")) || (st = check_ptr(dk, "dk")) || (st = check_ptr(dv, "dv")))
     return st;
-  const size_t need = fa_bwd_workspace_size(B, H, S, D);
+  int splits = 1;
+  size_t delta_bytes = 0;
+  const size_t need = bwd_workspace_layout(B, H, H_kv, S, D, &splits, &delta_bytes);
   if (!workspace) return fail(FA_ERR_WORKSPACE, "workspace is NULL (%zu bytes needed)", need);
   if (workspace_bytes < need)
     return fail(FA_ERR_WORKSPACE, "workspace has %zu bytes, %zu needed", workspace_bytes, need);
@@ -221,12 +306,12 @@ fa_status fa_bwd_marked(const void* q, const void* k, const void* v, const void*
   const bool bf16 = dtype == FA_BF16;
   fa::BwdMaps maps;
   if ((st = encode_qkv_map(&maps.q128, q, bf16, D, S, BH, "q")) ||
-      (st = encode_qkv_map(&maps.k128, k, bf16, D, S, BH, "k")) ||
-      (st = encode_qkv_map(&maps.v128, v, bf16, D, S, BH, "v")) ||
+      (st = encode_qkv_map(&maps.k128, k, bf16, D, S, BHkv, "k")) ||
+      (st = encode_qkv_map(&maps.v128, v, bf16, D, S, BHkv, "v")) ||
       (st = encode_qkv_map(&maps.do128, dout, bf16, D, S, BH, "dout")) ||
       (st = encode_qkv_map(&maps.q64, q, bf16, D, S, BH, "q", 64)) ||
-      (st = encode_qkv_map(&maps.k64, k, bf16, D, S, BH, "k", 64)) ||
-      (st = encode_qkv_map(&maps.v64, v, bf16, D, S, BH, "v", 64)) ||
+      (st = encode_qkv_map(&maps.k64, k, bf16, D, S, BHkv, "k", 64)) ||
+      (st = encode_qkv_map(&maps.v64, v, bf16, D, S, BHkv, "v", 64)) ||
       (st = encode_qkv_map(&maps.do64, dout, bf16, D, S, BH, "dout", 64)))
     return st;
   fa::BwdParams p;
@@ -239,6 +324,9 @@ fa_status fa_bwd_marked(const void* q, const void* k, const void* v, const void*
   p.dv = dv;
   p.S = static_cast<int>(S);
   p.BH = static_cast<int>(BH);
+  p.group = static_cast<int>(H / H_kv);
+  p.kv_splits = splits;
+  p.dkv_part = splits > 1 ? reinterpret_cast<float*>(static_cast<char*>(workspace) + delta_bytes) : nullptr;
   p.n_tiles = static_cast<int>((S + 127) / 128);
   p.n_partner = static_cast<int>((S + 63) / 64);
   p.causal = causal ? 1 : 0;
@@ -256,10 +344,16 @@ fa_status fa_bwd_marked(const void* q, const void* k, const void* v, const void*
   if ((st = from_cuda(fa::launch_bwd_preprocess(Di, bf16, p, s), "backward preprocess launch"))) return st;
   if ((st = mark(1))) return st;
   if ((st = from_cuda(fa::launch_bwd_dkdv(Di, bf16, maps, p, s), "backward dK/dV launch"))) return st;
+  if (splits > 1 && (st = from_cuda(fa::launch_bwd_dkv_reduce(Di, bf16, p, s), "backward dK/dV reduce launch")))
+    return st;
   if ((st = mark(2))) return st;
   if ((st = from_cuda(fa::launch_bwd_dq(Di, bf16, maps, p, s), "backward dQ launch"))) return st;
   return mark(3);
 }
+
+}  // namespace
+
+extern "C" {
 
 fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dout,
                          const float* lse, void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t S,

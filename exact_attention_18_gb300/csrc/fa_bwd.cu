@@ -83,6 +83,36 @@ __global__ void __launch_bounds__(256) fa_bwd_preprocess_kernel(const BwdParams 
   }
 }
 
+// ------------------------------------------------------------------ dK/dV partial sums
+// dV, dK = sum over the kv_splits partials (fixed order, fp32), rounded once.
+// One thread per 8 consecutive columns of a [dV | scale*dK] row.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256) fa_bwd_dkv_reduce_kernel(const BwdParams p, int64_t rows) {
+  constexpr int kG = 2 * D / 8;  // 8-column groups per row
+  const int64_t n = rows * kG;
+  const int64_t part_stride = rows * 2 * D;
+  for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < n;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t row = e / kG;
+    const int cg = static_cast<int>(e - row * kG);
+    const float* src = p.dkv_part + row * 2 * D + cg * 8;
+    float4 a = reinterpret_cast<const float4*>(src)[0];
+    float4 b = reinterpret_cast<const float4*>(src)[1];
+    for (int sp = 1; sp < p.kv_splits; ++sp) {
+      const float4 a2 = reinterpret_cast<const float4*>(src + sp * part_stride)[0];
+      const float4 b2 = reinterpret_cast<const float4*>(src + sp * part_stride)[1];
+      a.x += a2.x; a.y += a2.y; a.z += a2.z; a.w += a2.w;
+      b.x += b2.x; b.y += b2.y; b.z += b2.z; b.w += b2.w;
+    }
+    const uint4 w = make_uint4(pack2<BF16>(a.x, a.y), pack2<BF16>(a.z, a.w), pack2<BF16>(b.x, b.y),
+                               pack2<BF16>(b.z, b.w));
+    const bool is_dv = cg < D / 8;
+    void* out = is_dv ? p.dv : p.dk;
+    const int col = (is_dv ? cg : cg - D / 8) * 8;
+    reinterpret_cast<uint4*>(static_cast<char*>(out) + (row * D + col) * 2)[0] = w;
+  }
+}
+
 namespace {
 
 constexpr int kPartnerRows = 64;  // rows of a streamed B tile
@@ -267,7 +297,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int bh = blockIdx.x;
+  // Head of the CTA's own tiles: a K/V head in the dK/dV pass, a query head in
+  // the dQ pass.  K/V head h serves query heads h*group .. h*group+group-1; in
+  // the dK/dV pass kv_splits CTAs share a K/V head, CTA `kv_part` taking the
+  // group's heads kv_part*hpc .. kv_part*hpc+hpc-1.
+  const int bh = KV_OUTER ? static_cast<int>(blockIdx.x) / p.kv_splits : static_cast<int>(blockIdx.x);
+  const int kv_part = KV_OUTER ? static_cast<int>(blockIdx.x) - bh * p.kv_splits : 0;
+  const int hpc = KV_OUTER ? p.group / p.kv_splits : 1;
   const int S = p.S;
   const int nt = p.n_tiles;
   const int np = p.n_partner;
@@ -279,7 +315,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int own0 = own * 128;
   const int first = (KV_OUTER && p.causal) ? own0 / kPN : 0;
   const int last_excl = (!KV_OUTER && p.causal) ? min(np, (own0 + 127) / kPN + 1) : np;
-  const int niter = last_excl - first;
+  // Partner blocks per partner head; the dK/dV pass streams them for each of
+  // the group's query heads in turn and sums over all of them.
+  const int nper = last_excl - first;
+  const int niter = KV_OUTER ? hpc * nper : nper;
 
   if (threadIdx.x == 0) {
     mbar_init(bar_afull, 1);
@@ -333,19 +372,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     }
     int it = 0;
-    for (; it < niter; ++it) {
+    // Partner head and block of iteration `it`, stepped along without divisions.
+    int pz = KV_OUTER ? bh * p.group + kv_part * hpc : bh / p.group;
+    int pblk = first;
+    for (; it < niter; ++it, ++pblk) {
+      if (KV_OUTER && pblk == last_excl) {
+        pblk = first;
+        ++pz;
+      }
       const int st = it % L::kStages;
       const int use = it / L::kStages;
       if (use > 0 && !warp_wait(&bar_empty[st], (use - 1) & 1, abort_flag, p.err, kErrTimeoutLoad)) break;
-      const int r0 = (first + it) * kPN;
+      const int r0 = pblk * kPN;
       if (lane == 0) {
         mbar_arrive_expect_tx(&bar_bfull[st], 2 * GB::kTileBytes);
 #pragma unroll
         for (int ch = 0; ch < GB::kChunks; ++ch) {
           tma_load_3d(smem + L::kOffB1 + st * GB::kTileBytes + ch * GB::kChunkBytes, &tm_b1, &bar_bfull[st],
-                      ch * (GB::kRowBytes / 2), r0, bh);
+                      ch * (GB::kRowBytes / 2), r0, pz);
           tma_load_3d(smem + L::kOffB2 + st * GB::kTileBytes + ch * GB::kChunkBytes, &tm_b2, &bar_bfull[st],
-                      ch * (GB::kRowBytes / 2), r0, bh);
+                      ch * (GB::kRowBytes / 2), r0, pz);
         }
       }
       if constexpr (KV_OUTER) {
@@ -353,7 +399,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int h = 0; h < kPN; h += 32) {
           const int q = r0 + h + lane;
-          const int64_t src = rowbase + (q < S ? q : S - 1);
+          const int64_t src = static_cast<int64_t>(pz) * S + (q < S ? q : S - 1);
           cp_async_4(v + h + lane, p.lse + src, q < S);
           cp_async_4(v + kPN + h + lane, p.delta + src, q < S);
         }
@@ -482,9 +528,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       my_delta = p.delta[rowbase + my];
     }
     bool alive = true;
+    int pi = g;  // i modulo nper: the partner block within its head (dK/dV pass)
+    if constexpr (KV_OUTER) {
+      while (pi >= nper) pi -= nper;
+    }
     for (int i = g; i < niter; i += kBwdGroups) {
       const int st = i % L::kStages;
-      const int partner0 = (first + i) * kPN;
+      const int partner0 = (first + (KV_OUTER ? pi : i)) * kPN;
+      if constexpr (KV_OUTER) {
+        pi += kBwdGroups;
+        while (pi >= nper) pi -= nper;
+      }
       bool ok = true;
       if constexpr (KV_OUTER) ok = warp_wait(&bar_bfull[st], (i / L::kStages) & 1, abort_flag, p.err, kErrTimeoutSoftmax);
       ok = ok && warp_wait(&bar_xyfull[i % L::kXYBufs], (i / L::kXYBufs) & 1, abort_flag, p.err, kErrTimeoutSoftmax);
@@ -528,23 +582,38 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // four parts of at least 16 columns.
     constexpr int kParts = D >= 64 ? 4 : D / 16;
     constexpr int kEpiCols = D / kParts;
-    const int part = warp >> 2;
-    if (__all_sync(0xffffffffu, done) && part < kParts) {
+    const int col_part = warp >> 2;
+    if (__all_sync(0xffffffffu, done) && col_part < kParts) {
       tc_fence_after();
-      const int c_begin = part * kEpiCols;
+      const int c_begin = col_part * kEpiCols;
       const bool row_ok = my < S;
       const size_t off = (static_cast<size_t>(rowbase) + (row_ok ? my : 0)) * D;
       const uint32_t t_acc = tmem + lane_base;
       if constexpr (KV_OUTER) {
-        elem_t* dv_row = reinterpret_cast<elem_t*>(p.dv) + off;
-        elem_t* dk_row = reinterpret_cast<elem_t*>(p.dk) + off;
+        if (p.kv_splits == 1) {
+          elem_t* dv_row = reinterpret_cast<elem_t*>(p.dv) + off;
+          elem_t* dk_row = reinterpret_cast<elem_t*>(p.dk) + off;
 #pragma unroll
-        for (int c = c_begin; c < c_begin + kEpiCols; c += 16) {
-          uint32_t v16[16];
-          tmem_ld16(t_acc + L::kColAcc1 + c, v16);
-          if (row_ok) store_row16<BF16>(dv_row + c, v16, 1.f);
-          tmem_ld16(t_acc + L::kColAcc2 + c, v16);
-          if (row_ok) store_row16<BF16>(dk_row + c, v16, p.scale);
+          for (int c = c_begin; c < c_begin + kEpiCols; c += 16) {
+            uint32_t v16[16];
+            tmem_ld16(t_acc + L::kColAcc1 + c, v16);
+            if (row_ok) store_row16<BF16>(dv_row + c, v16, 1.f);
+            tmem_ld16(t_acc + L::kColAcc2 + c, v16);
+            if (row_ok) store_row16<BF16>(dk_row + c, v16, p.scale);
+          }
+        } else {
+          // This CTA's share of the group: fp32 rows [dV | scale * dK] of
+          // partial `kv_part`, summed by the reduce kernel.
+          const int64_t n_rows = static_cast<int64_t>(p.BH / p.group) * S;
+          float* prow = p.dkv_part + ((static_cast<int64_t>(kv_part) * n_rows + rowbase + (row_ok ? my : 0)) * (2 * D));
+#pragma unroll
+          for (int c = c_begin; c < c_begin + kEpiCols; c += 16) {
+            uint32_t v16[16];
+            tmem_ld16(t_acc + L::kColAcc1 + c, v16);
+            if (row_ok) store_row16_f32(prow + c, v16, 1.f);
+            tmem_ld16(t_acc + L::kColAcc2 + c, v16);
+            if (row_ok) store_row16_f32(prow + D + c, v16, p.scale);
+          }
         }
       } else {
         elem_t* dq_row = reinterpret_cast<elem_t*>(p.dq) + off;
@@ -585,12 +654,31 @@ cudaError_t launch_main_t(const CUtensorMap& a1, const CUtensorMap& a2, const CU
   auto kern = fa_bwd_main_kernel<D, BF16, KV_OUTER>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.BH, p.n_tiles);
+  // dK/dV pass: kv_splits CTAs per (K/V head, key tile); dQ pass: one per (query head, query tile).
+  dim3 grid(KV_OUTER ? p.BH / p.group * p.kv_splits : p.BH, p.n_tiles);
   kern<<<grid, kBwdThreads, L::kSmemBytes, stream>>>(a1, a2, b1, b2, p);
   return cudaGetLastError();
 }
 
+template <int D, bool BF16>
+cudaError_t launch_reduce_t(const BwdParams& p, cudaStream_t stream) {
+  const int64_t rows = static_cast<int64_t>(p.BH / p.group) * p.S;
+  const int64_t threads = rows * (2 * D / 8);
+  const int64_t blocks = (threads + 255) / 256;
+  const int grid = static_cast<int>(blocks < 152 * 8 ? blocks : 152 * 8);
+  fa_bwd_dkv_reduce_kernel<D, BF16><<<grid, 256, 0, stream>>>(p, rows);
+  return cudaGetLastError();
+}
+
 }  // namespace
+
+int bwd_kv_splits(int64_t BHkv, int64_t n_tiles, int group) {
+  constexpr int64_t kWant = 2 * 152;
+  if (group <= 1) return 1;
+  for (int s = 1; s < group; ++s)
+    if (group % s == 0 && BHkv * n_tiles * s >= kWant) return s;
+  return group;
+}
 
 #define FA_BWD_DISPATCH(CALL)                                   \
   switch (D) {                                                  \
@@ -611,6 +699,12 @@ cudaError_t launch_bwd_dkdv(int D, bool bf16, const BwdMaps& m, const BwdParams&
 #define FA_DKDV(DD, BB) launch_main_t<DD, BB, true>(m.k128, m.v128, m.q64, m.do64, p, stream)
   FA_BWD_DISPATCH(FA_DKDV)
 #undef FA_DKDV
+}
+
+cudaError_t launch_bwd_dkv_reduce(int D, bool bf16, const BwdParams& p, cudaStream_t stream) {
+#define FA_RED(DD, BB) launch_reduce_t<DD, BB>(p, stream)
+  FA_BWD_DISPATCH(FA_RED)
+#undef FA_RED
 }
 
 cudaError_t launch_bwd_dq(int D, bool bf16, const BwdMaps& m, const BwdParams& p, cudaStream_t stream) {

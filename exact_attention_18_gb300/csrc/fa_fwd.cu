@@ -136,6 +136,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int bh = blockIdx.x;
+  const int kvh = bh / p.group;  // K/V head shared by this query head's group
   const int S = p.S;
   // Under the causal mask the heaviest CTAs are launched first.
   const int cta = p.causal ? p.n_m_tiles - 1 - static_cast<int>(blockIdx.y) : static_cast<int>(blockIdx.y);
@@ -209,14 +210,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
             for (int h = 0; h < 2; ++h)
               tma_load_3d(smem + L::kOffK + st * L::kTileBytes + ch * L::kChunkBytes + h * kHalfBytes, &tm_k,
-                          &bar_kfull[st], ch * (L::kRowBytes / 2), it * kBlockN + h * (kBlockN / 2), bh);
+                          &bar_kfull[st], ch * (L::kRowBytes / 2), it * kBlockN + h * (kBlockN / 2), kvh);
           mbar_arrive_expect_tx(&bar_vfull[st], L::kTileBytes);
 #pragma unroll
           for (int ch = 0; ch < L::kChunks; ++ch)
 #pragma unroll
             for (int h = 0; h < 2; ++h)
               tma_load_3d(smem + L::kOffV + st * L::kTileBytes + ch * L::kChunkBytes + h * kHalfBytes, &tm_v,
-                          &bar_vfull[st], ch * (L::kRowBytes / 2), it * kBlockN + h * (kBlockN / 2), bh);
+                          &bar_vfull[st], ch * (L::kRowBytes / 2), it * kBlockN + h * (kBlockN / 2), kvh);
         }
         // Teardown: every copy this thread started must land before the CTA exits.
         drain_wait(bar_q, 0, p.err);

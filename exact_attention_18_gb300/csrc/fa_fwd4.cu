@@ -118,6 +118,7 @@ __global__ void __launch_bounds__(kF4Threads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int bh = blockIdx.x;
+  const int kvh = bh / p.group;  // K/V head shared by this query head's group
   const int S = p.S;
   // Under the causal mask the heaviest CTAs are launched first.
   const int cta = p.causal ? p.n_m_tiles - 1 - static_cast<int>(blockIdx.y) : static_cast<int>(blockIdx.y);
@@ -177,9 +178,9 @@ __global__ void __launch_bounds__(kF4Threads, 1)
           const int use = it / L::kStages;
           if (use > 0 && !mbar_wait(&bar_empty[st], (use - 1) & 1, abort_flag, p.err, kErrTimeoutLoad)) break;
           mbar_arrive_expect_tx(&bar_kfull[st], GK::kTileBytes);
-          tma_load_3d(smem + L::kOffK + st * GK::kTileBytes, &tm_k, &bar_kfull[st], 0, it * kBN, bh);
+          tma_load_3d(smem + L::kOffK + st * GK::kTileBytes, &tm_k, &bar_kfull[st], 0, it * kBN, kvh);
           mbar_arrive_expect_tx(&bar_vfull[st], GK::kTileBytes);
-          tma_load_3d(smem + L::kOffV + st * GK::kTileBytes, &tm_v, &bar_vfull[st], 0, it * kBN, bh);
+          tma_load_3d(smem + L::kOffV + st * GK::kTileBytes, &tm_v, &bar_vfull[st], 0, it * kBN, kvh);
         }
         // Teardown: every copy this thread started must land before the CTA exits.
         drain_wait(bar_q, 0, p.err);

@@ -16,20 +16,24 @@ struct FwdParams {
   int S;               // sequence length
   int n_m_tiles;       // CTAs per (b, h): ceil(S / fwd_rows_per_cta(D))
   int causal;          // nonzero: key j visible to query i iff j <= i
+  int group;           // query heads per K/V head: query head bh reads K/V head bh / group
   float scale_log2;    // scale * log2(e): scores enter exp2 in base 2
   int* err;            // device error word (set when a pipeline wait times out)
 };
 
 struct BwdParams {
-  const void* o;       // [BH, S, D] forward output
+  const void* o;       // [BH, S, D] forward output (BH counts query heads)
   const void* dout;    // [BH, S, D] loss gradient w.r.t. O
   const float* lse;    // [BH, S] natural-log logsumexp from the forward
   float* delta;        // [BH, S] workspace: rowsum(dO o O)
   void* dq;            // [BH, S, D]
-  void* dk;            // [BH, S, D]
-  void* dv;            // [BH, S, D]
+  void* dk;            // [BH / group, S, D]
+  void* dv;            // [BH / group, S, D]
   int S;
-  int BH;
+  int BH;              // query heads B*H
+  int group;           // query heads per K/V head (H / H_kv); K/V head of query head bh is bh / group
+  int kv_splits;       // dK/dV pass: CTAs sharing a (K/V head, key tile), each over group / kv_splits heads
+  float* dkv_part;     // kv_splits > 1: fp32 partial sums [kv_splits][BH / group][S][2 D] (dV | scale*dK)
   int n_tiles;         // ceil(S / 128): own tiles per (b, h)
   int n_partner;       // ceil(S / 64): streamed partner blocks per (b, h)
   int causal;
@@ -38,7 +42,8 @@ struct BwdParams {
   int* err;            // device error word
 };
 
-// Tensor maps of the backward's four inputs, each viewed as 3-D {D, S, BH}:
+// Tensor maps of the backward's four inputs, each viewed as 3-D {D, S, heads}
+// (B*H heads for Q and dO, B*H_kv for K and V):
 // 128-row boxes for a CTA's resident tiles, 64-row boxes for streamed blocks.
 struct BwdMaps {
   CUtensorMap q128, k128, v128, do128;
@@ -59,6 +64,13 @@ cudaError_t launch_fwd(int D, bool bf16, const CUtensorMap& tq, const CUtensorMa
 cudaError_t launch_bwd_preprocess(int D, bool bf16, const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_dkdv(int D, bool bf16, const BwdMaps& maps, const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_dq(int D, bool bf16, const BwdMaps& maps, const BwdParams& p, cudaStream_t stream);
+// Sums the kv_splits partial dK/dV rows and writes dK, dV (only when kv_splits > 1).
+cudaError_t launch_bwd_dkv_reduce(int D, bool bf16, const BwdParams& p, cudaStream_t stream);
+
+// CTAs per (K/V head, key tile) in the dK/dV pass: the smallest divisor of
+// `group` that gives at least two CTAs per SM of a 152-SM GPU (1 when the
+// heads alone do, or for ordinary multi-head attention).
+int bwd_kv_splits(int64_t BHkv, int64_t n_tiles, int group);
 
 // Address of this process's device error word on the current device.
 int* device_error_word();

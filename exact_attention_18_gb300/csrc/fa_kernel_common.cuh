@@ -119,4 +119,13 @@ __device__ __forceinline__ void store_row16(void* dst, const uint32_t* v, float 
   d[1] = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
+// 16 fp32 values (TMEM words) times `mul` to 16 consecutive floats (64 bytes, 16-byte aligned).
+__device__ __forceinline__ void store_row16_f32(float* dst, const uint32_t* v, float mul) {
+  float4* d = reinterpret_cast<float4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    d[i] = make_float4(__uint_as_float(v[4 * i]) * mul, __uint_as_float(v[4 * i + 1]) * mul,
+                       __uint_as_float(v[4 * i + 2]) * mul, __uint_as_float(v[4 * i + 3]) * mul);
+}
+
 }  // namespace fa

@@ -81,6 +81,24 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                  int64_t S, int64_t D, int causal, float scale, fa_dtype dtype, void* stream);
 
 /*
+ * Forward pass with grouped K/V heads (multi-query / grouped-query attention,
+ * "Inside FlashAttention" §6.1, the MQA / GQA interface: several query heads
+ * share one K/V head, and K, V are passed with fewer heads instead of being
+ * copied out to H heads).
+ *   q, o    : [B, H, S, D];  lse : [B, H, S] fp32.
+ *   k, v    : [B, H_kv, S, D].
+ * H must be a positive multiple of H_kv (H_kv >= 1); query head h of batch b
+ * reads K/V head h / (H / H_kv) of batch b, so each K/V head serves a run of
+ * H / H_kv consecutive query heads.  H_kv = H is fa_fwd; H_kv = 1 is
+ * multi-query attention.  A call with B*H == 0 (then H_kv == 0 is allowed
+ * when H == 0) or S == 0 launches nothing.  Every other convention
+ * (layout, alignment, ownership, errors) is fa_fwd's; a bad H_kv returns
+ * FA_ERR_INVALID_ARG.
+ */
+fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
+                     int64_t H_kv, int64_t S, int64_t D, int causal, float scale, fa_dtype dtype, void* stream);
+
+/*
  * Bytes of device workspace fa_bwd needs for these sizes: the fp32 row vector
  * D_i = rowsum(dO o O) for every (b, h, i), rounded up to 256 bytes.
  */
@@ -114,6 +132,43 @@ fa_status fa_bwd_marked(const void* q, const void* k, const void* v, const void*
                         const float* lse, void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t S,
                         int64_t D, int causal, float scale, fa_dtype dtype, void* workspace,
                         size_t workspace_bytes, void* stream, void* const* marks);
+
+/*
+ * Backward pass with grouped K/V heads: the gradient of fa_fwd_gqa.
+ *   q, o, dout, dq : [B, H, S, D];  lse : [B, H, S] fp32.
+ *   k, v, dk, dv   : [B, H_kv, S, D].
+ * A K/V head's gradients sum the contributions of all H / H_kv query heads
+ * that read it: dV_g = sum over the group's heads h of P_h^T dO_h, and dK_g
+ * likewise with dS_h^T Q_h.  A dK/dV CTA owns one (K/V head, 128-key block)
+ * and streams query heads of the group one after another through the same
+ * accumulators.  When the K/V heads alone give too few CTAs to fill the GPU
+ * (few K/V heads, short sequences), s CTAs share a (K/V head, key block),
+ * each over G/s of the group's heads (s the smallest divisor of G that gives
+ * 304 CTAs, else G); they write fp32 partial sums to the workspace and a
+ * fourth kernel adds them in a fixed order.  No atomics either way: results
+ * are deterministic.  Workspace: fa_bwd_gqa_workspace_size() bytes.  Other
+ * conventions as fa_bwd; H_kv as in fa_fwd_gqa.
+ */
+fa_status fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                     const float* lse, void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t H_kv,
+                     int64_t S, int64_t D, int causal, float scale, fa_dtype dtype, void* workspace,
+                     size_t workspace_bytes, void* stream);
+
+/*
+ * Bytes of device workspace fa_bwd_gqa needs: the fp32 row vector D of every
+ * query row (B*H*S floats, rounded up to 256 bytes), plus, when the dK/dV
+ * pass splits the group (see fa_bwd_gqa), s * B*H_kv*S*2*D fp32 partial sums
+ * (rounded up to 256 bytes).  Equals fa_bwd_workspace_size() when H_kv = H.
+ * Returns 0 for an empty problem or an H_kv that does not divide H.
+ */
+size_t fa_bwd_gqa_workspace_size(int64_t B, int64_t H, int64_t H_kv, int64_t S, int64_t D);
+
+/* fa_bwd_gqa with the timing marks of fa_bwd_marked (marks[2] is recorded
+ * after the dK/dV kernel and, when it runs, the partial-sum kernel). */
+fa_status fa_bwd_gqa_marked(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                            const float* lse, void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t H_kv,
+                            int64_t S, int64_t D, int causal, float scale, fa_dtype dtype, void* workspace,
+                            size_t workspace_bytes, void* stream, void* const* marks);
 
 /*
  * fa_bwd without a workspace argument, for callers that cannot allocate

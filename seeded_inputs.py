@@ -43,6 +43,11 @@ class Workload:
     qk_std: float = 1.0
     backward: bool = False
     seed: int = 0
+    H_kv: int | None = None  # K/V heads (grouped-query attention); None = H
+
+    @property
+    def kv_heads(self) -> int:
+        return self.H if self.H_kv is None else self.H_kv
 
     @property
     def scale(self) -> float:
@@ -54,17 +59,22 @@ class Workload:
 
     def describe(self) -> str:
         mask = "causal" if self.causal else "non-causal"
-        return f"B{self.B} H{self.H} S{self.S} D{self.D} {self.dtype} {mask}"
+        kv = "" if self.kv_heads == self.H else f" H_kv{self.kv_heads}"
+        return f"B{self.B} H{self.H}{kv} S{self.S} D{self.D} {self.dtype} {mask}"
 
 
 def make_inputs(w: Workload, with_dout: bool | None = None) -> dict:
-    """CPU tensors q, k, v (and do) for workload ``w`` per the module recipe."""
+    """CPU tensors q, k, v (and do) for workload ``w`` per the module recipe.
+
+    K and V have ``w.kv_heads`` heads; Q and dO have ``w.H``.
+    """
     shape = (w.B, w.H, w.S, w.D)
+    kv_shape = (w.B, w.kv_heads, w.S, w.D)
     dt = w.torch_dtype
     out = {
         "q": randn(shape, w.seed, dt, w.qk_std),
-        "k": randn(shape, w.seed + 1, dt, w.qk_std),
-        "v": randn(shape, w.seed + 2, dt),
+        "k": randn(kv_shape, w.seed + 1, dt, w.qk_std),
+        "v": randn(kv_shape, w.seed + 2, dt),
     }
     if with_dout if with_dout is not None else w.backward:
         out["do"] = randn(shape, w.seed + 3, dt)
@@ -86,3 +96,11 @@ for _d in C3_D:
     for _s in C3_S:
         CONFIGS[f"c3_d{_d}_s{_s}"] = Workload(
             f"c3_causal_fwdbwd_B8H1S{_s}D{_d}_bf16", 8, 1, _s, _d, "bf16", True, backward=True)
+
+# Grouped-query attention: the forward+backward of the causal B4 H16 S4096 D64
+# fp16 shape with 8 query heads per K/V head (H_kv = 2), and multi-query
+# attention (H_kv = 1) on the same shape.
+CONFIGS["gqa"] = Workload("gqa_causal_fwdbwd_B4H16Hkv2S4096D64_fp16", 4, 16, 4096, 64, "fp16", True,
+                          backward=True, H_kv=2)
+CONFIGS["mqa"] = Workload("mqa_causal_fwdbwd_B4H16Hkv1S4096D64_fp16", 4, 16, 4096, 64, "fp16", True,
+                          backward=True, H_kv=1)

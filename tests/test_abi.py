@@ -49,6 +49,22 @@ def test_workspace_size(lib):
     assert fa.fa_bwd_workspace_size(0, 4, 16, 64) == 0
 
 
+def test_gqa_workspace_size(lib):
+    """Delta for every query row, plus fp32 partial dK/dV rows when the dK/dV pass splits a group."""
+    delta = 4 * 16 * 4096 * 4
+    assert fa.fa_bwd_gqa_workspace_size(1, 4, 4, 128, 64) == fa.fa_bwd_workspace_size(1, 4, 128, 64)
+    # 8 K/V heads x 32 key tiles = 256 CTAs < 304: two CTAs share each (K/V head, key tile)
+    assert fa.fa_bwd_gqa_workspace_size(4, 16, 2, 4096, 64) == delta + 2 * 8 * 4096 * 128 * 4
+    # 4 x 32 = 128 CTAs: four per (K/V head, key tile), four query heads each
+    assert fa.fa_bwd_gqa_workspace_size(4, 16, 1, 4096, 64) == delta + 4 * 4 * 4096 * 128 * 4
+    # enough CTAs from the K/V heads alone: no partial sums
+    assert fa.fa_bwd_gqa_workspace_size(4, 8, 4, 2432, 64) == 4 * 8 * 2432 * 4
+    # too few CTAs even with one head per CTA: split over the whole group
+    assert fa.fa_bwd_gqa_workspace_size(1, 8, 2, 256, 64) == 1 * 8 * 256 * 4 + 4 * 2 * 256 * 128 * 4
+    assert fa.fa_bwd_gqa_workspace_size(1, 6, 4, 128, 64) == 0
+    assert fa.fa_bwd_gqa_workspace_size(0, 6, 3, 128, 64) == 0
+
+
 P = 0x10000  # a fake, 16-byte aligned address: never dereferenced by these calls
 
 
@@ -104,6 +120,46 @@ def test_bwd_empty_is_a_no_op(lib):
     assert bwd(S=0) == 0
     assert bwd(B=0, ws=0, wsb=0) == 0
     assert bwd(S=0, q=0, dq=0, ws=0, wsb=0) == 0
+
+
+def fwd_gqa(**kw):
+    a = dict(q=P, k=P, v=P, o=P, lse=P, B=1, H=4, H_kv=2, S=128, D=64, causal=0, scale=0.125, dtype=0, stream=None)
+    a.update(kw)
+    return fa.fa_fwd_gqa(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["H_kv"], a["S"], a["D"],
+                         a["causal"], a["scale"], a["dtype"], a["stream"])
+
+
+def bwd_gqa(**kw):
+    a = dict(q=P, k=P, v=P, o=P, do=P, lse=P, dq=P, dk=P, dv=P, B=1, H=4, H_kv=2, S=128, D=64, causal=0,
+             scale=0.125, dtype=0, ws=P * 16, wsb=1 << 20, stream=None)
+    a.update(kw)
+    return fa.fa_bwd_gqa(a["q"], a["k"], a["v"], a["o"], a["do"], a["lse"], a["dq"], a["dk"], a["dv"], a["B"],
+                         a["H"], a["H_kv"], a["S"], a["D"], a["causal"], a["scale"], a["dtype"], a["ws"], a["wsb"],
+                         a["stream"])
+
+
+GQA_BAD = [
+    (dict(H=6, H_kv=4), 1), (dict(H_kv=0), 1), (dict(H_kv=8), 1), (dict(H_kv=-1), 1), (dict(H=0, H_kv=1), 1),
+    (dict(H=0, H_kv=0, D=48), 2), (dict(D=48), 2), (dict(k=P + 8), 3), (dict(q=0), 1),
+]
+
+
+@pytest.mark.parametrize("kw,status", GQA_BAD)
+def test_fwd_gqa_rejects_bad_arguments(lib, kw, status):
+    assert fwd_gqa(**kw) == status
+    assert fa.fa_last_error_detail() != ""
+
+
+@pytest.mark.parametrize("kw,status", GQA_BAD + [(dict(ws=0), 4), (dict(dk=P + 4), 3)])
+def test_bwd_gqa_rejects_bad_arguments(lib, kw, status):
+    assert bwd_gqa(**kw) == status
+    assert fa.fa_last_error_detail() != ""
+
+
+@pytest.mark.parametrize("kw", [dict(H=0, H_kv=0), dict(B=0), dict(S=0, q=0, k=0, v=0, o=0, lse=0)])
+def test_gqa_empty_is_a_no_op(lib, kw):
+    assert fwd_gqa(**kw) == 0
+    assert bwd_gqa(**kw) == 0
 
 
 def test_binding_has_no_fallback(monkeypatch):
