@@ -43,16 +43,34 @@ sys.path.insert(0, ROOT)
 
 METRIC = "attention fwd/bwd TFLOPS and % of GB300 FP16 tensor peak (B4 H16 S4096 D64 causal)"
 WORKLOAD = "c2"
-WORKLOADS = ("c2", "gqa", "mqa")
+WORKLOADS = ("c2", "gqa", "mqa", "varlen")
 FLUSH_BYTES = 256 << 20  # > 129 MB L2
 KERNEL_SOURCES = ["exact_attention_18_gb300/csrc/fa_fwd.cu", "exact_attention_18_gb300/csrc/fa_fwd4.cu",
                   "exact_attention_18_gb300/csrc/fa_bwd.cu", "exact_attention_18_gb300/csrc/fa_softmax.cuh",
                   "exact_attention_18_gb300/csrc/fa_kernel_common.cuh", "exact_attention_18_gb300/csrc/sm103_ptx.cuh"]
 
 
+def is_packed(w):
+    return hasattr(w, "lengths")
+
+
+def head_list(w):
+    """Every attention head of the workload as (b, h, rows): B*H heads of S rows, or, for a
+    packed batch, H heads per sample of that sample's length."""
+    if is_packed(w):
+        return [(b, h, n) for b, n in enumerate(w.lengths) for h in range(w.H)]
+    return [(b, h, w.S) for b in range(w.B) for h in range(w.H)]
+
+
+def sq_rows(w):
+    """Sum over heads of rows^2 (the S^2 of the FLOP convention, per head)."""
+    return float(sum(n * n for _, _, n in head_list(w)))
+
+
 def conv_flops(w):
-    """FLOP convention: forward 4*B*H*S^2*D (halved when causal); backward 2.5x forward."""
-    f = 4.0 * w.B * w.H * w.S * w.S * w.D
+    """FLOP convention: forward 4*S^2*D per head (halved when causal), summed over heads
+    (B*H*S^2 fixed length, H * sum of squared sample lengths packed); backward 2.5x forward."""
+    f = 4.0 * sq_rows(w) * w.D
     if w.causal:
         f /= 2
     return f, 2.5 * f
@@ -65,8 +83,8 @@ def fwd_kernel_name(w):
 
 def kernel_work(w):
     """Algorithmic work per launch of each kernel (FLOPs of its tensor-core GEMMs, or HBM bytes)."""
-    units = w.B * w.H * w.S * w.S * w.D / (2.0 if w.causal else 1.0)
-    rows = w.B * w.H * w.S
+    units = sq_rows(w) * w.D / (2.0 if w.causal else 1.0)
+    rows = sum(n for _, _, n in head_list(w))
     return {
         fwd_kernel_name(w): ("tensor", 4.0 * units),        # S = QK^T, O += PV
         "fa_bwd_preprocess_kernel": ("hbm", rows * w.D * 2 * 2 + rows * 4),  # read O, dO; write Delta
@@ -167,51 +185,74 @@ def cpu_oracle_step(inp, w, heads):
     """
     import oracle
     grp = w.H // w.kv_heads
-    for b, h in heads:
-        q, do = inp["q"][b, h], inp["do"][b, h]
-        k, v = inp["k"][b, h // grp], inp["v"][b, h // grp]
+    cu = inp["cu_seqlens"].tolist() if is_packed(w) else None
+    for b, h, _ in heads:
+        if cu is None:
+            q, do = inp["q"][b, h], inp["do"][b, h]
+            k, v = inp["k"][b, h // grp], inp["v"][b, h // grp]
+        else:
+            a, e = cu[b], cu[b + 1]
+            q, do = inp["q"][a:e, h], inp["do"][a:e, h]
+            k, v = inp["k"][a:e, h // grp], inp["v"][a:e, h // grp]
         oracle.forward(q, k, v, w.causal, w.scale)
         oracle.backward(q, k, v, do, w.causal, w.scale)
 
 
+def head_flops(w, heads):
+    """Convention FLOPs (forward + backward) of the listed heads."""
+    f = 4.0 * w.D * sum(n * n for _, _, n in heads) * (0.5 if w.causal else 1.0)
+    return 3.5 * f
+
+
 def cpu_baseline(inp, w, n_heads: int):
     import torch
-    heads = [(i // w.H % w.B, i % w.H) for i in range(n_heads)]
+    all_heads = head_list(w)
+    heads = [all_heads[i % len(all_heads)] for i in range(n_heads)]
     t0 = time.perf_counter()
     cpu_oracle_step(inp, w, heads)
     dt = time.perf_counter() - t0
-    f, b = conv_flops(w)
-    flops = (f + b) * n_heads / (w.B * w.H)
-    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": torch.get_num_threads(), "kind": "oracle",
-            "sample": f"fp64 oracle fwd+bwd on {n_heads} of the {w.B * w.H} (b,h) heads, S={w.S} D={w.D} causal, "
+    return {"value": head_flops(w, heads) / dt / 1e12, "unit": "TFLOP/s", "cores": torch.get_num_threads(),
+            "kind": "oracle",
+            "sample": f"fp64 oracle fwd+bwd on {n_heads} of the {len(all_heads)} heads of {w.describe()}, "
                       f"{dt:.2f} s; convention FLOPs of those heads / wall time"}
+
+
+def workload_inputs(w):
+    from seeded_inputs import make_inputs, make_packed_inputs
+    return make_packed_inputs(w) if is_packed(w) else make_inputs(w, with_dout=True)
+
+
+def workload_config(w):
+    if is_packed(w):
+        return {"workload": w.name, "samples": w.batch, "lengths": list(w.lengths), "total_tokens": w.total,
+                "max_seqlen": w.max_seqlen, "H": w.H, "H_kv": w.kv_heads, "D": w.D, "causal": w.causal}
+    return {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.kv_heads, "S": w.S, "D": w.D, "causal": w.causal}
 
 
 def run_reference(args, w):
     """Reference arm: the CPU oracle as it stands, one head per step, rank 0 only."""
     import torch
-    from seeded_inputs import make_inputs
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    inp = make_inputs(w, with_dout=True)
-    nh = w.B * w.H
+    inp = workload_inputs(w)
+    all_heads = head_list(w)
+    nh = len(all_heads)
     for i in range(args.warmup):
-        cpu_oracle_step(inp, w, [((i // w.H) % w.B, i % w.H)])
+        cpu_oracle_step(inp, w, [all_heads[i % nh]])
+    done = []
     t0 = time.perf_counter()
     for i in range(args.steps):
-        j = (args.warmup + i) % nh
-        cpu_oracle_step(inp, w, [(j // w.H, j % w.H)])
+        hd = all_heads[(args.warmup + i) % nh]
+        cpu_oracle_step(inp, w, [hd])
+        done.append(hd)
     dt = time.perf_counter() - t0
-    f, b = conv_flops(w)
-    flops_per_step = (f + b) / nh
-    value = flops_per_step * args.steps / dt / 1e12
-    sample = f"fp64 CPU oracle fwd+bwd of one (b,h) head of {w.describe()} per step"
+    value = head_flops(w, done) / dt / 1e12
+    sample = f"fp64 CPU oracle fwd+bwd of one head of {w.describe()} per step"
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "B": w.B, "H": w.H, "S": w.S, "D": w.D, "causal": w.causal,
-                       "sample_per_step": "one (b,h) head"},
+            "config": dict(workload_config(w), sample_per_step="one (b,h) head"),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": torch.get_num_threads(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -232,8 +273,11 @@ def main():
     args.warmup = max(args.warmup, 3)
 
     import dataclasses
-    from seeded_inputs import CONFIGS
-    w = dataclasses.replace(CONFIGS[args.workload], backward=True)
+    from seeded_inputs import CONFIGS, PACKED_CONFIGS
+    if args.workload in PACKED_CONFIGS:
+        w = PACKED_CONFIGS[args.workload]
+    else:
+        w = dataclasses.replace(CONFIGS[args.workload], backward=True)
     global METRIC
     if args.workload != WORKLOAD:
         METRIC = f"attention fwd/bwd TFLOPS and % of GB300 FP16 tensor peak ({w.describe()})"
@@ -244,7 +288,6 @@ def main():
     import torch
     import exact_attention_18_gb300 as fa
     from exact_attention_18_gb300.sharding import job_throughput, max_over_ranks
-    from seeded_inputs import make_inputs
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -261,26 +304,39 @@ def main():
             dist.barrier()
         torch.cuda.synchronize()
 
-    inp = make_inputs(w, with_dout=True)
+    inp = workload_inputs(w)
     q, k, v, do = (inp[n].to(dev) for n in ("q", "k", "v", "do"))
     o = torch.empty_like(q)
-    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    packed = is_packed(w)
+    H, D, Hkv = w.H, w.D, w.kv_heads
+    lse_shape = (H, w.total) if packed else q.shape[:3]
+    lse = torch.empty(lse_shape, dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(k)
-    ws_bytes = fa.fa_bwd_gqa_workspace_size(w.B, w.H, w.kv_heads, w.S, w.D)
+    if packed:
+        cu = inp["cu_seqlens"].to(dev)
+        nb, ms, T = w.batch, w.max_seqlen, w.total
+        ws_bytes = fa.fa_bwd_varlen_workspace_size(nb, ms, T, H, Hkv, D)
+    else:
+        B, S = w.B, w.S
+        ws_bytes = fa.fa_bwd_gqa_workspace_size(B, H, Hkv, S, D)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     sp = stream.cuda_stream
     dt_code = fa.FA_FP16 if w.dtype == "fp16" else fa.FA_BF16
-    B, H, S, D = w.B, w.H, w.S, w.D
-    Hkv = w.kv_heads
 
-    def fwd_call(q_, k_, v_, o_, lse_):
+    def fwd_call(q_, k_, v_, o_, lse_, cu_=None):
+        if packed:
+            return fa.fa_fwd_varlen(q_, k_, v_, o_, lse_, cu_ or cu.data_ptr(), nb, ms, T, H, Hkv, D, w.causal, w.scale,
+                                    dt_code, sp)
         if Hkv == H:
             return fa.fa_fwd(q_, k_, v_, o_, lse_, B, H, S, D, w.causal, w.scale, dt_code, sp)
         return fa.fa_fwd_gqa(q_, k_, v_, o_, lse_, B, H, Hkv, S, D, w.causal, w.scale, dt_code, sp)
 
-    def bwd_call(q_, k_, v_, o_, do_, lse_, dq_, dk_, dv_, marks):
+    def bwd_call(q_, k_, v_, o_, do_, lse_, dq_, dk_, dv_, marks, cu_=None):
+        if packed:
+            return fa.fa_bwd_varlen_marked(q_, k_, v_, o_, do_, lse_, dq_, dk_, dv_, cu_ or cu.data_ptr(), nb, ms, T, H, Hkv,
+                                           D, w.causal, w.scale, dt_code, ws.data_ptr(), ws_bytes, sp, marks)
         if Hkv == H:
             return fa.fa_bwd_marked(q_, k_, v_, o_, do_, lse_, dq_, dk_, dv_, B, H, S, D, w.causal, w.scale,
                                     dt_code, ws.data_ptr(), ws_bytes, sp, marks)
@@ -365,19 +421,23 @@ def main():
             kernels[n] = {"ms": avg[n], "GB/s": ach, "frac_of_hbm_peak": ach / peaks["hbm_gbs"]}
 
     # ---------------------------------------------------------------- end to end through host buffers
-    # Every step copies its inputs q, k, v, dO from pinned host memory and reads all of its outputs
+    # Every step copies its inputs q, k, v, dO (and a packed batch's cu_seqlens) from pinned host
+    # memory and reads all of its outputs
     # (O, L, dQ, dK, dV) back, inside the timed region.  Two device buffer sets let the copies of
     # neighbouring steps (inputs of step i+1 on one copy stream, outputs of step i-1 on another)
     # overlap step i's kernels, as a training loop would pipeline them.
     e2e = None
     if not args.no_e2e:
-        pin = {n: inp[n].pin_memory() for n in ("q", "k", "v", "do")}
+        in_names = ("q", "k", "v", "do") + (("cu_seqlens",) if packed else ())
+        pin = {n: inp[n].pin_memory() for n in in_names}
         out_shapes = {"o": (o.shape, o.dtype), "lse": (lse.shape, lse.dtype), "dq": (q.shape, q.dtype),
                       "dk": (k.shape, k.dtype), "dv": (k.shape, k.dtype)}
         host_out = [{n: torch.empty(sh, dtype=dt).pin_memory() for n, (sh, dt) in out_shapes.items()}
                     for _ in range(2)]
-        dev_in = [{"q": q, "k": k, "v": v, "do": do},
-                  {n: torch.empty_like(t) for n, t in (("q", q), ("k", k), ("v", v), ("do", do))}]
+        dev_in0 = {"q": q, "k": k, "v": v, "do": do}
+        if packed:
+            dev_in0["cu_seqlens"] = cu
+        dev_in = [dev_in0, {n: torch.empty_like(t) for n, t in dev_in0.items()}]
         dev_out = [{"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv},
                    {n: torch.empty(sh, dtype=dt, device=dev) for n, (sh, dt) in out_shapes.items()}]
         h2d = sum(t.numel() * t.element_size() for t in pin.values())
@@ -385,13 +445,14 @@ def main():
         s_h2d, s_d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
         def run_step(bi, bo):
+            cu_ = bi["cu_seqlens"].data_ptr() if packed else None
             st = fwd_call(bi["q"].data_ptr(), bi["k"].data_ptr(), bi["v"].data_ptr(), bo["o"].data_ptr(),
-                          bo["lse"].data_ptr())
+                          bo["lse"].data_ptr(), cu_)
             if st:
                 raise RuntimeError(f"forward: {fa.fa_status_string(st)} {fa.fa_last_error_detail()}")
             st = bwd_call(bi["q"].data_ptr(), bi["k"].data_ptr(), bi["v"].data_ptr(), bo["o"].data_ptr(),
                           bi["do"].data_ptr(), bo["lse"].data_ptr(), bo["dq"].data_ptr(), bo["dk"].data_ptr(),
-                          bo["dv"].data_ptr(), None)
+                          bo["dv"].data_ptr(), None, cu_)
             if st:
                 raise RuntimeError(f"backward: {fa.fa_status_string(st)} {fa.fa_last_error_detail()}")
 
@@ -446,10 +507,15 @@ def main():
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "fp16", "data": "synthetic",
-            "config": {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.kv_heads, "S": w.S, "D": w.D,
-                       "causal": w.causal, "global_batch": w.B * world, "seq_len": w.S, "parallelism": f"independent x{world}",
-                       "step": "fa_fwd + fa_bwd" if w.kv_heads == w.H else "fa_fwd_gqa + fa_bwd_gqa", "l2": "flushed between timed steps (256 MiB write)",
-                       "flop_convention": "fwd 4*B*H*S^2*D/2 (causal), bwd 2.5x fwd"},
+            "config": dict(workload_config(w),
+                           global_batch=(w.batch if packed else w.B) * world,
+                           seq_len=w.max_seqlen if packed else w.S,
+                           parallelism=f"independent x{world}",
+                           step=("fa_fwd_varlen + fa_bwd_varlen" if packed else
+                                 "fa_fwd + fa_bwd" if w.kv_heads == w.H else "fa_fwd_gqa + fa_bwd_gqa"),
+                           l2="flushed between timed steps (256 MiB write)",
+                           flop_convention=("fwd 4*S^2*D per head (/2 causal; S the sample length when packed), "
+                                            "bwd 2.5x fwd")),
             "fwd": {"ms": fwd_ms, "TFLOP/s": f_fwd / (fwd_ms * 1e-3) / 1e12,
                     "frac_of_tensor_peak": f_fwd / (fwd_ms * 1e-3) / 1e12 / peaks["tensor_tflops"]},
             "bwd": {"ms": bwd_ms, "TFLOP/s": f_bwd / (bwd_ms * 1e-3) / 1e12,

@@ -6,10 +6,13 @@ the library's CUDA kernels.  PyTorch supplies device memory and streams.
 The raw entry points keep the C names and signatures (pointers as ints):
 ``fa_fwd``, ``fa_fwd_gqa``, ``fa_bwd``, ``fa_bwd_marked``, ``fa_bwd_gqa``,
 ``fa_bwd_gqa_marked``, ``fa_bwd_noalloc``, ``fa_bwd_workspace_size``, ``fa_bwd_gqa_workspace_size``,
-``fa_status_string``, ``fa_last_error_detail``, ``fa_check_device_errors``.
-``forward`` and ``backward`` wrap them for contiguous [B, H, S, D] CUDA tensors;
-K and V (and dK, dV) may have fewer heads H_kv dividing H (grouped-query and
-multi-query attention), in which case they call the ``_gqa`` entry points.
+``fa_fwd_varlen``, ``fa_bwd_varlen``, ``fa_bwd_varlen_marked``,
+``fa_bwd_varlen_workspace_size``, ``fa_status_string``, ``fa_last_error_detail``,
+``fa_check_device_errors``.  ``forward`` and ``backward`` wrap them for
+contiguous [B, H, S, D] CUDA tensors; K and V (and dK, dV) may have fewer heads
+H_kv dividing H (grouped-query and multi-query attention), in which case they
+call the ``_gqa`` entry points.  ``forward_varlen`` and ``backward_varlen`` do
+the same for packed batches: [T, H, D] tensors and int32 ``cu_seqlens``.
 
 The first call loads the compiled library and raises if it has not been built
 (``python -m exact_attention_18_gb300.build``); there is no fallback
@@ -24,7 +27,8 @@ import os
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libfa_gb300.so")
 
 __all__ = ["fa_fwd", "fa_fwd_gqa", "fa_bwd", "fa_bwd_marked", "fa_bwd_gqa", "fa_bwd_gqa_marked", "fa_bwd_noalloc",
-           "fa_bwd_workspace_size", "fa_bwd_gqa_workspace_size", "fa_status_string", "fa_last_error_detail",
+           "fa_bwd_workspace_size", "fa_bwd_gqa_workspace_size", "fa_fwd_varlen", "fa_bwd_varlen",
+           "fa_bwd_varlen_marked", "fa_bwd_varlen_workspace_size", "forward_varlen", "backward_varlen", "fa_status_string", "fa_last_error_detail",
            "fa_check_device_errors", "forward", "backward", "FAError", "FA_FP16", "FA_BF16", "STATUS",
            "library_path", "load_library"]
 
@@ -64,6 +68,14 @@ def _load():
                                       sz, vp, ctypes.POINTER(vp)]
     lib.fa_bwd_gqa_workspace_size.restype = sz
     lib.fa_bwd_gqa_workspace_size.argtypes = [i64, i64, i64, i64, i64]
+    lib.fa_fwd_varlen.restype = i32
+    lib.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i32, f32, i32, vp]
+    lib.fa_bwd_varlen_workspace_size.restype = sz
+    lib.fa_bwd_varlen_workspace_size.argtypes = [i64, i64, i64, i64, i64, i64]
+    lib.fa_bwd_varlen.restype = i32
+    lib.fa_bwd_varlen.argtypes = [vp] * 10 + [i64] * 6 + [i32, f32, i32, vp, sz, vp]
+    lib.fa_bwd_varlen_marked.restype = i32
+    lib.fa_bwd_varlen_marked.argtypes = [vp] * 10 + [i64] * 6 + [i32, f32, i32, vp, sz, vp, ctypes.POINTER(vp)]
     lib.fa_bwd_noalloc.restype = i32
     lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i32, f32, i32, vp]
     lib.fa_status_string.restype = ctypes.c_char_p
@@ -122,6 +134,32 @@ def fa_bwd_gqa_marked(q, k, v, o, dout, lse, dq, dk, dv, B, H, H_kv, S, D, causa
         arr = (ctypes.c_void_p * 4)(*[m if m else None for m in marks])
     return _load().fa_bwd_gqa_marked(q, k, v, o, dout, lse, dq, dk, dv, B, H, H_kv, S, D, int(causal),
                                      float(scale), int(dtype), workspace, workspace_bytes, stream, arr)
+
+
+def fa_fwd_varlen(q, k, v, o, lse, cu_seqlens, batch, max_seqlen, total, H, H_kv, D, causal, scale, dtype,
+                  stream) -> int:
+    return _load().fa_fwd_varlen(q, k, v, o, lse, cu_seqlens, batch, max_seqlen, total, H, H_kv, D, int(causal),
+                                 float(scale), int(dtype), stream)
+
+
+def fa_bwd_varlen_workspace_size(batch, max_seqlen, total, H, H_kv, D) -> int:
+    return _load().fa_bwd_varlen_workspace_size(batch, max_seqlen, total, H, H_kv, D)
+
+
+def fa_bwd_varlen(q, k, v, o, dout, lse, dq, dk, dv, cu_seqlens, batch, max_seqlen, total, H, H_kv, D, causal, scale,
+                  dtype, workspace, workspace_bytes, stream) -> int:
+    return _load().fa_bwd_varlen(q, k, v, o, dout, lse, dq, dk, dv, cu_seqlens, batch, max_seqlen, total, H, H_kv,
+                                 D, int(causal), float(scale), int(dtype), workspace, workspace_bytes, stream)
+
+
+def fa_bwd_varlen_marked(q, k, v, o, dout, lse, dq, dk, dv, cu_seqlens, batch, max_seqlen, total, H, H_kv, D,
+                         causal, scale, dtype, workspace, workspace_bytes, stream, marks) -> int:
+    arr = None
+    if marks is not None:
+        arr = (ctypes.c_void_p * 4)(*[m if m else None for m in marks])
+    return _load().fa_bwd_varlen_marked(q, k, v, o, dout, lse, dq, dk, dv, cu_seqlens, batch, max_seqlen, total, H,
+                                        H_kv, D, int(causal), float(scale), int(dtype), workspace, workspace_bytes,
+                                        stream, arr)
 
 
 def fa_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, B, H, S, D, causal, scale, dtype, stream) -> int:
@@ -253,4 +291,71 @@ def backward(q, k, v, o, do, lse, causal: bool = False, scale: float | None = No
         _check(fa_bwd_gqa(*args, B, H, hk, S, D, causal, scale, _dtype_code(q), *ws), "fa_bwd_gqa")
     if squeeze:
         return dq.squeeze(1), dk.squeeze(1), dv.squeeze(1)
+    return dq, dk, dv
+
+
+def _packed(x, name, heads=None):
+    if x.dim() != 3 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor [T, H, D]")
+    if heads is not None and x.shape[1] != heads:
+        raise ValueError(f"{name} must have {heads} heads")
+    return x
+
+
+def _cu(cu_seqlens, T):
+    import torch
+    if cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1 or not cu_seqlens.is_cuda \
+            or not cu_seqlens.is_contiguous() or cu_seqlens.numel() < 1:
+        raise ValueError("cu_seqlens must be a contiguous 1-D int32 CUDA tensor [batch + 1]")
+    return cu_seqlens.numel() - 1
+
+
+def forward_varlen(q, k, v, cu_seqlens, max_seqlen: int, causal: bool = False, scale: float | None = None,
+                   out=None, lse=None, stream=None):
+    """O [T, H, D] and L [H, T] of a packed batch (samples cu_seqlens[b] .. cu_seqlens[b+1]-1).
+
+    ``max_seqlen`` must bound every sample length (a host integer, so no device
+    read is needed); a violation is detected on the device and reported by
+    ``fa_check_device_errors``.
+    """
+    import torch
+    q = _packed(q, "q")
+    T, H, D = q.shape
+    k, v = _packed(k, "k"), _packed(v, "v")
+    hk = k.shape[1]
+    if k.shape[0] != T or k.shape[2] != D or v.shape != k.shape or k.dtype != q.dtype or v.dtype != q.dtype \
+            or hk < 1 or H % hk != 0:
+        raise ValueError("k and v must be [T, H_kv, D] with H_kv dividing H, in q's dtype")
+    batch = _cu(cu_seqlens, T)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    o = torch.empty_like(q) if out is None else out
+    l = torch.empty((H, T), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check(fa_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), l.data_ptr(), cu_seqlens.data_ptr(),
+                         batch, int(max_seqlen), T, H, hk, D, causal, scale, _dtype_code(q), _stream_ptr(stream)),
+           "fa_fwd_varlen")
+    return o, l
+
+
+def backward_varlen(q, k, v, o, do, lse, cu_seqlens, max_seqlen: int, causal: bool = False,
+                    scale: float | None = None, workspace=None, stream=None):
+    """dQ [T, H, D], dK, dV [T, H_kv, D] of a packed batch from the forward's O and L."""
+    import torch
+    q, o, do = _packed(q, "q"), _packed(o, "o"), _packed(do, "do")
+    T, H, D = q.shape
+    k, v = _packed(k, "k"), _packed(v, "v")
+    hk = k.shape[1]
+    if o.shape != q.shape or do.shape != q.shape or v.shape != k.shape or hk < 1 or H % hk != 0:
+        raise ValueError("o, do must match q; k, v must be [T, H_kv, D] with H_kv dividing H")
+    batch = _cu(cu_seqlens, T)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(k)
+    need = fa_bwd_varlen_workspace_size(batch, int(max_seqlen), T, H, hk, D)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _check(fa_bwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
+                         dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), cu_seqlens.data_ptr(), batch, int(max_seqlen),
+                         T, H, hk, D, causal, scale, _dtype_code(q), workspace.data_ptr(),
+                         workspace.numel() * workspace.element_size(), _stream_ptr(stream)), "fa_bwd_varlen")
     return dq, dk, dv

@@ -161,143 +161,124 @@ fa_status check_heads(int64_t H, int64_t H_kv) {
   return FA_OK;
 }
 
-fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
-                   int64_t H_kv, int64_t S, int64_t D, int causal, float scale, fa_dtype dtype, void* stream) {
-  g_detail[0] = 0;
-  fa_status st = check_common(B, H, S, D, scale, dtype);
+// One call's problem.  Fixed length: B entries of S rows, tensors [B, H(_kv), S, D].
+// Packed batch (cu != nullptr): B samples over T = total tokens, tensors
+// [T, H(_kv), D], S = the largest sample length; L is [H, T].
+struct Shape {
+  int64_t B, H, H_kv, S, D;
+  const int32_t* cu;
+  int64_t total;
+  bool is_packed;
+  bool packed() const { return is_packed; }
+  int64_t q_rows() const { return packed() ? total * H : B * H * S; }      // rows of Q, O, dO, L, Delta
+  int64_t kv_rows() const { return packed() ? total * H_kv : B * H_kv * S; }  // rows of K, V, dK, dV
+  bool empty() const { return B * H == 0 || S == 0 || (packed() && total == 0); }
+};
+
+fa_status check_shape(const Shape& sh, float scale, fa_dtype dtype) {
+  fa_status st = check_common(sh.B, sh.H, sh.S, sh.D, scale, dtype);
   if (st != FA_OK) return st;
-  if ((st = check_heads(H, H_kv))) return st;
-  const int64_t BH = B * H;
-  if (BH == 0 || S == 0) return FA_OK;  // empty: nothing is read or written, pointers may be NULL
+  if ((st = check_heads(sh.H, sh.H_kv))) return st;
+  if (sh.packed()) {
+    if (sh.total < 0) return fail(FA_ERR_INVALID_ARG, "negative total tokens %lld", (long long)sh.total);
+    if (sh.total >= (int64_t(1) << 31)) return fail(FA_ERR_UNSUPPORTED, "total tokens must be below 2^31");
+    if (sh.H > 0 && sh.total * sh.H >= (int64_t(1) << 31))
+      return fail(FA_ERR_UNSUPPORTED, "total tokens * H must be below 2^31");
+    if (sh.cu && (reinterpret_cast<uintptr_t>(sh.cu) & 3u) != 0)
+      return fail(FA_ERR_ALIGNMENT, "cu_seqlens is not 4-byte aligned");
+  }
+  return FA_OK;
+}
+
+// The tensor map of one input for the call's layout: {D, S, B*heads} (fixed
+// length; rows past S read zero) or {D, heads, T} (packed; tokens past T read
+// zero), box {row_bytes/2, box_rows, 1} or {row_bytes/2, 1, box_rows}.
+fa_status encode_input(CUtensorMap* map, const void* base, bool bf16, const Shape& sh, int64_t heads,
+                       const char* name, unsigned box_rows = 128) {
+  if (!sh.packed()) return encode_qkv_map(map, base, bf16, sh.D, sh.S, sh.B * heads, name, box_rows);
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const int rb = fa::row_bytes_for(static_cast<int>(sh.D));
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(sh.D), static_cast<cuuint64_t>(heads),
+                        static_cast<cuuint64_t>(sh.total)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(sh.D * 2), static_cast<cuuint64_t>(heads * sh.D * 2)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(rb / 2), 1u, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUtensorMapSwizzle swz = rb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                     : (rb == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
+  CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "tensor map for %s: cuTensorMapEncodeTiled error %d", name, (int)r);
+  return FA_OK;
+}
+
+fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, const Shape& sh, int causal,
+                   float scale, fa_dtype dtype, void* stream) {
+  g_detail[0] = 0;
+  fa_status st = check_shape(sh, scale, dtype);
+  if (st != FA_OK) return st;
+  if (sh.empty()) return FA_OK;  // empty: nothing is read or written, pointers may be NULL
   if ((st = check_ptr(q, "q")) || (st = check_ptr(k, "k")) || (st = check_ptr(v, "v")) ||
       (st = check_ptr(o, "o")) || (st = check_ptr(lse, "lse")))
     return st;
+  if (sh.packed() && !sh.cu) return fail(FA_ERR_INVALID_ARG, "cu_seqlens is NULL");
   const bool bf16 = dtype == FA_BF16;
   // Q in 128-row boxes (a CTA's own tiles); K and V in 64-row boxes.
   CUtensorMap tq, tk, tv;
-  const int64_t BHkv = B * H_kv;
-  if ((st = encode_qkv_map(&tq, q, bf16, D, S, BH, "q")) ||
-      (st = encode_qkv_map(&tk, k, bf16, D, S, BHkv, "k", 64)) ||
-      (st = encode_qkv_map(&tv, v, bf16, D, S, BHkv, "v", 64)))
+  if ((st = encode_input(&tq, q, bf16, sh, sh.H, "q")) || (st = encode_input(&tk, k, bf16, sh, sh.H_kv, "k", 64)) ||
+      (st = encode_input(&tv, v, bf16, sh, sh.H_kv, "v", 64)))
     return st;
   fa::FwdParams p;
   p.o = o;
   p.lse = lse;
-  p.S = static_cast<int>(S);
-  const int rows_per_cta = fa::fwd_rows_per_cta(static_cast<int>(D));
-  p.n_m_tiles = static_cast<int>((S + rows_per_cta - 1) / rows_per_cta);  // CTAs per (b, h)
+  p.S = static_cast<int>(sh.S);
+  p.cu_seqlens = sh.cu;
+  p.heads = static_cast<int>(sh.H);
+  p.total = static_cast<int>(sh.packed() ? sh.total : 0);
+  const int rows_per_cta = fa::fwd_rows_per_cta(static_cast<int>(sh.D));
+  p.n_m_tiles = static_cast<int>((sh.S + rows_per_cta - 1) / rows_per_cta);  // CTAs per (b, h)
   p.causal = causal ? 1 : 0;
-  p.group = static_cast<int>(H / H_kv);
+  p.group = static_cast<int>(sh.H / sh.H_kv);
   p.scale_log2 = scale * kLog2e;
   p.err = fa::device_error_word();
   if (!p.err) return fail(FA_ERR_CUDA, "cannot resolve the device error word on the current device");
-  return from_cuda(fa::launch_fwd(static_cast<int>(D), bf16, tq, tk, tv, p, static_cast<int>(BH),
+  return from_cuda(fa::launch_fwd(static_cast<int>(sh.D), bf16, tq, tk, tv, p, static_cast<int>(sh.B * sh.H),
                                   static_cast<cudaStream_t>(stream)),
                    "forward launch");
 }
-
-fa_status bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
-                   void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t H_kv, int64_t S, int64_t D,
-                   int causal, float scale, fa_dtype dtype, void* workspace, size_t workspace_bytes,
-                   void* stream, void* const* marks);
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 // Backward workspace: the fp32 row vector Delta of every query row, then, when
 // the dK/dV pass splits a K/V head's query heads over several CTAs, their fp32
-// partial [dV | dK] rows.  Sizes must already be validated (H_kv divides H).
-size_t bwd_workspace_layout(int64_t B, int64_t H, int64_t H_kv, int64_t S, int64_t D, int* splits,
-                            size_t* delta_bytes) {
+// partial [dV | dK] rows.  Heads must already be validated (H_kv divides H).
+size_t bwd_workspace_layout(const Shape& sh, int* splits, size_t* delta_bytes) {
   *splits = 1;
   *delta_bytes = 0;
-  if (B <= 0 || H <= 0 || S <= 0 || H_kv <= 0) return 0;
-  *delta_bytes = round256(static_cast<size_t>(B) * static_cast<size_t>(H) * static_cast<size_t>(S) * sizeof(float));
-  *splits = fa::bwd_kv_splits(B * H_kv, (S + 127) / 128, static_cast<int>(H / H_kv));
+  if (sh.B <= 0 || sh.H <= 0 || sh.S <= 0 || sh.H_kv <= 0 || (sh.packed() && sh.total <= 0)) return 0;
+  *delta_bytes = round256(static_cast<size_t>(sh.q_rows()) * sizeof(float));
+  *splits = fa::bwd_kv_splits(sh.B * sh.H_kv, (sh.S + 127) / 128, static_cast<int>(sh.H / sh.H_kv));
   if (*splits == 1) return *delta_bytes;
-  return *delta_bytes + round256(static_cast<size_t>(*splits) * static_cast<size_t>(B * H_kv) *
-                                 static_cast<size_t>(S) * static_cast<size_t>(2 * D) * sizeof(float));
+  return *delta_bytes + round256(static_cast<size_t>(*splits) * static_cast<size_t>(sh.kv_rows()) *
+                                 static_cast<size_t>(2 * sh.D) * sizeof(float));
 }
-
-}  // namespace
-
-extern "C" {
-
-fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H, int64_t S,
-                 int64_t D, int causal, float scale, fa_dtype dtype, void* stream) {
-  return fwd_impl(q, k, v, o, lse, B, H, H, S, D, causal, scale, dtype, stream);
-}
-
-fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
-                     int64_t H_kv, int64_t S, int64_t D, int causal, float scale, fa_dtype dtype, void* stream) {
-  return fwd_impl(q, k, v, o, lse, B, H, H_kv, S, D, causal, scale, dtype, stream);
-}
-
-size_t fa_bwd_workspace_size(int64_t B, int64_t H, int64_t S, int64_t D) {
-  int splits = 1;
-  size_t delta_bytes = 0;
-  return bwd_workspace_layout(B, H, H, S, D, &splits, &delta_bytes);
-}
-
-size_t fa_bwd_gqa_workspace_size(int64_t B, int64_t H, int64_t H_kv, int64_t S, int64_t D) {
-  if (H_kv <= 0 || H <= 0 || H % H_kv != 0) return 0;
-  int splits = 1;
-  size_t delta_bytes = 0;
-  return bwd_workspace_layout(B, H, H_kv, S, D, &splits, &delta_bytes);
-}
-
-fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
-                 void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t S, int64_t D, int causal, float scale,
-                 fa_dtype dtype, void* workspace, size_t workspace_bytes, void* stream) {
-  return fa_bwd_marked(q, k, v, o, dout, lse, dq, dk, dv, B, H, S, D, causal, scale, dtype, workspace,
-                       workspace_bytes, stream, nullptr);
-}
-
-fa_status fa_bwd_marked(const void* q, const void* k, const void* v, const void* o, const void* dout,
-                        const float* lse, void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t S, int64_t D,
-                        int causal, float scale, fa_dtype dtype, void* workspace, size_t workspace_bytes,
-                        void* stream, void* const* marks) {
-  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, B, H, H, S, D, causal, scale, dtype, workspace,
-                  workspace_bytes, stream, marks);
-}
-
-fa_status fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
-                     void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t H_kv, int64_t S, int64_t D,
-                     int causal, float scale, fa_dtype dtype, void* workspace, size_t workspace_bytes,
-                     void* stream) {
-  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, B, H, H_kv, S, D, causal, scale, dtype, workspace,
-                  workspace_bytes, stream, nullptr);
-}
-
-fa_status fa_bwd_gqa_marked(const void* q, const void* k, const void* v, const void* o, const void* dout,
-                            const float* lse, void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t H_kv,
-                            int64_t S, int64_t D, int causal, float scale, fa_dtype dtype, void* workspace,
-                            size_t workspace_bytes, void* stream, void* const* marks) {
-  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, B, H, H_kv, S, D, causal, scale, dtype, workspace,
-                  workspace_bytes, stream, marks);
-}
-
-}  // extern "C"
-
-namespace {
 
 fa_status bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
-                   void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t H_kv, int64_t S, int64_t D,
-                   int causal, float scale, fa_dtype dtype, void* workspace, size_t workspace_bytes,
-                   void* stream, void* const* marks) {
+                   void* dq, void* dk, void* dv, const Shape& sh, int causal, float scale, fa_dtype dtype,
+                   void* workspace, size_t workspace_bytes, void* stream, void* const* marks) {
   g_detail[0] = 0;
-  fa_status st = check_common(B, H, S, D, scale, dtype);
+  fa_status st = check_shape(sh, scale, dtype);
   if (st != FA_OK) return st;
-  if ((st = check_heads(H, H_kv))) return st;
-  const int64_t BH = B * H;
-  const int64_t BHkv = B * H_kv;
-  if (BH == 0 || S == 0) return FA_OK;  // empty: nothing is read or written, pointers may be NULL
+  if (sh.empty()) return FA_OK;  // empty: nothing is read or written, pointers may be NULL
   if ((st = check_ptr(q, "q")) || (st = check_ptr(k, "k")) || (st = check_ptr(v, "v")) ||
       (st = check_ptr(o, "o")) || (st = check_ptr(dout, "dout")) || (st = check_ptr(lse, "lse")) ||
       (st = check_ptr(dq, "dq")) || (st = check_ptr(dk, "dk")) || (st = check_ptr(dv, "dv")))
     return st;
+  if (sh.packed() && !sh.cu) return fail(FA_ERR_INVALID_ARG, "cu_seqlens is NULL");
   int splits = 1;
   size_t delta_bytes = 0;
-  const size_t need = bwd_workspace_layout(B, H, H_kv, S, D, &splits, &delta_bytes);
+  const size_t need = bwd_workspace_layout(sh, &splits, &delta_bytes);
   if (!workspace) return fail(FA_ERR_WORKSPACE, "workspace is NULL (%zu bytes needed)", need);
   if (workspace_bytes < need)
     return fail(FA_ERR_WORKSPACE, "workspace has %zu bytes, %zu needed", workspace_bytes, need);
@@ -305,14 +286,14 @@ fa_status bwd_impl(const void* q, const void* k, const void* v, const void* o, c
     return fail(FA_ERR_ALIGNMENT, "workspace is not 256-byte aligned");
   const bool bf16 = dtype == FA_BF16;
   fa::BwdMaps maps;
-  if ((st = encode_qkv_map(&maps.q128, q, bf16, D, S, BH, "q")) ||
-      (st = encode_qkv_map(&maps.k128, k, bf16, D, S, BHkv, "k")) ||
-      (st = encode_qkv_map(&maps.v128, v, bf16, D, S, BHkv, "v")) ||
-      (st = encode_qkv_map(&maps.do128, dout, bf16, D, S, BH, "dout")) ||
-      (st = encode_qkv_map(&maps.q64, q, bf16, D, S, BH, "q", 64)) ||
-      (st = encode_qkv_map(&maps.k64, k, bf16, D, S, BHkv, "k", 64)) ||
-      (st = encode_qkv_map(&maps.v64, v, bf16, D, S, BHkv, "v", 64)) ||
-      (st = encode_qkv_map(&maps.do64, dout, bf16, D, S, BH, "dout", 64)))
+  if ((st = encode_input(&maps.q128, q, bf16, sh, sh.H, "q")) ||
+      (st = encode_input(&maps.k128, k, bf16, sh, sh.H_kv, "k")) ||
+      (st = encode_input(&maps.v128, v, bf16, sh, sh.H_kv, "v")) ||
+      (st = encode_input(&maps.do128, dout, bf16, sh, sh.H, "dout")) ||
+      (st = encode_input(&maps.q64, q, bf16, sh, sh.H, "q", 64)) ||
+      (st = encode_input(&maps.k64, k, bf16, sh, sh.H_kv, "k", 64)) ||
+      (st = encode_input(&maps.v64, v, bf16, sh, sh.H_kv, "v", 64)) ||
+      (st = encode_input(&maps.do64, dout, bf16, sh, sh.H, "dout", 64)))
     return st;
   fa::BwdParams p;
   p.o = o;
@@ -322,38 +303,138 @@ fa_status bwd_impl(const void* q, const void* k, const void* v, const void* o, c
   p.dq = dq;
   p.dk = dk;
   p.dv = dv;
-  p.S = static_cast<int>(S);
-  p.BH = static_cast<int>(BH);
-  p.group = static_cast<int>(H / H_kv);
+  p.S = static_cast<int>(sh.S);
+  p.cu_seqlens = sh.cu;
+  p.heads = static_cast<int>(sh.H);
+  p.total = static_cast<int>(sh.packed() ? sh.total : 0);
+  p.BH = static_cast<int>(sh.B * sh.H);
+  p.group = static_cast<int>(sh.H / sh.H_kv);
   p.kv_splits = splits;
   p.dkv_part = splits > 1 ? reinterpret_cast<float*>(static_cast<char*>(workspace) + delta_bytes) : nullptr;
-  p.n_tiles = static_cast<int>((S + 127) / 128);
-  p.n_partner = static_cast<int>((S + 63) / 64);
+  p.n_tiles = static_cast<int>((sh.S + 127) / 128);
   p.causal = causal ? 1 : 0;
   p.scale = scale;
   p.scale_log2 = scale * kLog2e;
   p.err = fa::device_error_word();
   if (!p.err) return fail(FA_ERR_CUDA, "cannot resolve the device error word on the current device");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int Di = static_cast<int>(D);
+  const int Di = static_cast<int>(sh.D);
+  const int64_t q_rows = sh.q_rows(), kv_rows = sh.kv_rows();
   auto mark = [&](int i) -> fa_status {
     if (!marks || !marks[i]) return FA_OK;
     return from_cuda(cudaEventRecord(static_cast<cudaEvent_t>(marks[i]), s), "event record");
   };
   if ((st = mark(0))) return st;
-  if ((st = from_cuda(fa::launch_bwd_preprocess(Di, bf16, p, s), "backward preprocess launch"))) return st;
+  if ((st = from_cuda(fa::launch_bwd_preprocess(Di, bf16, p, q_rows, s), "backward preprocess launch"))) return st;
   if ((st = mark(1))) return st;
   if ((st = from_cuda(fa::launch_bwd_dkdv(Di, bf16, maps, p, s), "backward dK/dV launch"))) return st;
-  if (splits > 1 && (st = from_cuda(fa::launch_bwd_dkv_reduce(Di, bf16, p, s), "backward dK/dV reduce launch")))
+  if (splits > 1 &&
+      (st = from_cuda(fa::launch_bwd_dkv_reduce(Di, bf16, p, kv_rows, s), "backward dK/dV reduce launch")))
     return st;
   if ((st = mark(2))) return st;
   if ((st = from_cuda(fa::launch_bwd_dq(Di, bf16, maps, p, s), "backward dQ launch"))) return st;
   return mark(3);
 }
 
+Shape fixed(int64_t B, int64_t H, int64_t H_kv, int64_t S, int64_t D) {
+  return Shape{B, H, H_kv, S, D, nullptr, 0, false};
+}
+
+Shape packed(const int32_t* cu, int64_t batch, int64_t max_seqlen, int64_t total, int64_t H, int64_t H_kv,
+             int64_t D) {
+  return Shape{batch, H, H_kv, max_seqlen, D, cu, total, true};
+}
+
 }  // namespace
 
 extern "C" {
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H, int64_t S,
+                 int64_t D, int causal, float scale, fa_dtype dtype, void* stream) {
+  return fwd_impl(q, k, v, o, lse, fixed(B, H, H, S, D), causal, scale, dtype, stream);
+}
+
+fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
+                     int64_t H_kv, int64_t S, int64_t D, int causal, float scale, fa_dtype dtype, void* stream) {
+  return fwd_impl(q, k, v, o, lse, fixed(B, H, H_kv, S, D), causal, scale, dtype, stream);
+}
+
+fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                        const int32_t* cu_seqlens, int64_t batch, int64_t max_seqlen, int64_t total, int64_t H,
+                        int64_t H_kv, int64_t D, int causal, float scale, fa_dtype dtype, void* stream) {
+  return fwd_impl(q, k, v, o, lse, packed(cu_seqlens, batch, max_seqlen, total, H, H_kv, D), causal, scale, dtype,
+                  stream);
+}
+
+size_t fa_bwd_workspace_size(int64_t B, int64_t H, int64_t S, int64_t D) {
+  int splits = 1;
+  size_t delta_bytes = 0;
+  if (B < 0 || H < 0 || S < 0) return 0;
+  return bwd_workspace_layout(fixed(B, H, H, S, D), &splits, &delta_bytes);
+}
+
+size_t fa_bwd_gqa_workspace_size(int64_t B, int64_t H, int64_t H_kv, int64_t S, int64_t D) {
+  if (B < 0 || S < 0 || H_kv <= 0 || H <= 0 || H % H_kv != 0) return 0;
+  int splits = 1;
+  size_t delta_bytes = 0;
+  return bwd_workspace_layout(fixed(B, H, H_kv, S, D), &splits, &delta_bytes);
+}
+
+size_t fa_bwd_varlen_workspace_size(int64_t batch, int64_t max_seqlen, int64_t total, int64_t H, int64_t H_kv,
+                                    int64_t D) {
+  if (batch < 0 || max_seqlen < 0 || total < 0 || H_kv <= 0 || H <= 0 || H % H_kv != 0) return 0;
+  int splits = 1;
+  size_t delta_bytes = 0;
+  return bwd_workspace_layout(packed(nullptr, batch, max_seqlen, total, H, H_kv, D), &splits, &delta_bytes);
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                 void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t S, int64_t D, int causal, float scale,
+                 fa_dtype dtype, void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, fixed(B, H, H, S, D), causal, scale, dtype, workspace,
+                  workspace_bytes, stream, nullptr);
+}
+
+fa_status fa_bwd_marked(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                        const float* lse, void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t S, int64_t D,
+                        int causal, float scale, fa_dtype dtype, void* workspace, size_t workspace_bytes,
+                        void* stream, void* const* marks) {
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, fixed(B, H, H, S, D), causal, scale, dtype, workspace,
+                  workspace_bytes, stream, marks);
+}
+
+fa_status fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                     void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t H_kv, int64_t S, int64_t D,
+                     int causal, float scale, fa_dtype dtype, void* workspace, size_t workspace_bytes,
+                     void* stream) {
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, fixed(B, H, H_kv, S, D), causal, scale, dtype, workspace,
+                  workspace_bytes, stream, nullptr);
+}
+
+fa_status fa_bwd_gqa_marked(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                            const float* lse, void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t H_kv,
+                            int64_t S, int64_t D, int causal, float scale, fa_dtype dtype, void* workspace,
+                            size_t workspace_bytes, void* stream, void* const* marks) {
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, fixed(B, H, H_kv, S, D), causal, scale, dtype, workspace,
+                  workspace_bytes, stream, marks);
+}
+
+fa_status fa_bwd_varlen_marked(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                               const float* lse, void* dq, void* dk, void* dv, const int32_t* cu_seqlens,
+                               int64_t batch, int64_t max_seqlen, int64_t total, int64_t H, int64_t H_kv, int64_t D,
+                               int causal, float scale, fa_dtype dtype, void* workspace, size_t workspace_bytes,
+                               void* stream, void* const* marks) {
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, packed(cu_seqlens, batch, max_seqlen, total, H, H_kv, D),
+                  causal, scale, dtype, workspace, workspace_bytes, stream, marks);
+}
+
+fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                        const float* lse, void* dq, void* dk, void* dv, const int32_t* cu_seqlens, int64_t batch,
+                        int64_t max_seqlen, int64_t total, int64_t H, int64_t H_kv, int64_t D, int causal,
+                        float scale, fa_dtype dtype, void* workspace, size_t workspace_bytes, void* stream) {
+  return fa_bwd_varlen_marked(q, k, v, o, dout, lse, dq, dk, dv, cu_seqlens, batch, max_seqlen, total, H, H_kv, D,
+                              causal, scale, dtype, workspace, workspace_bytes, stream, nullptr);
+}
 
 fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dout,
                          const float* lse, void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t S,
@@ -400,6 +481,8 @@ fa_status fa_check_device_errors(void* stream) {
   if (code != 0) {
     const int zero = 0;
     cudaMemcpyToSymbol(fa::g_fa_device_error, &zero, sizeof(int));
+    if (code == fa::kErrBadSeqlens)
+      return fail(FA_ERR_INVALID_ARG, "cu_seqlens contradicts max_seqlen or the token count (checked on the device)");
     return fail(FA_ERR_TIMEOUT, "device pipeline wait timed out (code %d)", code);
   }
   return FA_OK;

@@ -43,6 +43,9 @@
 namespace fa {
 using namespace ptx;
 
+// Source of L = +inf for partner query rows past a sample's end (dK/dV pass).
+__device__ const float g_pos_inf = __builtin_huge_valf();
+
 // ------------------------------------------------------------------ preprocess
 // Delta_i = sum_d dO_id * O_id in fp32.  D/8 threads share a row, each
 // reading 16 bytes of O and of dO; a shuffle tree sums the group.
@@ -79,7 +82,10 @@ __global__ void __launch_bounds__(256) fa_bwd_preprocess_kernel(const BwdParams 
     }
 #pragma unroll
     for (int off = kTpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (row < rows && sub == 0) p.delta[row] = acc;
+    // Row `row` of [B*H*S, D] (fixed length) or of [T*H, D] (packed: token
+    // row / H, head row % H, whose Delta lives at [head, token]).
+    if (row < rows && sub == 0)
+      p.delta[p.cu_seqlens ? (row % p.heads) * p.total + row / p.heads : row] = acc;
   }
 }
 
@@ -304,15 +310,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int bh = KV_OUTER ? static_cast<int>(blockIdx.x) / p.kv_splits : static_cast<int>(blockIdx.x);
   const int kv_part = KV_OUTER ? static_cast<int>(blockIdx.x) - bh * p.kv_splits : 0;
   const int hpc = KV_OUTER ? p.group / p.kv_splits : 1;
-  const int S = p.S;
+  // Rows of the sample (the two layouts of BwdParams).  Head indices below are
+  // global (b*H + h) in the fixed-length layout and within a token (h) when
+  // packed: own_h for the CTA's own tiles, pz0 for the first partner head.
+  const bool packed = p.cu_seqlens != nullptr;
+  const int heads_own = KV_OUTER ? p.heads / p.group : p.heads;  // per batch entry
+  int S = p.S;
+  int tok0 = 0;
+  int own_h = bh;
+  int pz0 = KV_OUTER ? bh * p.group + kv_part * hpc : bh / p.group;
+  if (packed) {
+    const int b = bh / heads_own;
+    if (!packed_sample(p.cu_seqlens, b, p.S, p.total, p.err, &tok0, &S)) return;
+    own_h = bh - b * heads_own;
+    pz0 = KV_OUTER ? own_h * p.group + kv_part * hpc : own_h / p.group;
+  }
+  // Row r of head h: TMA coordinates (r, h) fixed, (h, tok0 + r) packed; its
+  // L and Delta at h * lstride + loff + r.
+  const int lstride = packed ? p.total : S;
+  const int loff = tok0;
   const int nt = p.n_tiles;
-  const int np = p.n_partner;
-  const int64_t rowbase = static_cast<int64_t>(bh) * S;
+  const int np = (S + kPN - 1) / kPN;
   // Own tile; heavy tiles first under the causal mask (key tile 0 and query
   // tile nt-1 see the most partners).
   const int own = KV_OUTER ? static_cast<int>(blockIdx.y)
                            : (p.causal ? nt - 1 - static_cast<int>(blockIdx.y) : static_cast<int>(blockIdx.y));
   const int own0 = own * 128;
+  if (own0 >= S) return;  // packed batch: this CTA lies past its sample
   const int first = (KV_OUTER && p.causal) ? own0 / kPN : 0;
   const int last_excl = (!KV_OUTER && p.causal) ? min(np, (own0 + 127) / kPN + 1) : np;
   // Partner blocks per partner head; the dK/dV pass streams them for each of
@@ -367,13 +391,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_arrive_expect_tx(bar_afull, 2 * GA::kTileBytes);
 #pragma unroll
       for (int ch = 0; ch < GA::kChunks; ++ch) {
-        tma_load_3d(smem + L::kOffA1 + ch * GA::kChunkBytes, &tm_a1, bar_afull, ch * (GA::kRowBytes / 2), own0, bh);
-        tma_load_3d(smem + L::kOffA2 + ch * GA::kChunkBytes, &tm_a2, bar_afull, ch * (GA::kRowBytes / 2), own0, bh);
+        tma_load_3d(smem + L::kOffA1 + ch * GA::kChunkBytes, &tm_a1, bar_afull, ch * (GA::kRowBytes / 2),
+                    packed ? own_h : own0, packed ? tok0 + own0 : own_h);
+        tma_load_3d(smem + L::kOffA2 + ch * GA::kChunkBytes, &tm_a2, bar_afull, ch * (GA::kRowBytes / 2),
+                    packed ? own_h : own0, packed ? tok0 + own0 : own_h);
       }
     }
     int it = 0;
     // Partner head and block of iteration `it`, stepped along without divisions.
-    int pz = KV_OUTER ? bh * p.group + kv_part * hpc : bh / p.group;
+    int pz = pz0;
     int pblk = first;
     for (; it < niter; ++it, ++pblk) {
       if (KV_OUTER && pblk == last_excl) {
@@ -389,18 +415,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int ch = 0; ch < GB::kChunks; ++ch) {
           tma_load_3d(smem + L::kOffB1 + st * GB::kTileBytes + ch * GB::kChunkBytes, &tm_b1, &bar_bfull[st],
-                      ch * (GB::kRowBytes / 2), r0, pz);
+                      ch * (GB::kRowBytes / 2), packed ? pz : r0, packed ? tok0 + r0 : pz);
           tma_load_3d(smem + L::kOffB2 + st * GB::kTileBytes + ch * GB::kChunkBytes, &tm_b2, &bar_bfull[st],
-                      ch * (GB::kRowBytes / 2), r0, pz);
+                      ch * (GB::kRowBytes / 2), packed ? pz : r0, packed ? tok0 + r0 : pz);
         }
       }
       if constexpr (KV_OUTER) {
         float* v = vecs + st * 2 * kPN;
 #pragma unroll
         for (int h = 0; h < kPN; h += 32) {
+          // Partner queries past the sample read L = +inf and Delta = 0, so
+          // their P and dS are exactly 0 (when packed, their Q and dO rows
+          // are the next sample's).
           const int q = r0 + h + lane;
-          const int64_t src = static_cast<int64_t>(pz) * S + (q < S ? q : S - 1);
-          cp_async_4(v + h + lane, p.lse + src, q < S);
+          const int64_t src = static_cast<int64_t>(pz) * lstride + loff + (q < S ? q : S - 1);
+          cp_async_4(v + h + lane, q < S ? p.lse + src : &g_pos_inf, true);
           cp_async_4(v + kPN + h + lane, p.delta + src, q < S);
         }
         cp_async_mbar_arrive(&bar_bfull[st]);
@@ -524,9 +553,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // (rows past S: L2 = +inf, so their probabilities are exactly 0).
     float my_l2 = INFINITY, my_delta = 0.f;
     if (!KV_OUTER && my < S) {
-      my_l2 = p.lse[rowbase + my] * kLog2e;
-      my_delta = p.delta[rowbase + my];
+      const int64_t li = static_cast<int64_t>(own_h) * lstride + loff + my;
+      my_l2 = p.lse[li] * kLog2e;
+      my_delta = p.delta[li];
     }
+    // dQ pass: last visible key of this row (its own index under the causal
+    // mask), and whether a partner block can hold keys past the sample that
+    // must be masked (packed batch: those rows belong to the next sample).
+    const int last_key = p.causal ? min(my, S - 1) : S - 1;
     bool alive = true;
     int pi = g;  // i modulo nper: the partner block within its head (dK/dV pass)
     if constexpr (KV_OUTER) {
@@ -553,10 +587,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const float* dv = lv + kPN;                    // and their Delta
       // Diagonal blocks under the causal mask: the dK/dV pass zeroes partner
       // column c where query partner0 + col0 + c < key `my`, the dQ pass where
-      // key partner0 + col0 + c > query `my`.  Rows and columns past S need no
-      // mask: their zero-filled operands make their terms vanish (see above).
-      const bool diag = p.causal && (KV_OUTER ? partner0 < own0 + 128 : partner0 + kPN - 1 > own0);
-      const int lim = my - partner0 - col0;
+      // key partner0 + col0 + c > its last visible key.  Partner queries past
+      // S have P = 0 from L = +inf; partner keys past S vanish through their
+      // zero-filled K rows, except when packed, where the dQ pass masks them.
+      const bool diag = (p.causal && (KV_OUTER ? partner0 < own0 + 128 : partner0 + kPN - 1 > own0)) ||
+                        (!KV_OUTER && packed && partner0 + kPN > S);
+      const int lim = last_key - partner0 - col0;
       // Off-diagonal blocks (all but one or two per tile) take the path with
       // no per-element compare or select.
       if constexpr (KV_OUTER) {
@@ -587,7 +623,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_after();
       const int c_begin = col_part * kEpiCols;
       const bool row_ok = my < S;
-      const size_t off = (static_cast<size_t>(rowbase) + (row_ok ? my : 0)) * D;
+      // Output row of (own head, row my): own_h * S + my fixed length,
+      // (tok0 + my) * heads_own + own_h packed.
+      const int mr = row_ok ? my : 0;
+      const int64_t orow = packed ? static_cast<int64_t>(tok0 + mr) * heads_own + own_h
+                                  : static_cast<int64_t>(own_h) * S + mr;
+      const size_t off = static_cast<size_t>(orow) * D;
       const uint32_t t_acc = tmem + lane_base;
       if constexpr (KV_OUTER) {
         if (p.kv_splits == 1) {
@@ -604,8 +645,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         } else {
           // This CTA's share of the group: fp32 rows [dV | scale * dK] of
           // partial `kv_part`, summed by the reduce kernel.
-          const int64_t n_rows = static_cast<int64_t>(p.BH / p.group) * S;
-          float* prow = p.dkv_part + ((static_cast<int64_t>(kv_part) * n_rows + rowbase + (row_ok ? my : 0)) * (2 * D));
+          const int64_t n_rows = packed ? static_cast<int64_t>(p.total) * heads_own
+                                        : static_cast<int64_t>(p.BH / p.group) * S;
+          float* prow = p.dkv_part + ((static_cast<int64_t>(kv_part) * n_rows + orow) * (2 * D));
 #pragma unroll
           for (int c = c_begin; c < c_begin + kEpiCols; c += 16) {
             uint32_t v16[16];
@@ -638,8 +680,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 namespace {
 
 template <int D, bool BF16>
-cudaError_t launch_pre_t(const BwdParams& p, cudaStream_t stream) {
-  const int64_t rows = static_cast<int64_t>(p.BH) * p.S;
+cudaError_t launch_pre_t(const BwdParams& p, int64_t rows, cudaStream_t stream) {
   const int64_t threads = rows * (D / 8);
   const int64_t blocks = (threads + 255) / 256;
   const int grid = static_cast<int>(blocks < 152 * 16 ? blocks : 152 * 16);
@@ -661,8 +702,7 @@ cudaError_t launch_main_t(const CUtensorMap& a1, const CUtensorMap& a2, const CU
 }
 
 template <int D, bool BF16>
-cudaError_t launch_reduce_t(const BwdParams& p, cudaStream_t stream) {
-  const int64_t rows = static_cast<int64_t>(p.BH / p.group) * p.S;
+cudaError_t launch_reduce_t(const BwdParams& p, int64_t rows, cudaStream_t stream) {
   const int64_t threads = rows * (2 * D / 8);
   const int64_t blocks = (threads + 255) / 256;
   const int grid = static_cast<int>(blocks < 152 * 8 ? blocks : 152 * 8);
@@ -689,8 +729,8 @@ int bwd_kv_splits(int64_t BHkv, int64_t n_tiles, int group) {
     default: return cudaErrorInvalidValue;                      \
   }
 
-cudaError_t launch_bwd_preprocess(int D, bool bf16, const BwdParams& p, cudaStream_t stream) {
-#define FA_PRE(DD, BB) launch_pre_t<DD, BB>(p, stream)
+cudaError_t launch_bwd_preprocess(int D, bool bf16, const BwdParams& p, int64_t rows, cudaStream_t stream) {
+#define FA_PRE(DD, BB) launch_pre_t<DD, BB>(p, rows, stream)
   FA_BWD_DISPATCH(FA_PRE)
 #undef FA_PRE
 }
@@ -701,8 +741,8 @@ cudaError_t launch_bwd_dkdv(int D, bool bf16, const BwdMaps& m, const BwdParams&
 #undef FA_DKDV
 }
 
-cudaError_t launch_bwd_dkv_reduce(int D, bool bf16, const BwdParams& p, cudaStream_t stream) {
-#define FA_RED(DD, BB) launch_reduce_t<DD, BB>(p, stream)
+cudaError_t launch_bwd_dkv_reduce(int D, bool bf16, const BwdParams& p, int64_t rows, cudaStream_t stream) {
+#define FA_RED(DD, BB) launch_reduce_t<DD, BB>(p, rows, stream)
   FA_BWD_DISPATCH(FA_RED)
 #undef FA_RED
 }

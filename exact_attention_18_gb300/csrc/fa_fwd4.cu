@@ -118,11 +118,23 @@ __global__ void __launch_bounds__(kF4Threads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int bh = blockIdx.x;
-  const int kvh = bh / p.group;  // K/V head shared by this query head's group
-  const int S = p.S;
+  // Where this head's rows live (the two layouts of FwdParams).  TMA
+  // coordinates of row r: (r, head) fixed length, (head, tok0 + r) packed.
+  const bool packed = p.cu_seqlens != nullptr;
+  int S = p.S;
+  int q_head = bh, kv_head = bh / p.group, tok0 = 0;  // K/V head shared by the query head's group
+  if (packed) {
+    const int b = bh / p.heads;
+    q_head = bh - b * p.heads;
+    kv_head = q_head / p.group;
+    if (!packed_sample(p.cu_seqlens, b, p.S, p.total, p.err, &tok0, &S)) return;
+  }
+  auto ty = [&](int r, int head) { return packed ? head : r; };
+  auto tz = [&](int r, int head) { return packed ? tok0 + r : head; };
   // Under the causal mask the heaviest CTAs are launched first.
   const int cta = p.causal ? p.n_m_tiles - 1 - static_cast<int>(blockIdx.y) : static_cast<int>(blockIdx.y);
   const int row0 = cta * kF4RowsPerCta;
+  if (row0 >= S) return;  // packed batch: this CTA lies past its sample
   const int n_kv = (S + kBN - 1) / kBN;
   // Key blocks visited by the 128-row tile starting at row r (0 past S).
   auto blocks_for = [&](int r) {
@@ -171,16 +183,19 @@ __global__ void __launch_bounds__(kF4Threads, 1)
         mbar_arrive_expect_tx(bar_q, kF4Tiles * GQ::kTileBytes);
 #pragma unroll
         for (int t = 0; t < kF4Tiles; ++t)
-          tma_load_3d(smem + L::kOffQ + t * GQ::kTileBytes, &tm_q, bar_q, 0, row0 + t * kBlockM, bh);
+          tma_load_3d(smem + L::kOffQ + t * GQ::kTileBytes, &tm_q, bar_q, 0, ty(row0 + t * kBlockM, q_head),
+                      tz(row0 + t * kBlockM, q_head));
         int it = 0;
         for (; it < nbp; ++it) {
           const int st = it % L::kStages;
           const int use = it / L::kStages;
           if (use > 0 && !mbar_wait(&bar_empty[st], (use - 1) & 1, abort_flag, p.err, kErrTimeoutLoad)) break;
           mbar_arrive_expect_tx(&bar_kfull[st], GK::kTileBytes);
-          tma_load_3d(smem + L::kOffK + st * GK::kTileBytes, &tm_k, &bar_kfull[st], 0, it * kBN, kvh);
+          tma_load_3d(smem + L::kOffK + st * GK::kTileBytes, &tm_k, &bar_kfull[st], 0, ty(it * kBN, kv_head),
+                      tz(it * kBN, kv_head));
           mbar_arrive_expect_tx(&bar_vfull[st], GK::kTileBytes);
-          tma_load_3d(smem + L::kOffV + st * GK::kTileBytes, &tm_v, &bar_vfull[st], 0, it * kBN, kvh);
+          tma_load_3d(smem + L::kOffV + st * GK::kTileBytes, &tm_v, &bar_vfull[st], 0, ty(it * kBN, kv_head),
+                      tz(it * kBN, kv_head));
         }
         // Teardown: every copy this thread started must land before the CTA exits.
         drain_wait(bar_q, 0, p.err);
@@ -374,14 +389,19 @@ __global__ void __launch_bounds__(kF4Threads, 1)
       tc_fence_after();
       const float inv_l = 1.f / l;
       const bool row_ok = row_g < S;
-      elem_t* orow = reinterpret_cast<elem_t*>(p.o) + (static_cast<size_t>(bh) * S + (row_ok ? row_g : 0)) * D;
+      // Output row: bh*S + row fixed length, (tok0 + row)*H + head packed;
+      // L at bh*S + row, or head*T + tok0 + row.
+      const int rr = row_ok ? row_g : 0;
+      const size_t o_row = packed ? static_cast<size_t>(tok0 + rr) * p.heads + q_head : static_cast<size_t>(bh) * S + rr;
+      const size_t l_idx = packed ? static_cast<size_t>(q_head) * p.total + tok0 + rr : static_cast<size_t>(bh) * S + rr;
+      elem_t* orow = reinterpret_cast<elem_t*>(p.o) + o_row * D;
 #pragma unroll
       for (int c = 0; c < D; c += 16) {
         uint32_t o16[16];
         tmem_ld16(t_o + c, o16);
         if (row_ok) store_row16<BF16>(orow + c, o16, inv_l);
       }
-      if (row_ok) p.lse[static_cast<size_t>(bh) * S + row_g] = (m + log2f(l)) * 0.69314718055994530942f;
+      if (row_ok) p.lse[l_idx] = (m + log2f(l)) * 0.69314718055994530942f;
     }
   }
 

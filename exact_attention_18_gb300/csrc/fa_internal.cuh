@@ -10,10 +10,19 @@ namespace fa {
 constexpr int kBlockM = 128;  // query rows per tile (= TMEM lanes)
 constexpr int kBlockN = 128;  // key rows per tile
 
+// Two layouts.  Fixed length (cu_seqlens == nullptr): [B*H, S, D] tensors,
+// row r of head bh at element (bh*S + r)*D, L at bh*S + r, tensor maps
+// {D, S, heads}.  Packed batch (cu_seqlens != nullptr): [T, H, D] tensors
+// (token-major), sample b = tokens cu[b] .. cu[b+1]-1, its row r is token
+// cu[b] + r; L is [H, T]; tensor maps {D, heads, T}; S is then the largest
+// sample length and blockIdx.x = b*H + h.
 struct FwdParams {
-  void* o;             // [BH, S, D] output
-  float* lse;          // [BH, S] natural-log logsumexp
-  int S;               // sequence length
+  void* o;             // [BH, S, D] or [T, H, D] output
+  float* lse;          // [BH, S] or [H, T] natural-log logsumexp
+  int S;               // sequence length (packed batch: max_seqlen)
+  const int* cu_seqlens;  // packed batch: [B + 1] token offsets in device memory; else nullptr
+  int heads;           // H (query heads per batch entry)
+  int total;           // packed batch: T tokens
   int n_m_tiles;       // CTAs per (b, h): ceil(S / fwd_rows_per_cta(D))
   int causal;          // nonzero: key j visible to query i iff j <= i
   int group;           // query heads per K/V head: query head bh reads K/V head bh / group
@@ -22,20 +31,23 @@ struct FwdParams {
 };
 
 struct BwdParams {
-  const void* o;       // [BH, S, D] forward output (BH counts query heads)
+  const void* o;       // [BH, S, D] (or [T, H, D]) forward output (BH counts query heads)
   const void* dout;    // [BH, S, D] loss gradient w.r.t. O
   const float* lse;    // [BH, S] natural-log logsumexp from the forward
   float* delta;        // [BH, S] workspace: rowsum(dO o O)
   void* dq;            // [BH, S, D]
   void* dk;            // [BH / group, S, D]
   void* dv;            // [BH / group, S, D]
-  int S;
+  int S;               // sequence length (packed batch: max_seqlen)
+  const int* cu_seqlens;  // packed batch: [B + 1] token offsets in device memory; else nullptr
+  int heads;           // H
+  int total;           // packed batch: T tokens
   int BH;              // query heads B*H
   int group;           // query heads per K/V head (H / H_kv); K/V head of query head bh is bh / group
   int kv_splits;       // dK/dV pass: CTAs sharing a (K/V head, key tile), each over group / kv_splits heads
-  float* dkv_part;     // kv_splits > 1: fp32 partial sums [kv_splits][BH / group][S][2 D] (dV | scale*dK)
+  float* dkv_part;     // kv_splits > 1: fp32 partial sums [kv_splits][K/V rows][2 D] (dV | scale*dK),
+                       // K/V rows in dK's own row order (B*H_kv*S, or T*H_kv packed)
   int n_tiles;         // ceil(S / 128): own tiles per (b, h)
-  int n_partner;       // ceil(S / 64): streamed partner blocks per (b, h)
   int causal;
   float scale;         // softmax scale (dQ, dK factor)
   float scale_log2;    // scale * log2(e)
@@ -61,11 +73,13 @@ cudaError_t launch_fwd4(int D, bool bf16, const CUtensorMap& tq, const CUtensorM
 cudaError_t launch_fwd(int D, bool bf16, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdParams& p, int BH, cudaStream_t stream);
 
-cudaError_t launch_bwd_preprocess(int D, bool bf16, const BwdParams& p, cudaStream_t stream);
+// rows: query rows (B*H*S, or T*H packed).
+cudaError_t launch_bwd_preprocess(int D, bool bf16, const BwdParams& p, int64_t rows, cudaStream_t stream);
 cudaError_t launch_bwd_dkdv(int D, bool bf16, const BwdMaps& maps, const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_dq(int D, bool bf16, const BwdMaps& maps, const BwdParams& p, cudaStream_t stream);
-// Sums the kv_splits partial dK/dV rows and writes dK, dV (only when kv_splits > 1).
-cudaError_t launch_bwd_dkv_reduce(int D, bool bf16, const BwdParams& p, cudaStream_t stream);
+// Sums the kv_splits partial dK/dV rows and writes dK, dV (only when kv_splits > 1);
+// rows: K/V rows (B*H_kv*S, or T*H_kv packed).
+cudaError_t launch_bwd_dkv_reduce(int D, bool bf16, const BwdParams& p, int64_t rows, cudaStream_t stream);
 
 // CTAs per (K/V head, key tile) in the dK/dV pass: the smallest divisor of
 // `group` that gives at least two CTAs per SM of a 152-SM GPU (1 when the

@@ -85,6 +85,24 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, int* 
   }
 }
 
+// Packed batch: first token and length of sample b from cu_seqlens (read by
+// every thread).  Returns false, and records kErrBadSeqlens, when the entries
+// contradict the call (negative start, decreasing offsets, a sample longer
+// than max_len, or one ending past `total` tokens); the caller then exits
+// before touching any tensor.
+__device__ __forceinline__ bool packed_sample(const int* cu, int b, int max_len, int total, int* err, int* tok0,
+                                              int* len) {
+  const int a = __ldg(cu + b);
+  const int e = __ldg(cu + b + 1);
+  *tok0 = a;
+  *len = e - a;
+  if (a < 0 || e < a || e - a > max_len || e > total) {
+    if (threadIdx.x == 0) ptx::record_error(err, kErrBadSeqlens);
+    return false;
+  }
+  return true;
+}
+
 // Named barrier among the `nthreads` threads (a multiple of 32) that use `id`.
 __device__ __forceinline__ void named_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

@@ -22,6 +22,7 @@ enum DeviceErrorCode : int {
   kErrTimeoutMma = 2,      // MMA issuer waited too long for operands
   kErrTimeoutSoftmax = 3,  // softmax warps waited too long for scores / partial O
   kErrTimeoutDrain = 4,    // teardown waited too long for in-flight copies / MMAs
+  kErrBadSeqlens = 5,      // packed batch: cu_seqlens inconsistent with max_seqlen / total
 };
 
 namespace ptx {

@@ -171,6 +171,49 @@ fa_status fa_bwd_gqa_marked(const void* q, const void* k, const void* v, const v
                             size_t workspace_bytes, void* stream, void* const* marks);
 
 /*
+ * Packed variable-length batches ("Inside FlashAttention" §6.1, varlen: samples
+ * of different lengths concatenated with no padding, a prefix-sum array
+ * cu_seqlens marking their bounds, and no attention across samples).
+ *   q, o           : [T, H, D]     (token-major; T = total tokens)
+ *   k, v           : [T, H_kv, D]  (H a positive multiple of H_kv, as in fa_fwd_gqa)
+ *   lse            : [H, T] fp32, natural-log logsumexp
+ *   cu_seqlens     : DEVICE int32 [batch + 1]; cu[0] = 0, non-decreasing,
+ *                    cu[batch] <= total; sample b is tokens cu[b] .. cu[b+1]-1
+ *                    (empty samples allowed) and attends only to itself, with the
+ *                    top-left causal mask inside the sample when causal.
+ *   max_seqlen     : host bound on every sample length (sizes the grid).
+ * The kernels read cu_seqlens themselves.  A sample longer than max_seqlen,
+ * or one that runs past `total`, is not computed: the kernels record it and
+ * fa_check_device_errors() then returns FA_ERR_INVALID_ARG.  Rows of tokens
+ * that no sample covers are left unwritten.  Other conventions as fa_fwd
+ * (cu_seqlens needs 4-byte alignment only).  batch, H, max_seqlen or total
+ * equal to 0 is an empty call.
+ */
+fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                        const int32_t* cu_seqlens, int64_t batch, int64_t max_seqlen, int64_t total, int64_t H,
+                        int64_t H_kv, int64_t D, int causal, float scale, fa_dtype dtype, void* stream);
+
+/* Workspace bytes of fa_bwd_varlen: Delta for the T*H query rows, plus the
+ * dK/dV partial sums when the grouped pass splits (as fa_bwd_gqa_workspace_size,
+ * with batch entries of up to max_seqlen rows; T*H_kv K/V rows). */
+size_t fa_bwd_varlen_workspace_size(int64_t batch, int64_t max_seqlen, int64_t total, int64_t H, int64_t H_kv,
+                                    int64_t D);
+
+/* Backward of fa_fwd_varlen: dq [T, H, D], dk, dv [T, H_kv, D]; the packed
+ * layout and checks of fa_fwd_varlen, the rest as fa_bwd_gqa. */
+fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                        const float* lse, void* dq, void* dk, void* dv, const int32_t* cu_seqlens, int64_t batch,
+                        int64_t max_seqlen, int64_t total, int64_t H, int64_t H_kv, int64_t D, int causal,
+                        float scale, fa_dtype dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/* fa_bwd_varlen with the timing marks of fa_bwd_marked. */
+fa_status fa_bwd_varlen_marked(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                               const float* lse, void* dq, void* dk, void* dv, const int32_t* cu_seqlens,
+                               int64_t batch, int64_t max_seqlen, int64_t total, int64_t H, int64_t H_kv, int64_t D,
+                               int causal, float scale, fa_dtype dtype, void* workspace, size_t workspace_bytes,
+                               void* stream, void* const* marks);
+
+/*
  * fa_bwd without a workspace argument, for callers that cannot allocate
  * device memory when they run the backward pass (for example code inside a
  * custom allocator or a fully carved-up memory pool, or a framework that
@@ -201,8 +244,10 @@ const char* fa_last_error_detail(void);
 
 /*
  * Synchronises `stream`, then reads and clears the device error word that the
- * kernels set when a pipeline wait times out.  Returns FA_ERR_TIMEOUT if it
- * was set, FA_ERR_CUDA if the synchronisation failed, else FA_OK.  Meant for
+ * kernels set when a pipeline wait times out or a packed batch's cu_seqlens
+ * contradicts its call.  Returns FA_ERR_TIMEOUT or FA_ERR_INVALID_ARG (the
+ * latter for cu_seqlens) if it was set, FA_ERR_CUDA if the synchronisation
+ * failed, else FA_OK.  Meant for
  * tests and debugging; the compute entry points never synchronise.
  */
 fa_status fa_check_device_errors(void* stream);

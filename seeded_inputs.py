@@ -104,3 +104,75 @@ CONFIGS["gqa"] = Workload("gqa_causal_fwdbwd_B4H16Hkv2S4096D64_fp16", 4, 16, 409
                           backward=True, H_kv=2)
 CONFIGS["mqa"] = Workload("mqa_causal_fwdbwd_B4H16Hkv1S4096D64_fp16", 4, 16, 4096, 64, "fp16", True,
                           backward=True, H_kv=1)
+
+
+@dataclass(frozen=True)
+class PackedWorkload:
+    """A packed variable-length batch: samples of the given lengths back to back,
+    tensors [T, H, D] (K, V: [T, H_kv, D]), int32 cu_seqlens [batch + 1]."""
+
+    name: str
+    lengths: tuple
+    H: int
+    D: int
+    dtype: str = "fp16"
+    causal: bool = True
+    seed: int = 0
+    H_kv: int | None = None
+
+    @property
+    def kv_heads(self) -> int:
+        return self.H if self.H_kv is None else self.H_kv
+
+    @property
+    def total(self) -> int:
+        return sum(self.lengths)
+
+    @property
+    def batch(self) -> int:
+        return len(self.lengths)
+
+    @property
+    def max_seqlen(self) -> int:
+        return max(self.lengths) if self.lengths else 0
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.D)
+
+    @property
+    def torch_dtype(self) -> torch.dtype:
+        return DTYPES[self.dtype]
+
+    def cu_seqlens(self) -> torch.Tensor:
+        cu = [0]
+        for n in self.lengths:
+            cu.append(cu[-1] + int(n))
+        return torch.tensor(cu, dtype=torch.int32)
+
+    def describe(self) -> str:
+        mask = "causal" if self.causal else "non-causal"
+        kv = "" if self.kv_heads == self.H else f" H_kv{self.kv_heads}"
+        return (f"packed {self.batch} samples ({self.total} tokens, max {self.max_seqlen}) H{self.H}{kv} "
+                f"D{self.D} {self.dtype} {mask}")
+
+
+def make_packed_inputs(w: PackedWorkload) -> dict:
+    """CPU tensors q, k, v, do [T, heads, D] and cu_seqlens for ``w`` (same recipe as make_inputs)."""
+    dt = w.torch_dtype
+    T = w.total
+    return {
+        "q": randn((T, w.H, w.D), w.seed, dt),
+        "k": randn((T, w.kv_heads, w.D), w.seed + 1, dt),
+        "v": randn((T, w.kv_heads, w.D), w.seed + 2, dt),
+        "do": randn((T, w.H, w.D), w.seed + 3, dt),
+        "cu_seqlens": w.cu_seqlens(),
+    }
+
+
+# A packed batch with the token count of the causal B4 H16 S4096 D64 workload
+# (16384 tokens) split into ten samples of mixed, mostly ragged lengths.
+VARLEN_LENGTHS = (4000, 3100, 2048, 1999, 1536, 1100, 1024, 700, 577, 300)
+PACKED_CONFIGS = {
+    "varlen": PackedWorkload("varlen_causal_fwdbwd_T16384_10seq_H16D64_fp16", VARLEN_LENGTHS, 16, 64, "fp16", True),
+}

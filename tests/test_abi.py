@@ -162,6 +162,56 @@ def test_gqa_empty_is_a_no_op(lib, kw):
     assert bwd_gqa(**kw) == 0
 
 
+def fwd_varlen(**kw):
+    a = dict(q=P, k=P, v=P, o=P, lse=P, cu=P, batch=2, max_seqlen=128, total=200, H=4, H_kv=2, D=64, causal=1,
+             scale=0.125, dtype=0, stream=None)
+    a.update(kw)
+    return fa.fa_fwd_varlen(a["q"], a["k"], a["v"], a["o"], a["lse"], a["cu"], a["batch"], a["max_seqlen"],
+                            a["total"], a["H"], a["H_kv"], a["D"], a["causal"], a["scale"], a["dtype"], a["stream"])
+
+
+def bwd_varlen(**kw):
+    a = dict(q=P, k=P, v=P, o=P, do=P, lse=P, dq=P, dk=P, dv=P, cu=P, batch=2, max_seqlen=128, total=200, H=4,
+             H_kv=2, D=64, causal=1, scale=0.125, dtype=0, ws=P * 16, wsb=1 << 24, stream=None)
+    a.update(kw)
+    return fa.fa_bwd_varlen(a["q"], a["k"], a["v"], a["o"], a["do"], a["lse"], a["dq"], a["dk"], a["dv"], a["cu"],
+                            a["batch"], a["max_seqlen"], a["total"], a["H"], a["H_kv"], a["D"], a["causal"],
+                            a["scale"], a["dtype"], a["ws"], a["wsb"], a["stream"])
+
+
+VARLEN_BAD = [
+    (dict(cu=0), 1), (dict(cu=P + 2), 3), (dict(total=-1), 1), (dict(max_seqlen=-5), 1), (dict(batch=-1), 1),
+    (dict(H_kv=3), 1), (dict(D=80), 2), (dict(q=P + 8), 3), (dict(total=1 << 31), 2),
+    (dict(max_seqlen=65536 * 128), 2),
+]
+
+
+@pytest.mark.parametrize("kw,status", VARLEN_BAD)
+def test_fwd_varlen_rejects_bad_arguments(lib, kw, status):
+    assert fwd_varlen(**kw) == status
+    assert fa.fa_last_error_detail() != ""
+
+
+@pytest.mark.parametrize("kw,status", VARLEN_BAD + [(dict(ws=0), 4), (dict(wsb=64), 4), (dict(dv=P + 4), 3)])
+def test_bwd_varlen_rejects_bad_arguments(lib, kw, status):
+    assert bwd_varlen(**kw) == status
+    assert fa.fa_last_error_detail() != ""
+
+
+@pytest.mark.parametrize("kw", [dict(batch=0), dict(total=0), dict(max_seqlen=0), dict(H=0, H_kv=0),
+                                dict(total=0, cu=0, q=0, k=0, v=0, o=0, lse=0)])
+def test_varlen_empty_is_a_no_op(lib, kw):
+    assert fwd_varlen(**kw) == 0
+    assert bwd_varlen(**kw) == 0
+
+
+def test_varlen_workspace_size(lib):
+    # Delta: 4 heads x 700 tokens; 3 samples x 2 K/V heads x 3 tiles = 18 CTAs -> the group (2) is split
+    assert fa.fa_bwd_varlen_workspace_size(3, 300, 700, 4, 2, 64) == 11264 + 2 * 700 * 2 * 128 * 4
+    assert fa.fa_bwd_varlen_workspace_size(3, 300, 700, 4, 4, 64) == 11264
+    assert fa.fa_bwd_varlen_workspace_size(3, 300, 700, 4, 3, 64) == 0
+
+
 def test_binding_has_no_fallback(monkeypatch):
     """Without the compiled library the binding raises instead of computing anything."""
     import importlib
