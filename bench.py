@@ -43,7 +43,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "attention fwd/bwd TFLOPS and % of GB300 FP16 tensor peak (B4 H16 S4096 D64 causal)"
 WORKLOAD = "c2"
-WORKLOADS = ("c2", "gqa", "mqa", "varlen")
+WORKLOADS = ("c2", "gqa", "mqa", "varlen", "window")
 FLUSH_BYTES = 256 << 20  # > 129 MB L2
 KERNEL_SOURCES = ["exact_attention_18_gb300/csrc/fa_fwd.cu", "exact_attention_18_gb300/csrc/fa_fwd4.cu",
                   "exact_attention_18_gb300/csrc/fa_bwd.cu", "exact_attention_18_gb300/csrc/fa_softmax.cuh",
@@ -67,12 +67,32 @@ def sq_rows(w):
     return float(sum(n * n for _, _, n in head_list(w)))
 
 
+def band_pairs(n, causal, window):
+    """Exact count of visible (query, key) pairs of one head of n rows under a window band."""
+    left, right = window
+    total = 0
+    for i in range(n):
+        lo = 0 if left < 0 else max(0, i - left)
+        hi = i if causal else (n - 1 if right < 0 else min(n - 1, i + right))
+        if causal and right >= 0:
+            hi = min(hi, i + right)
+        total += max(0, hi - lo + 1)
+    return total
+
+
+def pairs(w):
+    """Score pairs the FLOP convention counts: S^2 per head (halved when causal), or, with
+    a window band, the exact number of visible pairs."""
+    if getattr(w, "window", None) is not None:
+        return float(sum(band_pairs(n, w.causal, w.window) for _, _, n in head_list(w)))
+    return sq_rows(w) / (2.0 if w.causal else 1.0)
+
+
 def conv_flops(w):
-    """FLOP convention: forward 4*S^2*D per head (halved when causal), summed over heads
-    (B*H*S^2 fixed length, H * sum of squared sample lengths packed); backward 2.5x forward."""
-    f = 4.0 * sq_rows(w) * w.D
-    if w.causal:
-        f /= 2
+    """FLOP convention: forward 4*S^2*D per head (halved when causal; with a window band,
+    4*D per visible pair), summed over heads (B*H*S^2 fixed length, H * sum of squared
+    sample lengths packed); backward 2.5x forward."""
+    f = 4.0 * pairs(w) * w.D
     return f, 2.5 * f
 
 
@@ -83,7 +103,7 @@ def fwd_kernel_name(w):
 
 def kernel_work(w):
     """Algorithmic work per launch of each kernel (FLOPs of its tensor-core GEMMs, or HBM bytes)."""
-    units = sq_rows(w) * w.D / (2.0 if w.causal else 1.0)
+    units = pairs(w) * w.D
     rows = sum(n for _, _, n in head_list(w))
     return {
         fwd_kernel_name(w): ("tensor", 4.0 * units),        # S = QK^T, O += PV
@@ -194,13 +214,17 @@ def cpu_oracle_step(inp, w, heads):
             a, e = cu[b], cu[b + 1]
             q, do = inp["q"][a:e, h], inp["do"][a:e, h]
             k, v = inp["k"][a:e, h // grp], inp["v"][a:e, h // grp]
-        oracle.forward(q, k, v, w.causal, w.scale)
-        oracle.backward(q, k, v, do, w.causal, w.scale)
+        win = getattr(w, "window", None)
+        oracle.forward(q, k, v, w.causal, w.scale, window=win)
+        oracle.backward(q, k, v, do, w.causal, w.scale, window=win)
 
 
 def head_flops(w, heads):
     """Convention FLOPs (forward + backward) of the listed heads."""
-    f = 4.0 * w.D * sum(n * n for _, _, n in heads) * (0.5 if w.causal else 1.0)
+    if getattr(w, "window", None) is not None:
+        f = 4.0 * w.D * sum(band_pairs(n, w.causal, w.window) for _, _, n in heads)
+    else:
+        f = 4.0 * w.D * sum(n * n for _, _, n in heads) * (0.5 if w.causal else 1.0)
     return 3.5 * f
 
 
@@ -226,7 +250,10 @@ def workload_config(w):
     if is_packed(w):
         return {"workload": w.name, "samples": w.batch, "lengths": list(w.lengths), "total_tokens": w.total,
                 "max_seqlen": w.max_seqlen, "H": w.H, "H_kv": w.kv_heads, "D": w.D, "causal": w.causal}
-    return {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.kv_heads, "S": w.S, "D": w.D, "causal": w.causal}
+    cfg = {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.kv_heads, "S": w.S, "D": w.D, "causal": w.causal}
+    if w.window is not None:
+        cfg["window"] = list(w.window)
+    return cfg
 
 
 def run_reference(args, w):
@@ -325,7 +352,12 @@ def main():
     sp = stream.cuda_stream
     dt_code = fa.FA_FP16 if w.dtype == "fp16" else fa.FA_BF16
 
+    win = None if packed else w.window
+
     def fwd_call(q_, k_, v_, o_, lse_, cu_=None):
+        if win is not None:
+            return fa.fa_fwd_window(q_, k_, v_, o_, lse_, B, H, Hkv, S, D, w.causal, win[0], win[1], w.scale, dt_code,
+                                    sp)
         if packed:
             return fa.fa_fwd_varlen(q_, k_, v_, o_, lse_, cu_ or cu.data_ptr(), nb, ms, T, H, Hkv, D, w.causal, w.scale,
                                     dt_code, sp)
@@ -334,6 +366,9 @@ def main():
         return fa.fa_fwd_gqa(q_, k_, v_, o_, lse_, B, H, Hkv, S, D, w.causal, w.scale, dt_code, sp)
 
     def bwd_call(q_, k_, v_, o_, do_, lse_, dq_, dk_, dv_, marks, cu_=None):
+        if win is not None:
+            return fa.fa_bwd_window_marked(q_, k_, v_, o_, do_, lse_, dq_, dk_, dv_, B, H, Hkv, S, D, w.causal, win[0],
+                                           win[1], w.scale, dt_code, ws.data_ptr(), ws_bytes, sp, marks)
         if packed:
             return fa.fa_bwd_varlen_marked(q_, k_, v_, o_, do_, lse_, dq_, dk_, dv_, cu_ or cu.data_ptr(), nb, ms, T, H, Hkv,
                                            D, w.causal, w.scale, dt_code, ws.data_ptr(), ws_bytes, sp, marks)
@@ -512,10 +547,11 @@ def main():
                            seq_len=w.max_seqlen if packed else w.S,
                            parallelism=f"independent x{world}",
                            step=("fa_fwd_varlen + fa_bwd_varlen" if packed else
+                                 "fa_fwd_window + fa_bwd_window" if win is not None else
                                  "fa_fwd + fa_bwd" if w.kv_heads == w.H else "fa_fwd_gqa + fa_bwd_gqa"),
                            l2="flushed between timed steps (256 MiB write)",
-                           flop_convention=("fwd 4*S^2*D per head (/2 causal; S the sample length when packed), "
-                                            "bwd 2.5x fwd")),
+                           flop_convention=("fwd 4*S^2*D per head (/2 causal; S the sample length when packed; "
+                                            "4*D per visible pair with a window band), bwd 2.5x fwd")),
             "fwd": {"ms": fwd_ms, "TFLOP/s": f_fwd / (fwd_ms * 1e-3) / 1e12,
                     "frac_of_tensor_peak": f_fwd / (fwd_ms * 1e-3) / 1e12 / peaks["tensor_tflops"]},
             "bwd": {"ms": bwd_ms, "TFLOP/s": f_bwd / (bwd_ms * 1e-3) / 1e12,

@@ -6,12 +6,14 @@ the library's CUDA kernels.  PyTorch supplies device memory and streams.
 The raw entry points keep the C names and signatures (pointers as ints):
 ``fa_fwd``, ``fa_fwd_gqa``, ``fa_bwd``, ``fa_bwd_marked``, ``fa_bwd_gqa``,
 ``fa_bwd_gqa_marked``, ``fa_bwd_noalloc``, ``fa_bwd_workspace_size``, ``fa_bwd_gqa_workspace_size``,
+``fa_fwd_window``, ``fa_bwd_window``, ``fa_bwd_window_marked``,
 ``fa_fwd_varlen``, ``fa_bwd_varlen``, ``fa_bwd_varlen_marked``,
 ``fa_bwd_varlen_workspace_size``, ``fa_status_string``, ``fa_last_error_detail``,
 ``fa_check_device_errors``.  ``forward`` and ``backward`` wrap them for
 contiguous [B, H, S, D] CUDA tensors; K and V (and dK, dV) may have fewer heads
 H_kv dividing H (grouped-query and multi-query attention), in which case they
-call the ``_gqa`` entry points.  ``forward_varlen`` and ``backward_varlen`` do
+call the ``_gqa`` entry points; ``window=(left, right)`` selects the
+sliding-window entry points.  ``forward_varlen`` and ``backward_varlen`` do
 the same for packed batches: [T, H, D] tensors and int32 ``cu_seqlens``.
 
 The first call loads the compiled library and raises if it has not been built
@@ -28,7 +30,8 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "lib
 
 __all__ = ["fa_fwd", "fa_fwd_gqa", "fa_bwd", "fa_bwd_marked", "fa_bwd_gqa", "fa_bwd_gqa_marked", "fa_bwd_noalloc",
            "fa_bwd_workspace_size", "fa_bwd_gqa_workspace_size", "fa_fwd_varlen", "fa_bwd_varlen",
-           "fa_bwd_varlen_marked", "fa_bwd_varlen_workspace_size", "forward_varlen", "backward_varlen", "fa_status_string", "fa_last_error_detail",
+           "fa_bwd_varlen_marked", "fa_bwd_varlen_workspace_size", "forward_varlen", "backward_varlen",
+           "fa_fwd_window", "fa_bwd_window", "fa_bwd_window_marked", "fa_status_string", "fa_last_error_detail",
            "fa_check_device_errors", "forward", "backward", "FAError", "FA_FP16", "FA_BF16", "STATUS",
            "library_path", "load_library"]
 
@@ -76,6 +79,13 @@ def _load():
     lib.fa_bwd_varlen.argtypes = [vp] * 10 + [i64] * 6 + [i32, f32, i32, vp, sz, vp]
     lib.fa_bwd_varlen_marked.restype = i32
     lib.fa_bwd_varlen_marked.argtypes = [vp] * 10 + [i64] * 6 + [i32, f32, i32, vp, sz, vp, ctypes.POINTER(vp)]
+    lib.fa_fwd_window.restype = i32
+    lib.fa_fwd_window.argtypes = [vp] * 5 + [i64] * 5 + [i32, i64, i64, f32, i32, vp]
+    lib.fa_bwd_window.restype = i32
+    lib.fa_bwd_window.argtypes = [vp] * 9 + [i64] * 5 + [i32, i64, i64, f32, i32, vp, sz, vp]
+    lib.fa_bwd_window_marked.restype = i32
+    lib.fa_bwd_window_marked.argtypes = [vp] * 9 + [i64] * 5 + [i32, i64, i64, f32, i32, vp, sz, vp,
+                                                                ctypes.POINTER(vp)]
     lib.fa_bwd_noalloc.restype = i32
     lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i32, f32, i32, vp]
     lib.fa_status_string.restype = ctypes.c_char_p
@@ -134,6 +144,28 @@ def fa_bwd_gqa_marked(q, k, v, o, dout, lse, dq, dk, dv, B, H, H_kv, S, D, causa
         arr = (ctypes.c_void_p * 4)(*[m if m else None for m in marks])
     return _load().fa_bwd_gqa_marked(q, k, v, o, dout, lse, dq, dk, dv, B, H, H_kv, S, D, int(causal),
                                      float(scale), int(dtype), workspace, workspace_bytes, stream, arr)
+
+
+def fa_fwd_window(q, k, v, o, lse, B, H, H_kv, S, D, causal, window_left, window_right, scale, dtype,
+                  stream) -> int:
+    return _load().fa_fwd_window(q, k, v, o, lse, B, H, H_kv, S, D, int(causal), int(window_left),
+                                 int(window_right), float(scale), int(dtype), stream)
+
+
+def fa_bwd_window(q, k, v, o, dout, lse, dq, dk, dv, B, H, H_kv, S, D, causal, window_left, window_right, scale,
+                  dtype, workspace, workspace_bytes, stream) -> int:
+    return _load().fa_bwd_window(q, k, v, o, dout, lse, dq, dk, dv, B, H, H_kv, S, D, int(causal), int(window_left),
+                                 int(window_right), float(scale), int(dtype), workspace, workspace_bytes, stream)
+
+
+def fa_bwd_window_marked(q, k, v, o, dout, lse, dq, dk, dv, B, H, H_kv, S, D, causal, window_left, window_right,
+                         scale, dtype, workspace, workspace_bytes, stream, marks) -> int:
+    arr = None
+    if marks is not None:
+        arr = (ctypes.c_void_p * 4)(*[m if m else None for m in marks])
+    return _load().fa_bwd_window_marked(q, k, v, o, dout, lse, dq, dk, dv, B, H, H_kv, S, D, int(causal),
+                                        int(window_left), int(window_right), float(scale), int(dtype), workspace,
+                                        workspace_bytes, stream, arr)
 
 
 def fa_fwd_varlen(q, k, v, o, lse, cu_seqlens, batch, max_seqlen, total, H, H_kv, D, causal, scale, dtype,
@@ -233,11 +265,14 @@ def _kv_heads(q, k, v):
     return hk
 
 
-def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None, stream=None):
+def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None, stream=None,
+            window=None):
     """O and fp32 natural-log LSE of exact attention; tensors [B, H, S, D] (or [B, S, D]).
 
     K and V may have H_kv heads with H a multiple of H_kv (grouped-query
-    attention; query head h reads K/V head h // (H // H_kv)).
+    attention; query head h reads K/V head h // (H // H_kv)).  ``window =
+    (left, right)`` restricts query i to keys i - left .. i + right (negative =
+    unlimited).
     """
     import torch
     squeeze = q.dim() == 3
@@ -248,7 +283,11 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
         scale = 1.0 / math.sqrt(D)
     o = torch.empty_like(q) if out is None else out.view(q.shape)
     l = torch.empty((B, H, S), dtype=torch.float32, device=q.device) if lse is None else lse.view(B, H, S)
-    if hk == H:
+    if window is not None:
+        _check(fa_fwd_window(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), l.data_ptr(), B, H, hk, S, D,
+                             causal, window[0], window[1], scale, _dtype_code(q), _stream_ptr(stream)),
+               "fa_fwd_window")
+    elif hk == H:
         _check(fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), l.data_ptr(), B, H, S, D, causal,
                       scale, _dtype_code(q), _stream_ptr(stream)), "fa_fwd")
     else:
@@ -260,7 +299,7 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
 
 
 def backward(q, k, v, o, do, lse, causal: bool = False, scale: float | None = None, dq=None, dk=None, dv=None,
-             workspace=None, stream=None):
+             workspace=None, stream=None, window=None):
     """dQ, dK, dV of exact attention from the forward's O and LSE (recompute backward).
 
     With K, V of H_kv < H heads, dK and dV have H_kv heads and sum over each
@@ -285,7 +324,10 @@ def backward(q, k, v, o, do, lse, causal: bool = False, scale: float | None = No
     args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
             dq.data_ptr(), dk.data_ptr(), dv.data_ptr())
     ws = (workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_ptr(stream))
-    if hk == H:
+    if window is not None:
+        _check(fa_bwd_window(*args, B, H, hk, S, D, causal, window[0], window[1], scale, _dtype_code(q), *ws),
+               "fa_bwd_window")
+    elif hk == H:
         _check(fa_bwd(*args, B, H, S, D, causal, scale, _dtype_code(q), *ws), "fa_bwd")
     else:
         _check(fa_bwd_gqa(*args, B, H, hk, S, D, causal, scale, _dtype_code(q), *ws), "fa_bwd_gqa")

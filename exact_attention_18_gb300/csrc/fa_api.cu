@@ -169,7 +169,19 @@ struct Shape {
   const int32_t* cu;
   int64_t total;
   bool is_packed;
+  int64_t win_left = -1, win_right = -1;  // window band; negative = unlimited
   bool packed() const { return is_packed; }
+  // Kernel window sides (fa::kNoWindow = unlimited; causal fixes the right side at 0).
+  int kernel_left() const { return win_left < 0 || win_left >= S ? fa::kNoWindow : static_cast<int>(win_left); }
+  int kernel_right(bool causal) const {
+    if (causal) return 0;
+    return win_right < 0 || win_right >= S ? fa::kNoWindow : static_cast<int>(win_right);
+  }
+  // The general kernels serve packed batches and windows that cut the band;
+  // fixed-length full/causal calls take the specialised ones.
+  bool general(bool causal) const {
+    return is_packed || kernel_left() != fa::kNoWindow || (!causal && kernel_right(false) != fa::kNoWindow);
+  }
   int64_t q_rows() const { return packed() ? total * H : B * H * S; }      // rows of Q, O, dO, L, Delta
   int64_t kv_rows() const { return packed() ? total * H_kv : B * H_kv * S; }  // rows of K, V, dK, dV
   bool empty() const { return B * H == 0 || S == 0 || (packed() && total == 0); }
@@ -239,11 +251,14 @@ fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* 
   const int rows_per_cta = fa::fwd_rows_per_cta(static_cast<int>(sh.D));
   p.n_m_tiles = static_cast<int>((sh.S + rows_per_cta - 1) / rows_per_cta);  // CTAs per (b, h)
   p.causal = causal ? 1 : 0;
+  p.win_left = sh.kernel_left();
+  p.win_right = sh.kernel_right(causal != 0);
   p.group = static_cast<int>(sh.H / sh.H_kv);
   p.scale_log2 = scale * kLog2e;
   p.err = fa::device_error_word();
   if (!p.err) return fail(FA_ERR_CUDA, "cannot resolve the device error word on the current device");
-  return from_cuda(fa::launch_fwd(static_cast<int>(sh.D), bf16, tq, tk, tv, p, static_cast<int>(sh.B * sh.H),
+  return from_cuda(fa::launch_fwd(static_cast<int>(sh.D), bf16, sh.general(causal != 0), tq, tk, tv, p,
+                                  static_cast<int>(sh.B * sh.H),
                                   static_cast<cudaStream_t>(stream)),
                    "forward launch");
 }
@@ -313,6 +328,8 @@ fa_status bwd_impl(const void* q, const void* k, const void* v, const void* o, c
   p.dkv_part = splits > 1 ? reinterpret_cast<float*>(static_cast<char*>(workspace) + delta_bytes) : nullptr;
   p.n_tiles = static_cast<int>((sh.S + 127) / 128);
   p.causal = causal ? 1 : 0;
+  p.win_left = sh.kernel_left();
+  p.win_right = sh.kernel_right(causal != 0);
   p.scale = scale;
   p.scale_log2 = scale * kLog2e;
   p.err = fa::device_error_word();
@@ -327,17 +344,25 @@ fa_status bwd_impl(const void* q, const void* k, const void* v, const void* o, c
   if ((st = mark(0))) return st;
   if ((st = from_cuda(fa::launch_bwd_preprocess(Di, bf16, p, q_rows, s), "backward preprocess launch"))) return st;
   if ((st = mark(1))) return st;
-  if ((st = from_cuda(fa::launch_bwd_dkdv(Di, bf16, maps, p, s), "backward dK/dV launch"))) return st;
+  const bool general = sh.general(causal != 0);
+  if ((st = from_cuda(fa::launch_bwd_dkdv(Di, bf16, general, maps, p, s), "backward dK/dV launch"))) return st;
   if (splits > 1 &&
       (st = from_cuda(fa::launch_bwd_dkv_reduce(Di, bf16, p, kv_rows, s), "backward dK/dV reduce launch")))
     return st;
   if ((st = mark(2))) return st;
-  if ((st = from_cuda(fa::launch_bwd_dq(Di, bf16, maps, p, s), "backward dQ launch"))) return st;
+  if ((st = from_cuda(fa::launch_bwd_dq(Di, bf16, general, maps, p, s), "backward dQ launch"))) return st;
   return mark(3);
 }
 
 Shape fixed(int64_t B, int64_t H, int64_t H_kv, int64_t S, int64_t D) {
   return Shape{B, H, H_kv, S, D, nullptr, 0, false};
+}
+
+Shape windowed(int64_t B, int64_t H, int64_t H_kv, int64_t S, int64_t D, int64_t left, int64_t right) {
+  Shape sh{B, H, H_kv, S, D, nullptr, 0, false};
+  sh.win_left = left;
+  sh.win_right = right;
+  return sh;
 }
 
 Shape packed(const int32_t* cu, int64_t batch, int64_t max_seqlen, int64_t total, int64_t H, int64_t H_kv,
@@ -357,6 +382,13 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
 fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
                      int64_t H_kv, int64_t S, int64_t D, int causal, float scale, fa_dtype dtype, void* stream) {
   return fwd_impl(q, k, v, o, lse, fixed(B, H, H_kv, S, D), causal, scale, dtype, stream);
+}
+
+fa_status fa_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
+                        int64_t H_kv, int64_t S, int64_t D, int causal, int64_t window_left, int64_t window_right,
+                        float scale, fa_dtype dtype, void* stream) {
+  return fwd_impl(q, k, v, o, lse, windowed(B, H, H_kv, S, D, window_left, window_right), causal, scale, dtype,
+                  stream);
 }
 
 fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -417,6 +449,23 @@ fa_status fa_bwd_gqa_marked(const void* q, const void* k, const void* v, const v
                             size_t workspace_bytes, void* stream, void* const* marks) {
   return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, fixed(B, H, H_kv, S, D), causal, scale, dtype, workspace,
                   workspace_bytes, stream, marks);
+}
+
+fa_status fa_bwd_window_marked(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                               const float* lse, void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t H_kv,
+                               int64_t S, int64_t D, int causal, int64_t window_left, int64_t window_right,
+                               float scale, fa_dtype dtype, void* workspace, size_t workspace_bytes, void* stream,
+                               void* const* marks) {
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, windowed(B, H, H_kv, S, D, window_left, window_right), causal,
+                  scale, dtype, workspace, workspace_bytes, stream, marks);
+}
+
+fa_status fa_bwd_window(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                        const float* lse, void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t H_kv,
+                        int64_t S, int64_t D, int causal, int64_t window_left, int64_t window_right, float scale,
+                        fa_dtype dtype, void* workspace, size_t workspace_bytes, void* stream) {
+  return fa_bwd_window_marked(q, k, v, o, dout, lse, dq, dk, dv, B, H, H_kv, S, D, causal, window_left,
+                              window_right, scale, dtype, workspace, workspace_bytes, stream, nullptr);
 }
 
 fa_status fa_bwd_varlen_marked(const void* q, const void* k, const void* v, const void* o, const void* dout,

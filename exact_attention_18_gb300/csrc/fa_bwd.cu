@@ -43,7 +43,8 @@
 namespace fa {
 using namespace ptx;
 
-// Source of L = +inf for partner query rows past a sample's end (dK/dV pass).
+// Source of L = +inf for partner query rows past a sample's end (dK/dV pass,
+// general instantiation).
 __device__ const float g_pos_inf = __builtin_huge_valf();
 
 // ------------------------------------------------------------------ preprocess
@@ -175,10 +176,11 @@ __device__ __forceinline__ uint32_t packed_col(int kk) { return kk < 2 ? kk * 8 
 // of X (P, dK/dV pass only) and Y (dS) already read.  In the dK/dV pass each
 // column is a partner query whose L and Delta come from lv, dv; in the dQ
 // pass they are the thread's own row's.  With DIAG the causal mask zeroes
-// partner column c where c < lim (dK/dV pass) or c > lim (dQ pass).
-template <bool BF16, bool KV_OUTER, bool DIAG>
+// partner column c where c < lim (dK/dV pass) or c > lim (dQ pass); with WIN
+// (a window band, dQ pass) also where c < lo.
+template <bool BF16, bool KV_OUTER, bool DIAG, bool WIN = false>
 __device__ __forceinline__ void grad_block(uint32_t tX, uint32_t tY, const float* lv, const float* dv, float2 c2,
-                                           float my_l2, float my_delta, int lim) {
+                                           float my_l2, float my_delta, int lim, int lo = 0) {
   constexpr float kLog2e = 1.4426950408889634f;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
@@ -199,8 +201,8 @@ __device__ __forceinline__ void grad_block(uint32_t tX, uint32_t tY, const float
       const float2 y = __ffma2_rn(make_float2(__uint_as_float(xs[c]), __uint_as_float(xs[c + 1])), c2, nl2);
       float2 pr = make_float2(ex2(y.x), ex2(y.y));
       if constexpr (DIAG) {
-        if (KV_OUTER ? cc < lim : cc > lim) pr.x = 0.f;
-        if (KV_OUTER ? cc + 1 < lim : cc + 1 > lim) pr.y = 0.f;
+        if ((KV_OUTER ? cc < lim : cc > lim) || (WIN && cc < lo)) pr.x = 0.f;
+        if ((KV_OUTER ? cc + 1 < lim : cc + 1 > lim) || (WIN && cc + 1 < lo)) pr.y = 0.f;
       }
       const float2 gr = __fadd2_rn(make_float2(__uint_as_float(ys[c]), __uint_as_float(ys[c + 1])),
                                    make_float2(-dl.x, -dl.y));
@@ -225,9 +227,11 @@ __device__ __forceinline__ void grad_block(uint32_t tX, uint32_t tY, const float
 // of such a column pair go back with 16x128b stores to packed column
 // (8i + 2(t%4)) / 2 = 4i + t%4, the layout the accumulation MMAs read.
 // lim0: key index of the warp's first row minus its first partner column.
-template <bool BF16, bool DIAG>
+// With WIN (a window band) the mask keeps, for key row j, the partner
+// queries j - wr .. j + wl: columns lim - wr .. lim + wl.
+template <bool BF16, bool DIAG, bool WIN = false>
 __device__ __forceinline__ void grad_block_kv(uint32_t tX, uint32_t tY, const float* lv, const float* dv, float2 c2,
-                                              int lim0) {
+                                              int lim0, int wr = 0, int wl = 0) {
   constexpr float kLog2e = 1.4426950408889634f;
   const int lane = threadIdx.x & 31;
   const int u = lane & 3;   // column pair within each group of 8
@@ -258,8 +262,13 @@ __device__ __forceinline__ void grad_block_kv(uint32_t tX, uint32_t tY, const fl
         if constexpr (DIAG) {
           const int lim = lim0 + 16 * half + r + 8 * k;  // zero partner columns c < lim (query before key)
           const int cc = 8 * i + 2 * u;
-          if (cc < lim) pr.x = 0.f;
-          if (cc + 1 < lim) pr.y = 0.f;
+          if constexpr (WIN) {
+            if (cc < lim - wr || cc > lim + wl) pr.x = 0.f;
+            if (cc + 1 < lim - wr || cc + 1 > lim + wl) pr.y = 0.f;
+          } else {
+            if (cc < lim) pr.x = 0.f;
+            if (cc + 1 < lim) pr.y = 0.f;
+          }
         }
         const float2 gr = __fadd2_rn(make_float2(__uint_as_float(ys[e]), __uint_as_float(ys[e + 1])), dl[i]);
         const float2 ds = __fmul2_rn(pr, gr);
@@ -274,7 +283,11 @@ __device__ __forceinline__ void grad_block_kv(uint32_t tX, uint32_t tY, const fl
 
 }  // namespace
 
-template <int D, bool BF16, bool KV_OUTER>
+// GENERAL = true is the instantiation for packed variable-length batches and
+// window bands (the layouts of BwdParams; "Inside FlashAttention" §6.1):
+// the CTA finds its sample from cu_seqlens, streams only the partner blocks
+// that meet its tile's band, and masks blocks crossing either band edge.
+template <int D, bool BF16, bool KV_OUTER, bool GENERAL>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_a1, const __grid_constant__ CUtensorMap tm_a2,
                        const __grid_constant__ CUtensorMap tm_b1, const __grid_constant__ CUtensorMap tm_b2,
@@ -310,35 +323,51 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int bh = KV_OUTER ? static_cast<int>(blockIdx.x) / p.kv_splits : static_cast<int>(blockIdx.x);
   const int kv_part = KV_OUTER ? static_cast<int>(blockIdx.x) - bh * p.kv_splits : 0;
   const int hpc = KV_OUTER ? p.group / p.kv_splits : 1;
-  // Rows of the sample (the two layouts of BwdParams).  Head indices below are
-  // global (b*H + h) in the fixed-length layout and within a token (h) when
+  // General instantiation: the sample of a packed batch.  Head indices are
+  // global (b*H + h) in the fixed-length layout and within a token when
   // packed: own_h for the CTA's own tiles, pz0 for the first partner head.
-  const bool packed = p.cu_seqlens != nullptr;
   const int heads_own = KV_OUTER ? p.heads / p.group : p.heads;  // per batch entry
-  int S = p.S;
-  int tok0 = 0;
-  int own_h = bh;
+  int S_ = p.S, tok0 = 0, own_h = bh;
   int pz0 = KV_OUTER ? bh * p.group + kv_part * hpc : bh / p.group;
-  if (packed) {
-    const int b = bh / heads_own;
-    if (!packed_sample(p.cu_seqlens, b, p.S, p.total, p.err, &tok0, &S)) return;
-    own_h = bh - b * heads_own;
-    pz0 = KV_OUTER ? own_h * p.group + kv_part * hpc : own_h / p.group;
+  bool packed = false;
+  if constexpr (GENERAL) {
+    packed = p.cu_seqlens != nullptr;
+    if (packed) {
+      const int b = bh / heads_own;
+      if (!packed_sample(p.cu_seqlens, b, p.S, p.total, p.err, &tok0, &S_)) return;
+      own_h = bh - b * heads_own;
+      pz0 = KV_OUTER ? own_h * p.group + kv_part * hpc : own_h / p.group;
+    }
   }
-  // Row r of head h: TMA coordinates (r, h) fixed, (h, tok0 + r) packed; its
-  // L and Delta at h * lstride + loff + r.
-  const int lstride = packed ? p.total : S;
-  const int loff = tok0;
+  const int S = S_;
   const int nt = p.n_tiles;
   const int np = (S + kPN - 1) / kPN;
+  const int64_t rowbase = static_cast<int64_t>(bh) * S;
+  // Row r of head h: L and Delta at h * lstride + loff + r (general instantiation).
+  const int lstride = (GENERAL && packed) ? p.total : S;
+  const int loff = tok0;
   // Own tile; heavy tiles first under the causal mask (key tile 0 and query
   // tile nt-1 see the most partners).
   const int own = KV_OUTER ? static_cast<int>(blockIdx.y)
                            : (p.causal ? nt - 1 - static_cast<int>(blockIdx.y) : static_cast<int>(blockIdx.y));
   const int own0 = own * 128;
-  if (own0 >= S) return;  // packed batch: this CTA lies past its sample
-  const int first = (KV_OUTER && p.causal) ? own0 / kPN : 0;
-  const int last_excl = (!KV_OUTER && p.causal) ? min(np, (own0 + 127) / kPN + 1) : np;
+  if constexpr (GENERAL) {
+    if (own0 >= S) return;  // packed batch: this CTA lies past its sample
+  }
+  // Window (general instantiation): key j is visible to query i iff i - wl <= j <= i + wr.
+  const int wl = GENERAL ? p.win_left : 0;
+  const int wr = GENERAL ? p.win_right : 0;
+  // Partner blocks [first, last_excl): queries j - wr .. j + wl of the tile's
+  // keys (dK/dV pass) or keys i - wl .. i + wr of its queries (dQ pass).
+  int first, last_excl;
+  if constexpr (GENERAL) {
+    const int below = KV_OUTER ? wr : wl, above = KV_OUTER ? wl : wr;
+    first = max(0, own0 - below) / kPN;
+    last_excl = min(np, min(S - 1, own0 + 127 + above) / kPN + 1);
+  } else {
+    first = (KV_OUTER && p.causal) ? own0 / kPN : 0;
+    last_excl = (!KV_OUTER && p.causal) ? min(np, (own0 + 127) / kPN + 1) : np;
+  }
   // Partner blocks per partner head; the dK/dV pass streams them for each of
   // the group's query heads in turn and sums over all of them.
   const int nper = last_excl - first;
@@ -392,9 +421,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
       for (int ch = 0; ch < GA::kChunks; ++ch) {
         tma_load_3d(smem + L::kOffA1 + ch * GA::kChunkBytes, &tm_a1, bar_afull, ch * (GA::kRowBytes / 2),
-                    packed ? own_h : own0, packed ? tok0 + own0 : own_h);
+                    (GENERAL && packed) ? own_h : own0, (GENERAL && packed) ? tok0 + own0 : own_h);
         tma_load_3d(smem + L::kOffA2 + ch * GA::kChunkBytes, &tm_a2, bar_afull, ch * (GA::kRowBytes / 2),
-                    packed ? own_h : own0, packed ? tok0 + own0 : own_h);
+                    (GENERAL && packed) ? own_h : own0, (GENERAL && packed) ? tok0 + own0 : own_h);
       }
     }
     int it = 0;
@@ -415,22 +444,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int ch = 0; ch < GB::kChunks; ++ch) {
           tma_load_3d(smem + L::kOffB1 + st * GB::kTileBytes + ch * GB::kChunkBytes, &tm_b1, &bar_bfull[st],
-                      ch * (GB::kRowBytes / 2), packed ? pz : r0, packed ? tok0 + r0 : pz);
+                      ch * (GB::kRowBytes / 2), (GENERAL && packed) ? pz : r0, (GENERAL && packed) ? tok0 + r0 : pz);
           tma_load_3d(smem + L::kOffB2 + st * GB::kTileBytes + ch * GB::kChunkBytes, &tm_b2, &bar_bfull[st],
-                      ch * (GB::kRowBytes / 2), packed ? pz : r0, packed ? tok0 + r0 : pz);
+                      ch * (GB::kRowBytes / 2), (GENERAL && packed) ? pz : r0, (GENERAL && packed) ? tok0 + r0 : pz);
         }
       }
       if constexpr (KV_OUTER) {
         float* v = vecs + st * 2 * kPN;
 #pragma unroll
         for (int h = 0; h < kPN; h += 32) {
-          // Partner queries past the sample read L = +inf and Delta = 0, so
-          // their P and dS are exactly 0 (when packed, their Q and dO rows
-          // are the next sample's).
           const int q = r0 + h + lane;
-          const int64_t src = static_cast<int64_t>(pz) * lstride + loff + (q < S ? q : S - 1);
-          cp_async_4(v + h + lane, q < S ? p.lse + src : &g_pos_inf, true);
-          cp_async_4(v + kPN + h + lane, p.delta + src, q < S);
+          if constexpr (GENERAL) {
+            // Partner queries past the sample read L = +inf and Delta = 0, so
+            // their P and dS are exactly 0 (when packed, their Q and dO rows
+            // are the next sample's).
+            const int64_t src = static_cast<int64_t>(pz) * lstride + loff + (q < S ? q : S - 1);
+            cp_async_4(v + h + lane, q < S ? p.lse + src : &g_pos_inf, true);
+            cp_async_4(v + kPN + h + lane, p.delta + src, q < S);
+          } else {
+            const int64_t src = static_cast<int64_t>(pz) * S + (q < S ? q : S - 1);
+            cp_async_4(v + h + lane, p.lse + src, q < S);
+            cp_async_4(v + kPN + h + lane, p.delta + src, q < S);
+          }
         }
         cp_async_mbar_arrive(&bar_bfull[st]);
       }
@@ -553,14 +588,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // (rows past S: L2 = +inf, so their probabilities are exactly 0).
     float my_l2 = INFINITY, my_delta = 0.f;
     if (!KV_OUTER && my < S) {
-      const int64_t li = static_cast<int64_t>(own_h) * lstride + loff + my;
+      const int64_t li = GENERAL ? static_cast<int64_t>(own_h) * lstride + loff + my : rowbase + my;
       my_l2 = p.lse[li] * kLog2e;
       my_delta = p.delta[li];
     }
-    // dQ pass: last visible key of this row (its own index under the causal
-    // mask), and whether a partner block can hold keys past the sample that
-    // must be masked (packed batch: those rows belong to the next sample).
-    const int last_key = p.causal ? min(my, S - 1) : S - 1;
     bool alive = true;
     int pi = g;  // i modulo nper: the partner block within its head (dK/dV pass)
     if constexpr (KV_OUTER) {
@@ -587,25 +618,46 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const float* dv = lv + kPN;                    // and their Delta
       // Diagonal blocks under the causal mask: the dK/dV pass zeroes partner
       // column c where query partner0 + col0 + c < key `my`, the dQ pass where
-      // key partner0 + col0 + c > its last visible key.  Partner queries past
-      // S have P = 0 from L = +inf; partner keys past S vanish through their
-      // zero-filled K rows, except when packed, where the dQ pass masks them.
-      const bool diag = (p.causal && (KV_OUTER ? partner0 < own0 + 128 : partner0 + kPN - 1 > own0)) ||
-                        (!KV_OUTER && packed && partner0 + kPN > S);
-      const int lim = last_key - partner0 - col0;
+      // key partner0 + col0 + c > query `my`.  Rows and columns past S need no
+      // mask: their zero-filled operands make their terms vanish (see above).
       // Off-diagonal blocks (all but one or two per tile) take the path with
       // no per-element compare or select.
-      if constexpr (KV_OUTER) {
-        const int lim0 = own0 + q4 * 32 - partner0 - col0;
-        if (diag)
-          grad_block_kv<BF16, true>(tX, tY, lv, dv, c2, lim0);
-        else
-          grad_block_kv<BF16, false>(tX, tY, lv, dv, c2, lim0);
+      if constexpr (GENERAL) {
+        // Window band: blocks crossing either edge are masked; the dQ pass
+        // also masks a packed sample's ragged last key block (those rows are
+        // the next sample's).  Partner queries past S have P = 0 from L = +inf.
+        if constexpr (KV_OUTER) {
+          const bool edge = partner0 < own0 + 127 - wr || partner0 + kPN - 1 > own0 + wl;
+          const int lim0 = own0 + q4 * 32 - partner0 - col0;
+          if (edge)
+            grad_block_kv<BF16, true, true>(tX, tY, lv, dv, c2, lim0, wr, wl);
+          else
+            grad_block_kv<BF16, false>(tX, tY, lv, dv, c2, lim0);
+        } else {
+          const bool edge = partner0 + kPN - 1 > own0 + wr || partner0 < own0 + 127 - wl ||
+                            (packed && partner0 + kPN > S);
+          const int hi = min(S - 1, my + wr) - partner0 - col0;
+          const int lo = my - wl - partner0 - col0;
+          if (edge)
+            grad_block<BF16, KV_OUTER, true, true>(tX, tY, lv, dv, c2, my_l2, my_delta, hi, lo);
+          else
+            grad_block<BF16, KV_OUTER, false>(tX, tY, lv, dv, c2, my_l2, my_delta, hi);
+        }
       } else {
-        if (diag)
-          grad_block<BF16, KV_OUTER, true>(tX, tY, lv, dv, c2, my_l2, my_delta, lim);
-        else
-          grad_block<BF16, KV_OUTER, false>(tX, tY, lv, dv, c2, my_l2, my_delta, lim);
+        const bool diag = p.causal && (KV_OUTER ? partner0 < own0 + 128 : partner0 + kPN - 1 > own0);
+        const int lim = my - partner0 - col0;
+        if constexpr (KV_OUTER) {
+          const int lim0 = own0 + q4 * 32 - partner0 - col0;
+          if (diag)
+            grad_block_kv<BF16, true>(tX, tY, lv, dv, c2, lim0);
+          else
+            grad_block_kv<BF16, false>(tX, tY, lv, dv, c2, lim0);
+        } else {
+          if (diag)
+            grad_block<BF16, KV_OUTER, true>(tX, tY, lv, dv, c2, my_l2, my_delta, lim);
+          else
+            grad_block<BF16, KV_OUTER, false>(tX, tY, lv, dv, c2, my_l2, my_delta, lim);
+        }
       }
       tmem_st_wait();
       tc_fence_before();
@@ -623,11 +675,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_after();
       const int c_begin = col_part * kEpiCols;
       const bool row_ok = my < S;
-      // Output row of (own head, row my): own_h * S + my fixed length,
-      // (tok0 + my) * heads_own + own_h packed.
+      // Output row: bh*S + my (fixed length) or (tok0 + my)*heads_own + own_h (packed).
       const int mr = row_ok ? my : 0;
-      const int64_t orow = packed ? static_cast<int64_t>(tok0 + mr) * heads_own + own_h
-                                  : static_cast<int64_t>(own_h) * S + mr;
+      const int64_t orow = (GENERAL && packed) ? static_cast<int64_t>(tok0 + mr) * heads_own + own_h : rowbase + mr;
       const size_t off = static_cast<size_t>(orow) * D;
       const uint32_t t_acc = tmem + lane_base;
       if constexpr (KV_OUTER) {
@@ -645,8 +695,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         } else {
           // This CTA's share of the group: fp32 rows [dV | scale * dK] of
           // partial `kv_part`, summed by the reduce kernel.
-          const int64_t n_rows = packed ? static_cast<int64_t>(p.total) * heads_own
-                                        : static_cast<int64_t>(p.BH / p.group) * S;
+          const int64_t n_rows = (GENERAL && packed) ? static_cast<int64_t>(p.total) * heads_own
+                                                     : static_cast<int64_t>(p.BH / p.group) * S;
           float* prow = p.dkv_part + ((static_cast<int64_t>(kv_part) * n_rows + orow) * (2 * D));
 #pragma unroll
           for (int c = c_begin; c < c_begin + kEpiCols; c += 16) {
@@ -688,11 +738,11 @@ cudaError_t launch_pre_t(const BwdParams& p, int64_t rows, cudaStream_t stream) 
   return cudaGetLastError();
 }
 
-template <int D, bool BF16, bool KV_OUTER>
+template <int D, bool BF16, bool KV_OUTER, bool GENERAL>
 cudaError_t launch_main_t(const CUtensorMap& a1, const CUtensorMap& a2, const CUtensorMap& b1,
                           const CUtensorMap& b2, const BwdParams& p, cudaStream_t stream) {
   using L = BwdLayout<D>;
-  auto kern = fa_bwd_main_kernel<D, BF16, KV_OUTER>;
+  auto kern = fa_bwd_main_kernel<D, BF16, KV_OUTER, GENERAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
   if (e != cudaSuccess) return e;
   // dK/dV pass: kv_splits CTAs per (K/V head, key tile); dQ pass: one per (query head, query tile).
@@ -735,8 +785,11 @@ cudaError_t launch_bwd_preprocess(int D, bool bf16, const BwdParams& p, int64_t 
 #undef FA_PRE
 }
 
-cudaError_t launch_bwd_dkdv(int D, bool bf16, const BwdMaps& m, const BwdParams& p, cudaStream_t stream) {
-#define FA_DKDV(DD, BB) launch_main_t<DD, BB, true>(m.k128, m.v128, m.q64, m.do64, p, stream)
+cudaError_t launch_bwd_dkdv(int D, bool bf16, bool general, const BwdMaps& m, const BwdParams& p,
+                            cudaStream_t stream) {
+#define FA_DKDV(DD, BB)                                                                      \
+  (general ? launch_main_t<DD, BB, true, true>(m.k128, m.v128, m.q64, m.do64, p, stream)     \
+           : launch_main_t<DD, BB, true, false>(m.k128, m.v128, m.q64, m.do64, p, stream))
   FA_BWD_DISPATCH(FA_DKDV)
 #undef FA_DKDV
 }
@@ -747,8 +800,11 @@ cudaError_t launch_bwd_dkv_reduce(int D, bool bf16, const BwdParams& p, int64_t 
 #undef FA_RED
 }
 
-cudaError_t launch_bwd_dq(int D, bool bf16, const BwdMaps& m, const BwdParams& p, cudaStream_t stream) {
-#define FA_DQ(DD, BB) launch_main_t<DD, BB, false>(m.q128, m.do128, m.k64, m.v64, p, stream)
+cudaError_t launch_bwd_dq(int D, bool bf16, bool general, const BwdMaps& m, const BwdParams& p,
+                          cudaStream_t stream) {
+#define FA_DQ(DD, BB)                                                                         \
+  (general ? launch_main_t<DD, BB, false, true>(m.q128, m.do128, m.k64, m.v64, p, stream)     \
+           : launch_main_t<DD, BB, false, false>(m.q128, m.do128, m.k64, m.v64, p, stream))
   FA_BWD_DISPATCH(FA_DQ)
 #undef FA_DQ
 }

@@ -86,20 +86,21 @@ struct FwdLayout : TileGeom<D> {
 };
 
 // P~ = exp2(c2 * s - m) for the block's 128 scores, packed as 16-bit pairs
-// into pk; with `masked`, columns past lim are exactly 0.  Returns the fp32
-// sum of the unrounded P~ (the block's share of the running sum l).
-template <bool BF16>
-__device__ __forceinline__ float exp_block(const uint32_t* sr, float2 c2, float m, bool masked, int lim,
+// into pk; with `masked`, columns past lim (and, with LO, before lo) are
+// exactly 0.  Returns the fp32 sum of the unrounded P~ (the block's share of
+// the running sum l).
+template <bool BF16, bool LO>
+__device__ __forceinline__ float exp_block(const uint32_t* sr, float2 c2, float m, bool masked, int lo, int lim,
                                            uint32_t* pk) {
   const float m_use = (m == -INFINITY) ? 0.f : m;  // rows with no visible key so far
   const float2 negm = make_float2(-m_use, -m_use);
   float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
   if (masked) {
 #pragma unroll
-    for (int k0 = 0; k0 < kBlockN; k0 += 16) exp16<BF16, true>(sr, k0, c2, negm, lim, acc, pk + k0 / 2);
+    for (int k0 = 0; k0 < kBlockN; k0 += 16) exp16<BF16, true, LO>(sr, k0, c2, negm, lo, lim, acc, pk + k0 / 2);
   } else {
 #pragma unroll
-    for (int k0 = 0; k0 < kBlockN; k0 += 16) exp16<BF16, false>(sr, k0, c2, negm, lim, acc, pk + k0 / 2);
+    for (int k0 = 0; k0 < kBlockN; k0 += 16) exp16<BF16, false>(sr, k0, c2, negm, lo, lim, acc, pk + k0 / 2);
   }
   const float2 a = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
   return a.x + a.y;
@@ -108,8 +109,9 @@ __device__ __forceinline__ float exp_block(const uint32_t* sr, float2 c2, float 
 }  // namespace
 
 // tm_q: 128-row boxes (a CTA's own query tiles); tm_k, tm_v: 64-row boxes
-// (each K/V block arrives as two half-block copies).
-template <int D, bool BF16>
+// (each K/V block arrives as two half-block copies).  GENERAL: packed
+// batches and windows, as in the four-tile kernel.
+template <int D, bool BF16, bool GENERAL>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -136,31 +138,57 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int bh = blockIdx.x;
-  // Where this head's rows live (the two layouts of FwdParams).  TMA
-  // coordinates of row r: (r, head) fixed length, (head, tok0 + r) packed.
-  const bool packed = p.cu_seqlens != nullptr;
-  int S = p.S;
-  int q_head = bh, kv_head = bh / p.group, tok0 = 0;  // K/V head shared by the query head's group
-  if (packed) {
-    const int b = bh / p.heads;
-    q_head = bh - b * p.heads;
-    kv_head = q_head / p.group;
-    if (!packed_sample(p.cu_seqlens, b, p.S, p.total, p.err, &tok0, &S)) return;
+  // General instantiation: the sample of a packed batch (the layouts of
+  // FwdParams); q_head / kvh are then heads within a token.
+  int S_ = p.S, kvh_ = bh / p.group, q_head = bh, tok0 = 0;
+  bool packed = false;
+  if constexpr (GENERAL) {
+    packed = p.cu_seqlens != nullptr;
+    if (packed) {
+      const int b = bh / p.heads;
+      q_head = bh - b * p.heads;
+      kvh_ = q_head / p.group;
+      if (!packed_sample(p.cu_seqlens, b, p.S, p.total, p.err, &tok0, &S_)) return;
+    }
   }
-  auto ty = [&](int r, int head) { return packed ? head : r; };
-  auto tz = [&](int r, int head) { return packed ? tok0 + r : head; };
+  const int kvh = kvh_;  // K/V head shared by this query head's group
+  const int S = S_;
   // Under the causal mask the heaviest CTAs are launched first.
   const int cta = p.causal ? p.n_m_tiles - 1 - static_cast<int>(blockIdx.y) : static_cast<int>(blockIdx.y);
   const int row0 = cta * 2 * kBlockM;
-  if (row0 >= S) return;  // packed batch: this CTA lies past its sample
+  if constexpr (GENERAL) {
+    if (row0 >= S) return;  // packed batch: this CTA lies past its sample
+  }
   const int n_kv = (S + kBlockN - 1) / kBlockN;
-  // Key blocks visited by the 128-row tile starting at row r (0 past S).
-  auto blocks_for = [&](int r) {
-    return r >= S ? 0 : (p.causal ? min(n_kv, (r + kBlockM + kBlockN - 1) / kBlockN) : n_kv);
+  // Window (general instantiation): key j is visible to query i iff i - wl <= j <= i + wr.
+  const int wl = GENERAL ? p.win_left : 0;
+  const int wr = GENERAL ? p.win_right : 0;
+  // Key blocks [first_blk(r), blocks_for(r)) of the 128-row tile starting at row r (empty past S).
+  auto first_blk = [&](int r) -> int {
+    if constexpr (GENERAL) return r >= S ? 0 : max(0, r - wl) / kBlockN;
+    else return 0;
   };
-  const int nb0 = blocks_for(row0);
-  const int nb1 = blocks_for(row0 + kBlockM);
-  const int nbp = max(nb0, nb1);  // blocks the CTA loads
+  auto blocks_for = [&](int r) -> int {
+    if constexpr (GENERAL) return r >= S ? 0 : min(n_kv, min(S - 1, r + kBlockM - 1 + wr) / kBlockN + 1);
+    else return r >= S ? 0 : (p.causal ? min(n_kv, (r + kBlockM + kBlockN - 1) / kBlockN) : n_kv);
+  };
+  const int kb_cta = first_blk(row0);  // the CTA loads key blocks kb_cta, kb_cta + 1, ...
+  // Tile t uses loaded blocks beg_t .. end_t - 1.
+  const int lo0 = first_blk(row0) - kb_cta, hi0 = blocks_for(row0) - kb_cta;
+  const int lo1 = first_blk(row0 + kBlockM) - kb_cta, hi1 = blocks_for(row0 + kBlockM) - kb_cta;
+  const int beg0 = hi0 > lo0 ? lo0 : 0, end0 = hi0 > lo0 ? hi0 : 0;
+  const int beg1 = hi1 > lo1 ? lo1 : 0, end1 = hi1 > lo1 ? hi1 : 0;
+  const int nb0 = end0 - beg0;
+  const int nb1 = end1 - beg1;
+  const int nbp = max(end0, end1);  // blocks the CTA loads
+  // TMA coordinates of `row` of `head` (x = column offset): (x, row, head) in
+  // the {D, S, heads} maps, (x, head, tok0 + row) in the packed {D, heads, T} maps.
+  auto tma_rows = [&](void* dst, const CUtensorMap* map, uint64_t* bar, int x, int row, int head) {
+    if (GENERAL && packed)
+      tma_load_3d(dst, map, bar, x, head, tok0 + row);
+    else
+      tma_load_3d(dst, map, bar, x, row, head);
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
@@ -207,8 +235,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int t = 0; t < 2; ++t)
 #pragma unroll
           for (int ch = 0; ch < L::kChunks; ++ch)
-            tma_load_3d(smem + L::kOffQ + t * L::kTileBytes + ch * L::kChunkBytes, &tm_q, bar_q,
-                        ch * (L::kRowBytes / 2), ty(row0 + t * kBlockM, q_head), tz(row0 + t * kBlockM, q_head));
+            tma_rows(smem + L::kOffQ + t * L::kTileBytes + ch * L::kChunkBytes, &tm_q, bar_q,
+                     ch * (L::kRowBytes / 2), row0 + t * kBlockM, q_head);
         // K and V blocks, each as two 64-row half-block copies.
         constexpr int kHalfBytes = (kBlockN / 2) * L::kRowBytes;
         int it = 0;
@@ -221,17 +249,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           for (int ch = 0; ch < L::kChunks; ++ch)
 #pragma unroll
             for (int h = 0; h < 2; ++h)
-              tma_load_3d(smem + L::kOffK + st * L::kTileBytes + ch * L::kChunkBytes + h * kHalfBytes, &tm_k,
-                          &bar_kfull[st], ch * (L::kRowBytes / 2), ty(it * kBlockN + h * (kBlockN / 2), kv_head),
-                          tz(it * kBlockN + h * (kBlockN / 2), kv_head));
+              tma_rows(smem + L::kOffK + st * L::kTileBytes + ch * L::kChunkBytes + h * kHalfBytes, &tm_k,
+                       &bar_kfull[st], ch * (L::kRowBytes / 2), (kb_cta + it) * kBlockN + h * (kBlockN / 2), kvh);
           mbar_arrive_expect_tx(&bar_vfull[st], L::kTileBytes);
 #pragma unroll
           for (int ch = 0; ch < L::kChunks; ++ch)
 #pragma unroll
             for (int h = 0; h < 2; ++h)
-              tma_load_3d(smem + L::kOffV + st * L::kTileBytes + ch * L::kChunkBytes + h * kHalfBytes, &tm_v,
-                          &bar_vfull[st], ch * (L::kRowBytes / 2), ty(it * kBlockN + h * (kBlockN / 2), kv_head),
-                          tz(it * kBlockN + h * (kBlockN / 2), kv_head));
+              tma_rows(smem + L::kOffV + st * L::kTileBytes + ch * L::kChunkBytes + h * kHalfBytes, &tm_v,
+                       &bar_vfull[st], ch * (L::kRowBytes / 2), (kb_cta + it) * kBlockN + h * (kBlockN / 2), kvh);
         }
         // Teardown: every copy this thread started must land before the CTA exits.
         drain_wait(bar_q, 0, p.err);
@@ -248,14 +274,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       // converged and one elected lane issues each MMA; descriptors are built
       // once per stage and advanced by compile-time offsets.
       const int t = warp - 9;
-      const int nbt = t == 0 ? nb0 : nb1;
+      const int beg = t == 0 ? beg0 : beg1;  // this tile's loaded blocks beg .. nbt - 1
+      const int nbt = t == 0 ? end0 : end1;
       constexpr uint32_t idesc_qk = make_idesc_f16(BF16, 128, kBlockN, false, false);
       constexpr uint32_t idesc_pv = make_idesc_f16(BF16, 128, D, false, true);
       const AccFlags acc = runtime_flags(S);
       const uint64_t q_desc = make_sdesc(sQ + t * L::kTileBytes, 16, 8 * L::kRowBytes, L::kSwz);
-      // S_t = Q_t K(j)^T; with separate P, first wait until the warpgroup has loaded S_t(j-1).
-      auto qk = [&](int j) -> bool {
-        if (L::kSepP && j > 0 && !warp_wait(&bar_sfree[t], (j - 1) & 1, abort_flag, p.err, kErrTimeoutMma))
+      // S_t = Q_t K(j)^T (the tile's block jl); with separate P, first wait
+      // until the warpgroup has loaded S_t(jl-1).
+      auto qk = [&](int j, int jl) -> bool {
+        if (L::kSepP && jl > 0 && !warp_wait(&bar_sfree[t], (jl - 1) & 1, abort_flag, p.err, kErrTimeoutMma))
           return false;
         tc_fence_after();
         const uint64_t k_desc =
@@ -267,10 +295,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         mma_commit_warp(&bar_sfull[t]);
         return true;
       };
-      // O_t += P_t(j) V(j) once P_t(j) is stored and O_t rescaled.
-      auto pv = [&](int j) -> bool {
+      // O_t += P_t(jl) V(j) once P_t(jl) is stored and O_t rescaled.
+      auto pv = [&](int j, int jl) -> bool {
         const int st = j % L::kStages;
-        if (!warp_wait(&bar_pfull[t], j & 1, abort_flag, p.err, kErrTimeoutMma)) return false;
+        if (!warp_wait(&bar_pfull[t], jl & 1, abort_flag, p.err, kErrTimeoutMma)) return false;
         if (!warp_wait(&bar_vfull[st], (j / L::kStages) & 1, abort_flag, p.err, kErrTimeoutMma)) return false;
         tc_fence_after();
         const uint64_t v_desc = make_sdesc(sV + st * L::kTileBytes, L::kChunkBytes, 8 * L::kRowBytes, L::kSwz);
@@ -278,7 +306,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < kBlockN / 16; ++kk)
           mma_ts_warp(tmem + L::kColO + D * t, t_p + kk * 8, desc_plus(v_desc, mnmajor_step_bytes<D>(kk)), idesc_pv,
-                      (j > 0 || kk > 0) ? acc.on : acc.off);
+                      (jl > 0 || kk > 0) ? acc.on : acc.off);
         if (L::kSepP) mma_commit_warp(&bar_pvdone[t]);
         if (j == nbt - 1) mma_commit_warp(&bar_ofinal[t]);
         return true;
@@ -296,16 +324,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         ok = warp_wait(&bar_kfull[j % L::kStages], (j / L::kStages) & 1, abort_flag, p.err, kErrTimeoutMma);
         if (!ok) break;
         tc_fence_after();
+        const bool q_in = j >= beg && j < nbt;              // S_t of loaded block j
+        const bool p_in = j >= 1 && j - 1 >= beg && j - 1 < nbt;  // P_t V of loaded block j - 1
         if (L::kSepP) {  // S_t(j) first, then O_t += P_t(j-1) V(j-1)
-          if (j < nbt && !(ok = qk(j))) break;
-          if (j >= 1 && j - 1 < nbt && !(ok = pv(j - 1))) break;
+          if (q_in && !(ok = qk(j, j - beg))) break;
+          if (p_in && !(ok = pv(j - 1, j - 1 - beg))) break;
         } else {  // P_t(j-1) lives in S_t: its P V must precede S_t(j)
-          if (j >= 1 && j - 1 < nbt && !(ok = pv(j - 1))) break;
-          if (j < nbt && !(ok = qk(j))) break;
+          if (p_in && !(ok = pv(j - 1, j - 1 - beg))) break;
+          if (q_in && !(ok = qk(j, j - beg))) break;
         }
         if (j >= 1 && !(ok = release(j - 1))) break;
       }
-      if (ok && nbp - 1 < nbt) ok = pv(nbp - 1);
+      if (ok && nbp - 1 >= beg && nbp - 1 < nbt) ok = pv(nbp - 1, nbp - 1 - beg);
       if (ok) release(nbp - 1);
       // Teardown: wait for every MMA this warp issued.
       mma_commit_warp(&bar_drain[t]);
@@ -321,6 +351,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const int row_g = tile_row0 + r;
     const int nb = t == 0 ? nb0 : nb1;
     const int nb_other = t == 0 ? nb1 : nb0;
+    const int kb0 = kb_cta + (t == 0 ? beg0 : beg1);  // the tile's first key block
     const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
     const uint32_t t_s = tmem + lane_base + L::kColS + 128u * t;
     const uint32_t t_p = tmem + lane_base + L::kColP + L::kStrideP * t;
@@ -328,7 +359,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const float sl2 = p.scale_log2;
     const float2 c2 = make_float2(sl2, sl2);
     const bool neg_scale = sl2 < 0.f;
-    const int last = p.causal ? min(S - 1, row_g) : S - 1;  // last visible key of this row
+    // Last (and, general instantiation, first) visible key of this row.
+    const int last = GENERAL ? min(S - 1, row_g + wr) : (p.causal ? min(S - 1, row_g) : S - 1);
+    const int first_key = row_g - wl;
     float m = -INFINITY;  // running (possibly stale) maximum, base-2 scaled
     float l = 0.f;
     bool alive = true;
@@ -341,12 +374,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tc_fence_after();
       tmem_ld128(t_s, sr);
       if (L::kSepP) warp_arrive(&bar_sfree[t]);  // S_t(j) is in registers: the MMA may overwrite it
-      const int kv0 = j * kBlockN;
-      const int lim = last - kv0;  // columns c <= lim are visible to this row
-      // Masked blocks: the diagonal block under the causal mask, and a ragged
-      // last key block.
-      const bool masked = (kv0 + kBlockN > S) || (p.causal && kv0 + kBlockN - 1 > tile_row0);
-      if (j == 0) m = block_max_scaled<kBlockN>(sr, masked, lim, sl2, neg_scale);
+      const int kv0 = (kb0 + j) * kBlockN;
+      const int lim = last - kv0;      // columns c <= lim are visible to this row
+      const int lo = first_key - kv0;  // and (general instantiation) c >= lo
+      // Masked blocks: the diagonal block under the causal mask (an edge of
+      // the window band), and a ragged last key block.
+      const bool masked = GENERAL ? (kv0 + kBlockN > S) || (kv0 + kBlockN - 1 > tile_row0 + wr) ||
+                                        (kv0 < tile_row0 + kBlockM - 1 - wl)
+                                  : (kv0 + kBlockN > S) || (p.causal && kv0 + kBlockN - 1 > tile_row0);
+      if (j == 0) m = block_max_scaled<kBlockN, GENERAL>(sr, masked, lo, lim, sl2, neg_scale);
       // The two tiles' warps of one sub-partition take turns at the
       // exponentials, so one's loads, stores and waits overlap the other's.
       if (kTurns && (t == 0 ? j >= 1 && j - 1 < nb_other : j < nb_other) &&
@@ -357,19 +393,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       uint32_t pk[kBlockN / 2];
       float alpha = 1.f;
       bool upd = false;
-      float blk = exp_block<BF16>(sr, c2, m, masked, lim, pk);
+      float blk = exp_block<BF16, GENERAL>(sr, c2, m, masked, lo, lim, pk);
       // Every P~ <= 2^8 holds if the block's sum does.  Otherwise (or on NaN)
       // this block's maximum is too far above the stale m: move m to it,
-      // rescale, and redo the block ("T5 讲解" §④ online update).
-      const bool need = !(blk <= kSumLimit);
+      // rescale, and redo the block ("T5 讲解" §④ online update).  A window can
+      // hide every key of a row's first blocks: the first block that shows the
+      // row a key then sets m.
+      bool need = !(blk <= kSumLimit);
+      if constexpr (GENERAL) need = need || (m == -INFINITY && max(lo, 0) <= min(lim, kBlockN - 1));
       if (__any_sync(0xffffffffu, need)) {
-        const float m_blk = block_max_scaled<kBlockN>(sr, masked, lim, sl2, neg_scale);
+        const float m_blk = block_max_scaled<kBlockN, GENERAL>(sr, masked, lo, lim, sl2, neg_scale);
         if (need && m_blk > m) {
           alpha = ex2(m - m_blk);
           m = m_blk;
           upd = true;
         }
-        if (__any_sync(0xffffffffu, upd)) blk = exp_block<BF16>(sr, c2, m, masked, lim, pk);
+        if (__any_sync(0xffffffffu, upd)) blk = exp_block<BF16, GENERAL>(sr, c2, m, masked, lo, lim, pk);
       }
       if (kTurns && (t == 0 ? j < nb_other : j + 1 < nb_other)) {
         __syncwarp();
@@ -410,11 +449,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tc_fence_after();
       const float inv_l = 1.f / l;
       const bool row_ok = row_g < S;
-      // Output row: bh*S + row fixed length, (tok0 + row)*H + head packed;
-      // L at bh*S + row, or head*T + tok0 + row.
+      // Output row bh*S + row (fixed length) or (tok0 + row)*H + head (packed);
+      // L at the same row, or at head*T + tok0 + row.
       const int rr = row_ok ? row_g : 0;
-      const size_t o_row = packed ? static_cast<size_t>(tok0 + rr) * p.heads + q_head : static_cast<size_t>(bh) * S + rr;
-      const size_t l_idx = packed ? static_cast<size_t>(q_head) * p.total + tok0 + rr : static_cast<size_t>(bh) * S + rr;
+      const size_t o_row = (GENERAL && packed) ? static_cast<size_t>(tok0 + rr) * p.heads + q_head
+                                               : static_cast<size_t>(bh) * S + rr;
+      const size_t l_idx = (GENERAL && packed) ? static_cast<size_t>(q_head) * p.total + tok0 + rr : o_row;
       elem_t* orow = reinterpret_cast<elem_t*>(p.o) + o_row * D;
 #pragma unroll
       for (int c = 0; c < D; c += 16) {
@@ -435,11 +475,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 }
 
 namespace {
-template <int D, bool BF16>
+template <int D, bool BF16, bool GENERAL>
 cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
                          int BH, cudaStream_t stream) {
   using L = FwdLayout<D>;
-  auto kern = fa_fwd_kernel<D, BF16>;
+  auto kern = fa_fwd_kernel<D, BF16, GENERAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
   if (e != cudaSuccess) return e;
   // The register split above assumes the launch gives exactly kLaunchRegs per
@@ -454,17 +494,20 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
 }
 }  // namespace
 
-cudaError_t launch_fwd(int D, bool bf16, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const FwdParams& p, int BH, cudaStream_t stream) {
-#define FA_FWD_CASE(DD)                                                  \
-  case DD:                                                               \
-    return bf16 ? launch_fwd_t<DD, true>(tq, tk, tv, p, BH, stream)      \
-                : launch_fwd_t<DD, false>(tq, tk, tv, p, BH, stream);
+cudaError_t launch_fwd(int D, bool bf16, bool general, const CUtensorMap& tq, const CUtensorMap& tk,
+                       const CUtensorMap& tv, const FwdParams& p, int BH, cudaStream_t stream) {
+#define FA_FWD_CASE(DD)                                                               \
+  case DD:                                                                            \
+    if (general)                                                                      \
+      return bf16 ? launch_fwd_t<DD, true, true>(tq, tk, tv, p, BH, stream)           \
+                  : launch_fwd_t<DD, false, true>(tq, tk, tv, p, BH, stream);         \
+    return bf16 ? launch_fwd_t<DD, true, false>(tq, tk, tv, p, BH, stream)            \
+                : launch_fwd_t<DD, false, false>(tq, tk, tv, p, BH, stream);
   switch (D) {
     case 16:
     case 32:
     case 64:
-      return launch_fwd4(D, bf16, tq, tk, tv, p, BH, stream);
+      return launch_fwd4(D, bf16, general, tq, tk, tv, p, BH, stream);
     FA_FWD_CASE(128)
     default:
       return cudaErrorInvalidValue;

@@ -37,6 +37,14 @@
 // Causal: tile t visits key blocks up to its diagonal ("T5 讲解" §⑤); the
 // element-wise mask runs only on the two blocks that cross the diagonal and
 // on a ragged last block ("fa-triton" §Causal Mask 的处理：off-band 与 on-band).
+//
+// GENERAL = true is the instantiation for packed variable-length batches and
+// sliding windows ("Inside FlashAttention" §6.1): the CTA finds its sample
+// from cu_seqlens, reads rows through {D, heads, T} tensor maps, and a tile
+// visits only the key blocks that meet its band [i - win_left, i + win_right];
+// blocks crossing either edge of the band are masked element-wise on both
+// sides.  GENERAL = false is the fixed-length full/causal kernel, kept free of
+// that bookkeeping.
 #include "fa_softmax.cuh"
 
 namespace fa {
@@ -91,7 +99,7 @@ struct F4Layout {
 }  // namespace
 
 // tm_q: 128-row boxes (the CTA's query tiles); tm_k, tm_v: 64-row boxes.
-template <int D, bool BF16>
+template <int D, bool BF16, bool GENERAL>
 __global__ void __launch_bounds__(kF4Threads, 1)
     fa_fwd4_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -118,31 +126,53 @@ __global__ void __launch_bounds__(kF4Threads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int bh = blockIdx.x;
-  // Where this head's rows live (the two layouts of FwdParams).  TMA
-  // coordinates of row r: (r, head) fixed length, (head, tok0 + r) packed.
-  const bool packed = p.cu_seqlens != nullptr;
-  int S = p.S;
-  int q_head = bh, kv_head = bh / p.group, tok0 = 0;  // K/V head shared by the query head's group
-  if (packed) {
-    const int b = bh / p.heads;
-    q_head = bh - b * p.heads;
-    kv_head = q_head / p.group;
-    if (!packed_sample(p.cu_seqlens, b, p.S, p.total, p.err, &tok0, &S)) return;
+  // General instantiation: the sample of a packed batch (the layouts of
+  // FwdParams); q_head / kvh are then heads within a token.
+  int S_ = p.S, kvh_ = bh / p.group, q_head = bh, tok0 = 0;
+  bool packed = false;
+  if constexpr (GENERAL) {
+    packed = p.cu_seqlens != nullptr;
+    if (packed) {
+      const int b = bh / p.heads;
+      q_head = bh - b * p.heads;
+      kvh_ = q_head / p.group;
+      if (!packed_sample(p.cu_seqlens, b, p.S, p.total, p.err, &tok0, &S_)) return;
+    }
   }
-  auto ty = [&](int r, int head) { return packed ? head : r; };
-  auto tz = [&](int r, int head) { return packed ? tok0 + r : head; };
+  const int kvh = kvh_;  // K/V head shared by this query head's group
+  const int S = S_;
   // Under the causal mask the heaviest CTAs are launched first.
   const int cta = p.causal ? p.n_m_tiles - 1 - static_cast<int>(blockIdx.y) : static_cast<int>(blockIdx.y);
   const int row0 = cta * kF4RowsPerCta;
-  if (row0 >= S) return;  // packed batch: this CTA lies past its sample
+  if constexpr (GENERAL) {
+    if (row0 >= S) return;  // packed batch: this CTA lies past its sample
+  }
   const int n_kv = (S + kBN - 1) / kBN;
-  // Key blocks visited by the 128-row tile starting at row r (0 past S).
-  auto blocks_for = [&](int r) {
-    return r >= S ? 0 : (p.causal ? min(n_kv, (r + kBlockM + kBN - 1) / kBN) : n_kv);
+  // Window (general instantiation): key j is visible to query i iff i - wl <= j <= i + wr.
+  const int wl = GENERAL ? p.win_left : 0;
+  const int wr = GENERAL ? p.win_right : 0;
+  // Key blocks [first_blk(r), blocks_for(r)) of the 128-row tile starting at
+  // row r (empty past S).
+  auto first_blk = [&](int r) -> int {
+    if constexpr (GENERAL) return r >= S ? 0 : max(0, r - wl) / kBN;
+    else return 0;
   };
-  int nbp = 0;  // blocks the CTA loads
+  auto blocks_for = [&](int r) -> int {
+    if constexpr (GENERAL) return r >= S ? 0 : min(n_kv, min(S - 1, r + kBlockM - 1 + wr) / kBN + 1);
+    else return r >= S ? 0 : (p.causal ? min(n_kv, (r + kBlockM + kBN - 1) / kBN) : n_kv);
+  };
+  const int kb_cta = first_blk(row0);  // the CTA loads key blocks kb_cta, kb_cta + 1, ...
+  int nbp = 0;                         // blocks the CTA loads
 #pragma unroll
-  for (int t = 0; t < kF4Tiles; ++t) nbp = max(nbp, blocks_for(row0 + t * kBlockM));
+  for (int t = 0; t < kF4Tiles; ++t) nbp = max(nbp, blocks_for(row0 + t * kBlockM) - kb_cta);
+  // TMA coordinates of `row` of `head`: (row, head) in the {D, S, heads}
+  // maps, (head, tok0 + row) in the packed {D, heads, T} maps.
+  auto tma_rows = [&](void* dst, const CUtensorMap* map, uint64_t* bar, int row, int head) {
+    if (GENERAL && packed)
+      tma_load_3d(dst, map, bar, 0, head, tok0 + row);
+    else
+      tma_load_3d(dst, map, bar, 0, row, head);
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
@@ -183,19 +213,16 @@ __global__ void __launch_bounds__(kF4Threads, 1)
         mbar_arrive_expect_tx(bar_q, kF4Tiles * GQ::kTileBytes);
 #pragma unroll
         for (int t = 0; t < kF4Tiles; ++t)
-          tma_load_3d(smem + L::kOffQ + t * GQ::kTileBytes, &tm_q, bar_q, 0, ty(row0 + t * kBlockM, q_head),
-                      tz(row0 + t * kBlockM, q_head));
+          tma_rows(smem + L::kOffQ + t * GQ::kTileBytes, &tm_q, bar_q, row0 + t * kBlockM, q_head);
         int it = 0;
         for (; it < nbp; ++it) {
           const int st = it % L::kStages;
           const int use = it / L::kStages;
           if (use > 0 && !mbar_wait(&bar_empty[st], (use - 1) & 1, abort_flag, p.err, kErrTimeoutLoad)) break;
           mbar_arrive_expect_tx(&bar_kfull[st], GK::kTileBytes);
-          tma_load_3d(smem + L::kOffK + st * GK::kTileBytes, &tm_k, &bar_kfull[st], 0, ty(it * kBN, kv_head),
-                      tz(it * kBN, kv_head));
+          tma_rows(smem + L::kOffK + st * GK::kTileBytes, &tm_k, &bar_kfull[st], (kb_cta + it) * kBN, kvh);
           mbar_arrive_expect_tx(&bar_vfull[st], GK::kTileBytes);
-          tma_load_3d(smem + L::kOffV + st * GK::kTileBytes, &tm_v, &bar_vfull[st], 0, ty(it * kBN, kv_head),
-                      tz(it * kBN, kv_head));
+          tma_rows(smem + L::kOffV + st * GK::kTileBytes, &tm_v, &bar_vfull[st], (kb_cta + it) * kBN, kvh);
         }
         // Teardown: every copy this thread started must land before the CTA exits.
         drain_wait(bar_q, 0, p.err);
@@ -210,11 +237,16 @@ __global__ void __launch_bounds__(kF4Threads, 1)
       // Warp kF4MmaWarp0 + w serves tiles w * kF4TilesPerMma, ... (a contiguous
       // pair).  Each runs converged and one elected lane issues every MMA.
       const int w = warp - kF4MmaWarp0;
-      int nbt[kF4TilesPerMma];
+      // Tile h of this warp uses loaded blocks beg[h] .. nbt[h]-1 (beg = 0
+      // unless a window starts the tile's band later).
+      int beg[kF4TilesPerMma], nbt[kF4TilesPerMma];
       int nbw = 0;
 #pragma unroll
       for (int h = 0; h < kF4TilesPerMma; ++h) {
-        nbt[h] = blocks_for(row0 + (w * kF4TilesPerMma + h) * kBlockM);
+        const int r = row0 + (w * kF4TilesPerMma + h) * kBlockM;
+        const int lo = first_blk(r) - kb_cta, hi = blocks_for(r) - kb_cta;
+        beg[h] = hi > lo ? lo : 0;
+        nbt[h] = hi > lo ? hi : 0;
         nbw = max(nbw, nbt[h]);
       }
       constexpr uint32_t idesc_qk = make_idesc_f16(BF16, 128, kBN, false, false);
@@ -229,14 +261,14 @@ __global__ void __launch_bounds__(kF4Threads, 1)
           mma_ss_warp(tmem + 128u * t, desc_plus(q_desc, kmajor_step_bytes<D, 128>(kk)),
                       desc_plus(k_desc, kmajor_step_bytes<D, kBN>(kk)), idesc_qk, kk > 0 ? acc.on : acc.off);
       };
-      // O_t += P_t(j) V(j), P from tile t's S columns.
-      auto pv = [&](int t, int j) {
+      // O_t += P_t(j) V(j), P from tile t's S columns; jl = the tile's own block count so far.
+      auto pv = [&](int t, int j, int jl) {
         const uint64_t v_desc =
             make_sdesc(sV + (j % L::kStages) * GK::kTileBytes, GK::kChunkBytes, 8 * GK::kRowBytes, GK::kSwz);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
           mma_ts_warp(tmem + 128u * t + L::kColO, tmem + 128u * t + kk * 8,
-                      desc_plus(v_desc, mnmajor_step_bytes<D>(kk)), idesc_pv, (j > 0 || kk > 0) ? acc.on : acc.off);
+                      desc_plus(v_desc, mnmajor_step_bytes<D>(kk)), idesc_pv, (jl > 0 || kk > 0) ? acc.on : acc.off);
       };
       bool ok = warp_wait(bar_q, 0, abort_flag, p.err, kErrTimeoutMma);
       if (ok && nbw > 0) ok = warp_wait(&bar_kfull[0], 0, abort_flag, p.err, kErrTimeoutMma);
@@ -244,7 +276,7 @@ __global__ void __launch_bounds__(kF4Threads, 1)
         tc_fence_after();
 #pragma unroll
         for (int h = 0; h < kF4TilesPerMma; ++h) {
-          if (nbt[h] == 0) continue;
+          if (nbt[h] == 0 || beg[h] != 0) continue;
           const int t = w * kF4TilesPerMma + h;
           qk(t, 0);
           mma_commit_warp(&bar_sfull[t]);
@@ -263,10 +295,21 @@ __global__ void __launch_bounds__(kF4Threads, 1)
           if (!ok) break;
           if (j >= nbt[h]) continue;
           const int t = w * kF4TilesPerMma + h;
-          ok = warp_wait(&bar_pfull[t], j & 1, abort_flag, p.err, kErrTimeoutMma);
+          if constexpr (GENERAL) {
+            if (j < beg[h]) {  // the tile's band starts later: its first scores once K(beg) is in
+              if (j + 1 == beg[h]) {
+                tc_fence_after();
+                qk(t, j + 1);
+                mma_commit_warp(&bar_sfull[t]);
+              }
+              continue;
+            }
+          }
+          const int jl = GENERAL ? j - beg[h] : j;
+          ok = warp_wait(&bar_pfull[t], jl & 1, abort_flag, p.err, kErrTimeoutMma);
           if (!ok) break;
           tc_fence_after();
-          pv(t, j);
+          pv(t, j, jl);
           if (j + 1 < nbt[h]) {
             qk(t, j + 1);
             mma_commit_warp(&bar_sfull[t]);
@@ -296,14 +339,17 @@ __global__ void __launch_bounds__(kF4Threads, 1)
     const int r = q4 * 32 + lane;
     const int tile_row0 = row0 + t * kBlockM;
     const int row_g = tile_row0 + r;
-    const int nb = blocks_for(tile_row0);
+    const int kb0 = first_blk(tile_row0);  // the tile's first key block
+    const int nb = max(0, blocks_for(tile_row0) - kb0);
     const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
     const uint32_t t_s = tmem + lane_base + 128u * t;  // S_t, and P_t over it
     const uint32_t t_o = t_s + L::kColO;
     const float sl2 = p.scale_log2;
     const float2 c2 = make_float2(sl2, sl2);
     const bool neg_scale = sl2 < 0.f;
-    const int last = p.causal ? min(S - 1, row_g) : S - 1;  // last visible key of this row
+    // Last (and, general instantiation, first) visible key of this row.
+    const int last = GENERAL ? min(S - 1, row_g + wr) : (p.causal ? min(S - 1, row_g) : S - 1);
+    const int first_key = row_g - wl;
     float m = -INFINITY;  // running (possibly stale) maximum, base-2 scaled
     float l = 0.f;
     bool alive = true;
@@ -315,12 +361,15 @@ __global__ void __launch_bounds__(kF4Threads, 1)
       tc_fence_after();
       uint32_t sr[kBN];
       tmem_ld64(t_s, sr);
-      const int kv0 = j * kBN;
-      const int lim = last - kv0;  // columns c <= lim are visible to this row
-      // Masked blocks: those crossing the diagonal under the causal mask, and
-      // a ragged last key block.
-      const bool masked = (kv0 + kBN > S) || (p.causal && kv0 + kBN - 1 > tile_row0);
-      if (j == 0) m = block_max_scaled<kBN>(sr, masked, lim, sl2, neg_scale);
+      const int kv0 = (kb0 + j) * kBN;
+      const int lim = last - kv0;      // columns c <= lim are visible to this row
+      const int lo = first_key - kv0;  // and (general instantiation) c >= lo
+      // Masked blocks: those crossing the diagonal under the causal mask (an
+      // edge of the window band), and a ragged last key block.
+      const bool masked =
+          GENERAL ? (kv0 + kBN > S) || (kv0 + kBN - 1 > tile_row0 + wr) || (kv0 < tile_row0 + kBlockM - 1 - wl)
+                  : (kv0 + kBN > S) || (p.causal && kv0 + kBN - 1 > tile_row0);
+      if (j == 0) m = block_max_scaled<kBN, GENERAL>(sr, masked, lo, lim, sl2, neg_scale);
       float alpha = 1.f;
       bool upd = false;
       float blk;
@@ -334,14 +383,14 @@ __global__ void __launch_bounds__(kF4Threads, 1)
 #pragma unroll
           for (int k0 = 0; k0 < kBN; k0 += 16) {
             uint32_t pk[8];
-            exp16<BF16, true>(sr, k0, c2, negm, lim, acc, pk);
+            exp16<BF16, true, GENERAL>(sr, k0, c2, negm, lo, lim, acc, pk);
             tmem_st8(t_s + k0 / 2, pk);
           }
         } else {
 #pragma unroll
           for (int k0 = 0; k0 < kBN; k0 += 16) {
             uint32_t pk[8];
-            exp16<BF16, false>(sr, k0, c2, negm, lim, acc, pk);
+            exp16<BF16, false>(sr, k0, c2, negm, lo, lim, acc, pk);
             tmem_st8(t_s + k0 / 2, pk);
           }
         }
@@ -352,9 +401,14 @@ __global__ void __launch_bounds__(kF4Threads, 1)
       // Every P~ <= 2^8 holds if the block's sum does.  Otherwise (or on NaN)
       // the stale m is too far below this block's maximum: move m, rescale,
       // and redo the block.
-      const bool need = !(blk <= kF4SumLimit);
+      bool need = !(blk <= kF4SumLimit);
+      if constexpr (GENERAL) {
+        // A window can hide every key of a row's first blocks: m is still
+        // -inf there, and the first block that shows the row a key sets it.
+        need = need || (m == -INFINITY && max(lo, 0) <= min(lim, kBN - 1));
+      }
       if (__any_sync(0xffffffffu, need)) {
-        const float m_blk = block_max_scaled<kBN>(sr, masked, lim, sl2, neg_scale);
+        const float m_blk = block_max_scaled<kBN, GENERAL>(sr, masked, lo, lim, sl2, neg_scale);
         if (need && m_blk > m) {
           alpha = ex2(m - m_blk);
           m = m_blk;
@@ -389,11 +443,12 @@ __global__ void __launch_bounds__(kF4Threads, 1)
       tc_fence_after();
       const float inv_l = 1.f / l;
       const bool row_ok = row_g < S;
-      // Output row: bh*S + row fixed length, (tok0 + row)*H + head packed;
-      // L at bh*S + row, or head*T + tok0 + row.
+      // Output row bh*S + row (fixed length) or (tok0 + row)*H + head (packed);
+      // L at the same row, or at head*T + tok0 + row.
       const int rr = row_ok ? row_g : 0;
-      const size_t o_row = packed ? static_cast<size_t>(tok0 + rr) * p.heads + q_head : static_cast<size_t>(bh) * S + rr;
-      const size_t l_idx = packed ? static_cast<size_t>(q_head) * p.total + tok0 + rr : static_cast<size_t>(bh) * S + rr;
+      const size_t o_row = (GENERAL && packed) ? static_cast<size_t>(tok0 + rr) * p.heads + q_head
+                                               : static_cast<size_t>(bh) * S + rr;
+      const size_t l_idx = (GENERAL && packed) ? static_cast<size_t>(q_head) * p.total + tok0 + rr : o_row;
       elem_t* orow = reinterpret_cast<elem_t*>(p.o) + o_row * D;
 #pragma unroll
       for (int c = 0; c < D; c += 16) {
@@ -414,11 +469,11 @@ __global__ void __launch_bounds__(kF4Threads, 1)
 }
 
 namespace {
-template <int D, bool BF16>
+template <int D, bool BF16, bool GENERAL>
 cudaError_t launch_fwd4_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
                           int BH, cudaStream_t stream) {
   using L = F4Layout<D>;
-  auto kern = fa_fwd4_kernel<D, BF16>;
+  auto kern = fa_fwd4_kernel<D, BF16, GENERAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
   if (e != cudaSuccess) return e;
   // The register split assumes the launch gives exactly kF4LaunchRegs per
@@ -435,12 +490,15 @@ cudaError_t launch_fwd4_t(const CUtensorMap& tq, const CUtensorMap& tk, const CU
 
 int fwd_rows_per_cta(int D) { return D <= 64 ? kF4RowsPerCta : 2 * kBlockM; }
 
-cudaError_t launch_fwd4(int D, bool bf16, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                        const FwdParams& p, int BH, cudaStream_t stream) {
-#define FA_FWD4_CASE(DD)                                                 \
-  case DD:                                                               \
-    return bf16 ? launch_fwd4_t<DD, true>(tq, tk, tv, p, BH, stream)     \
-                : launch_fwd4_t<DD, false>(tq, tk, tv, p, BH, stream);
+cudaError_t launch_fwd4(int D, bool bf16, bool general, const CUtensorMap& tq, const CUtensorMap& tk,
+                        const CUtensorMap& tv, const FwdParams& p, int BH, cudaStream_t stream) {
+#define FA_FWD4_CASE(DD)                                                                       \
+  case DD:                                                                                     \
+    if (general)                                                                               \
+      return bf16 ? launch_fwd4_t<DD, true, true>(tq, tk, tv, p, BH, stream)                   \
+                  : launch_fwd4_t<DD, false, true>(tq, tk, tv, p, BH, stream);                 \
+    return bf16 ? launch_fwd4_t<DD, true, false>(tq, tk, tv, p, BH, stream)                    \
+                : launch_fwd4_t<DD, false, false>(tq, tk, tv, p, BH, stream);
   switch (D) {
     FA_FWD4_CASE(16)
     FA_FWD4_CASE(32)

@@ -9,6 +9,7 @@ namespace fa {
 
 constexpr int kBlockM = 128;  // query rows per tile (= TMEM lanes)
 constexpr int kBlockN = 128;  // key rows per tile
+constexpr int kNoWindow = 1 << 30;  // an unlimited window side (larger than any sequence)
 
 // Two layouts.  Fixed length (cu_seqlens == nullptr): [B*H, S, D] tensors,
 // row r of head bh at element (bh*S + r)*D, L at bh*S + r, tensor maps
@@ -25,6 +26,8 @@ struct FwdParams {
   int total;           // packed batch: T tokens
   int n_m_tiles;       // CTAs per (b, h): ceil(S / fwd_rows_per_cta(D))
   int causal;          // nonzero: key j visible to query i iff j <= i
+  int win_left;        // general kernels: key j visible to query i iff i - win_left <= j <= i + win_right
+  int win_right;       // (kNoWindow = unlimited; causal sets win_right = 0)
   int group;           // query heads per K/V head: query head bh reads K/V head bh / group
   float scale_log2;    // scale * log2(e): scores enter exp2 in base 2
   int* err;            // device error word (set when a pipeline wait times out)
@@ -49,6 +52,8 @@ struct BwdParams {
                        // K/V rows in dK's own row order (B*H_kv*S, or T*H_kv packed)
   int n_tiles;         // ceil(S / 128): own tiles per (b, h)
   int causal;
+  int win_left;        // general kernels: window as in FwdParams
+  int win_right;
   float scale;         // softmax scale (dQ, dK factor)
   float scale_log2;    // scale * log2(e)
   int* err;            // device error word
@@ -65,18 +70,22 @@ struct BwdMaps {
 // Query rows one forward CTA covers for head dimension D.
 int fwd_rows_per_cta(int D);
 
-// Launchers (one per kernel family); they dispatch on D and dtype.
+// Launchers (one per kernel family); they dispatch on D and dtype, and take
+// the general instantiation (packed batches, windows) when `general` is set;
+// the fixed-length full/causal calls run the specialised one.
 // launch_fwd4: the four-tile forward for D <= 64; launch_fwd: any D (passes
 // D <= 64 on to launch_fwd4).
-cudaError_t launch_fwd4(int D, bool bf16, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                        const FwdParams& p, int BH, cudaStream_t stream);
-cudaError_t launch_fwd(int D, bool bf16, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const FwdParams& p, int BH, cudaStream_t stream);
+cudaError_t launch_fwd4(int D, bool bf16, bool general, const CUtensorMap& tq, const CUtensorMap& tk,
+                        const CUtensorMap& tv, const FwdParams& p, int BH, cudaStream_t stream);
+cudaError_t launch_fwd(int D, bool bf16, bool general, const CUtensorMap& tq, const CUtensorMap& tk,
+                       const CUtensorMap& tv, const FwdParams& p, int BH, cudaStream_t stream);
 
 // rows: query rows (B*H*S, or T*H packed).
 cudaError_t launch_bwd_preprocess(int D, bool bf16, const BwdParams& p, int64_t rows, cudaStream_t stream);
-cudaError_t launch_bwd_dkdv(int D, bool bf16, const BwdMaps& maps, const BwdParams& p, cudaStream_t stream);
-cudaError_t launch_bwd_dq(int D, bool bf16, const BwdMaps& maps, const BwdParams& p, cudaStream_t stream);
+cudaError_t launch_bwd_dkdv(int D, bool bf16, bool general, const BwdMaps& maps, const BwdParams& p,
+                            cudaStream_t stream);
+cudaError_t launch_bwd_dq(int D, bool bf16, bool general, const BwdMaps& maps, const BwdParams& p,
+                          cudaStream_t stream);
 // Sums the kv_splits partial dK/dV rows and writes dK, dV (only when kv_splits > 1);
 // rows: K/V rows (B*H_kv*S, or T*H_kv packed).
 cudaError_t launch_bwd_dkv_reduce(int D, bool bf16, const BwdParams& p, int64_t rows, cudaStream_t stream);

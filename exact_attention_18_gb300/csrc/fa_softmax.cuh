@@ -21,9 +21,11 @@ __device__ __forceinline__ float min3(float a, float b, float c) {
 
 // Scaled row maximum c * max_k s_k over the NC scores of a block (the minimum
 // raw score when c < 0, whose scaled value is then the largest); with
-// `masked`, only columns k <= lim count.  -inf if no column is visible.
-template <int NC>
-__device__ __forceinline__ float block_max_scaled(const uint32_t* sr, bool masked, int lim, float sl2, bool neg) {
+// `masked`, only columns k <= lim (and, with LO, k >= lo) count.  -inf if no
+// column is visible.
+template <int NC, bool LO = false>
+__device__ __forceinline__ float block_max_scaled(const uint32_t* sr, bool masked, int lo, int lim, float sl2,
+                                                  bool neg) {
   static_assert(NC % 16 == 0, "block width");
   float mx;
   if (!masked) {
@@ -49,28 +51,31 @@ __device__ __forceinline__ float block_max_scaled(const uint32_t* sr, bool maske
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
       const float x = __uint_as_float(sr[c]);
-      if (c <= lim) mx = neg ? fminf(mx, x) : fmaxf(mx, x);
+      if (c <= lim && (!LO || c >= lo)) mx = neg ? fminf(mx, x) : fmaxf(mx, x);
     }
+  }
+  if constexpr (LO) {
+    if (masked && (lo > NC - 1 || lim < lo)) return -INFINITY;
   }
   return lim < 0 ? -INFINITY : mx * sl2;
 }
 
 // P~_k = exp2(c * s_k - m) for scores k0 .. k0+15 of a block, packed as eight
 // 16-bit pairs into pk (key k0+2i in the low half of pk[i]); with MASKED,
-// columns past lim are exactly 0.  The unrounded P~ are added into acc.
-// MASKED is a template parameter so the unmasked blocks (all but the diagonal
-// and ragged ones) carry no per-element compare or select.
-template <bool BF16, bool MASKED>
-__device__ __forceinline__ void exp16(const uint32_t* sr, int k0, float2 c2, float2 negm, int lim, float2* acc,
-                                      uint32_t* pk) {
+// columns past lim (and, with LO, before lo) are exactly 0.  The unrounded P~
+// are added into acc.  MASKED is a template parameter so the unmasked blocks
+// (all but the diagonal and ragged ones) carry no per-element compare or select.
+template <bool BF16, bool MASKED, bool LO = false>
+__device__ __forceinline__ void exp16(const uint32_t* sr, int k0, float2 c2, float2 negm, int lo, int lim,
+                                      float2* acc, uint32_t* pk) {
 #pragma unroll
   for (int c = 0; c < 16; c += 2) {
     const float2 y =
         __ffma2_rn(make_float2(__uint_as_float(sr[k0 + c]), __uint_as_float(sr[k0 + c + 1])), c2, negm);
     float2 e = make_float2(ptx::ex2(y.x), ptx::ex2(y.y));
     if constexpr (MASKED) {
-      if (k0 + c > lim) e.x = 0.f;
-      if (k0 + c + 1 > lim) e.y = 0.f;
+      if (k0 + c > lim || (LO && k0 + c < lo)) e.x = 0.f;
+      if (k0 + c + 1 > lim || (LO && k0 + c + 1 < lo)) e.y = 0.f;
     }
     acc[(c / 2) & 3] = __fadd2_rn(acc[(c / 2) & 3], e);
     pk[c / 2] = pack2<BF16>(e.x, e.y);

@@ -171,6 +171,35 @@ fa_status fa_bwd_gqa_marked(const void* q, const void* k, const void* v, const v
                             size_t workspace_bytes, void* stream, void* const* marks);
 
 /*
+ * Sliding-window (local) attention ("Inside FlashAttention" §6.1, window_size
+ * = (left, right): only the key blocks inside the window are computed).  Key j
+ * is visible to query i only if i - window_left <= j <= i + window_right; a
+ * negative side is unlimited, and `causal` additionally hides j > i (so
+ * causal with (left, 0) is the usual local causal window).  Layouts, grouped
+ * heads (H_kv) and every other convention as fa_fwd_gqa / fa_bwd_gqa.  Each
+ * 128-row query tile (or 128-key tile in the backward) visits only the key
+ * (query) blocks that meet its band; blocks crossing either edge of the band
+ * are masked element-wise, the others run unmasked.  Every query row sees at
+ * least its own key, so no row is empty.  A window that covers the whole
+ * sequence runs the ordinary kernels.  Workspace: fa_bwd_gqa_workspace_size().
+ */
+fa_status fa_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
+                        int64_t H_kv, int64_t S, int64_t D, int causal, int64_t window_left, int64_t window_right,
+                        float scale, fa_dtype dtype, void* stream);
+
+fa_status fa_bwd_window(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                        const float* lse, void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t H_kv,
+                        int64_t S, int64_t D, int causal, int64_t window_left, int64_t window_right, float scale,
+                        fa_dtype dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/* fa_bwd_window with the timing marks of fa_bwd_marked. */
+fa_status fa_bwd_window_marked(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                               const float* lse, void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t H_kv,
+                               int64_t S, int64_t D, int causal, int64_t window_left, int64_t window_right,
+                               float scale, fa_dtype dtype, void* workspace, size_t workspace_bytes, void* stream,
+                               void* const* marks);
+
+/*
  * Packed variable-length batches ("Inside FlashAttention" §6.1, varlen: samples
  * of different lengths concatenated with no padding, a prefix-sum array
  * cu_seqlens marking their bounds, and no attention across samples).

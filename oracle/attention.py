@@ -34,6 +34,13 @@ lengths and a top-left causal mask) gets O_i = 0 and L_i = -inf.
 
 ``row_block`` only bounds memory: each block of query rows is computed from its
 complete score rows, exactly as above; dK and dV then sum the per-block terms.
+
+Window band ("Inside FlashAttention" §6.1, sliding window: only keys inside a
+window around the query count, ``window_size=(left, right)``): with
+``window=(left, right)`` key j is visible to query i only if
+i - left <= j <= i + right, a negative side meaning unlimited; ``causal``
+additionally hides j > i (so causal with (left, 0) is the page's example).
+The band is applied as one more -inf mask on S, nothing else changes.
 """
 from __future__ import annotations
 
@@ -48,14 +55,21 @@ def as_f64(x: torch.Tensor) -> torch.Tensor:
 
 
 def scores(q: torch.Tensor, k: torch.Tensor, scale: float, causal: bool,
-           row_start: int = 0) -> torch.Tensor:
-    """S = scale * q k^T for query rows row_start.. of q; -inf above the diagonal if causal."""
+           row_start: int = 0, window=None) -> torch.Tensor:
+    """S = scale * q k^T for query rows row_start.. of q; -inf above the diagonal if
+    causal, and outside the band i - left <= j <= i + right if a window is given."""
     s = scale * torch.matmul(q, k.transpose(-1, -2))
+    nq, nk = s.shape[-2], s.shape[-1]
+    qi = torch.arange(row_start, row_start + nq).view(nq, 1)
+    kj = torch.arange(nk).view(1, nk)
     if causal:
-        nq, nk = s.shape[-2], s.shape[-1]
-        qi = torch.arange(row_start, row_start + nq).view(nq, 1)
-        kj = torch.arange(nk).view(1, nk)
         s = s.masked_fill(kj > qi, float("-inf"))
+    if window is not None:
+        left, right = window
+        if left is not None and left >= 0:
+            s = s.masked_fill(kj < qi - left, float("-inf"))
+        if right is not None and right >= 0:
+            s = s.masked_fill(kj > qi + right, float("-inf"))
     return s
 
 
@@ -71,7 +85,7 @@ def softmax_rows(s: torch.Tensor):
     return p, lse.squeeze(-1)
 
 
-def forward(q, k, v, causal: bool, scale: float, row_block: int | None = None):
+def forward(q, k, v, causal: bool, scale: float, row_block: int | None = None, window=None):
     """Exact attention output O [..., S, D] and logsumexp L [..., S] in fp64."""
     q, k, v = as_f64(q), as_f64(k), as_f64(v)
     n = q.shape[-2]
@@ -80,13 +94,13 @@ def forward(q, k, v, causal: bool, scale: float, row_block: int | None = None):
     lse = torch.empty(q.shape[:-1], dtype=F64)
     for r0 in range(0, n, rb):
         r1 = min(n, r0 + rb)
-        p, l_blk = softmax_rows(scores(q[..., r0:r1, :], k, scale, causal, r0))
+        p, l_blk = softmax_rows(scores(q[..., r0:r1, :], k, scale, causal, r0, window))
         o[..., r0:r1, :] = torch.matmul(p, v)
         lse[..., r0:r1] = l_blk
     return o, lse
 
 
-def backward(q, k, v, do, causal: bool, scale: float, row_block: int | None = None):
+def backward(q, k, v, do, causal: bool, scale: float, row_block: int | None = None, window=None):
     """Gradients (dQ, dK, dV) of loss = <O, dO> from the closed-form softmax Jacobian."""
     q, k, v, do = as_f64(q), as_f64(k), as_f64(v), as_f64(do)
     n = q.shape[-2]
@@ -96,7 +110,7 @@ def backward(q, k, v, do, causal: bool, scale: float, row_block: int | None = No
     dv = torch.zeros(v.shape, dtype=F64)
     for r0 in range(0, n, rb):
         r1 = min(n, r0 + rb)
-        p, _ = softmax_rows(scores(q[..., r0:r1, :], k, scale, causal, r0))
+        p, _ = softmax_rows(scores(q[..., r0:r1, :], k, scale, causal, r0, window))
         do_b = do[..., r0:r1, :]
         dv += torch.matmul(p.transpose(-1, -2), do_b)
         dp = torch.matmul(do_b, v.transpose(-1, -2))

@@ -47,17 +47,18 @@ def expand_kv(x: torch.Tensor, h_q: int) -> torch.Tensor:
     return torch.repeat_interleave(as_f64(x), g, dim=-3)
 
 
-def forward_gqa(q, k, v, causal: bool, scale: float, row_block: int | None = None):
-    """O [..., H, S, D] and L [..., H, S] with K, V of H_kv heads."""
+def forward_gqa(q, k, v, causal: bool, scale: float, row_block: int | None = None, window=None):
+    """O [..., H, S, D] and L [..., H, S] with K, V of H_kv heads (window as in ``oracle.forward``)."""
     h_q = q.shape[-3]
-    return forward(q, expand_kv(k, h_q), expand_kv(v, h_q), causal, scale, row_block=row_block)
+    return forward(q, expand_kv(k, h_q), expand_kv(v, h_q), causal, scale, row_block=row_block, window=window)
 
 
-def backward_gqa(q, k, v, do, causal: bool, scale: float, row_block: int | None = None):
+def backward_gqa(q, k, v, do, causal: bool, scale: float, row_block: int | None = None, window=None):
     """(dQ [..., H, S, D], dK [..., H_kv, S, D], dV [..., H_kv, S, D]) of loss = <O, dO>."""
     h_q, h_kv = q.shape[-3], k.shape[-3]
     g = group_size(h_q, h_kv)
-    dq, dk_h, dv_h = backward(q, expand_kv(k, h_q), expand_kv(v, h_q), do, causal, scale, row_block=row_block)
+    dq, dk_h, dv_h = backward(q, expand_kv(k, h_q), expand_kv(v, h_q), do, causal, scale, row_block=row_block,
+                              window=window)
     lead = dk_h.shape[:-3]
     s, d = dk_h.shape[-2], dk_h.shape[-1]
     dk = dk_h.reshape(*lead, h_kv, g, s, d).sum(dim=-3)

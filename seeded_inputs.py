@@ -44,6 +44,7 @@ class Workload:
     backward: bool = False
     seed: int = 0
     H_kv: int | None = None  # K/V heads (grouped-query attention); None = H
+    window: tuple | None = None  # (left, right) band; negative side = unlimited; None = no band
 
     @property
     def kv_heads(self) -> int:
@@ -60,7 +61,8 @@ class Workload:
     def describe(self) -> str:
         mask = "causal" if self.causal else "non-causal"
         kv = "" if self.kv_heads == self.H else f" H_kv{self.kv_heads}"
-        return f"B{self.B} H{self.H}{kv} S{self.S} D{self.D} {self.dtype} {mask}"
+        win = "" if self.window is None else f" window{tuple(self.window)}"
+        return f"B{self.B} H{self.H}{kv} S{self.S} D{self.D} {self.dtype} {mask}{win}"
 
 
 def make_inputs(w: Workload, with_dout: bool | None = None) -> dict:
@@ -176,3 +178,8 @@ VARLEN_LENGTHS = (4000, 3100, 2048, 1999, 1536, 1100, 1024, 700, 577, 300)
 PACKED_CONFIGS = {
     "varlen": PackedWorkload("varlen_causal_fwdbwd_T16384_10seq_H16D64_fp16", VARLEN_LENGTHS, 16, 64, "fp16", True),
 }
+
+# Sliding window: c2's shape and mask with a local band of 1024 keys to the
+# left of each query (the page's window_size=(left, 0) example form).
+CONFIGS["window"] = Workload("window_causal_fwdbwd_B4H16S4096D64_fp16_left1024", 4, 16, 4096, 64, "fp16", True,
+                             backward=True, window=(1024, 0))
