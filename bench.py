@@ -43,11 +43,12 @@ sys.path.insert(0, ROOT)
 
 METRIC = "attention fwd/bwd TFLOPS and % of GB300 FP16 tensor peak (B4 H16 S4096 D64 causal)"
 WORKLOAD = "c2"
-WORKLOADS = ("c2", "gqa", "mqa", "varlen", "window")
+WORKLOADS = ("c2", "gqa", "mqa", "varlen", "window", "splitkv")
 FLUSH_BYTES = 256 << 20  # > 129 MB L2
 KERNEL_SOURCES = ["exact_attention_18_gb300/csrc/fa_fwd.cu", "exact_attention_18_gb300/csrc/fa_fwd4.cu",
                   "exact_attention_18_gb300/csrc/fa_bwd.cu", "exact_attention_18_gb300/csrc/fa_softmax.cuh",
-                  "exact_attention_18_gb300/csrc/fa_kernel_common.cuh", "exact_attention_18_gb300/csrc/sm103_ptx.cuh"]
+                  "exact_attention_18_gb300/csrc/fa_kernel_common.cuh", "exact_attention_18_gb300/csrc/sm103_ptx.cuh",
+                  "exact_attention_18_gb300/csrc/fa_internal.cuh"]
 
 
 def is_packed(w):
@@ -347,6 +348,14 @@ def main():
         B, S = w.B, w.S
         ws_bytes = fa.fa_bwd_gqa_workspace_size(B, H, Hkv, S, D)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    # Split-KV forward (the splitkv workload): shard count and the partials' workspace.
+    n_split = fa.fa_splitkv_num_splits(B, H, S, D) if args.workload == "splitkv" else 0
+    split_bytes = fa.fa_fwd_splitkv_workspace_size(B, H, S, D, n_split) if n_split else 0
+    split_ws = torch.empty(max(split_bytes, 256), dtype=torch.uint8, device=dev)
+    # Kernel launches per step: forward (+ merge when split), Delta, dK/dV (+ partial-sum
+    # reduction when the grouped pass splits), dQ.
+    delta_bytes = ((H * (w.total if packed else B * S) * 4) + 255) // 256 * 256
+    launches_per_step = 4 + (1 if n_split else 0) + (1 if ws_bytes > delta_bytes else 0)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     sp = stream.cuda_stream
@@ -355,6 +364,9 @@ def main():
     win = None if packed else w.window
 
     def fwd_call(q_, k_, v_, o_, lse_, cu_=None):
+        if n_split:
+            return fa.fa_fwd_splitkv(q_, k_, v_, o_, lse_, B, H, Hkv, S, D, w.causal, n_split, w.scale, dt_code,
+                                     split_ws.data_ptr(), split_bytes, sp)
         if win is not None:
             return fa.fa_fwd_window(q_, k_, v_, o_, lse_, B, H, Hkv, S, D, w.causal, win[0], win[1], w.scale, dt_code,
                                     sp)
@@ -430,6 +442,23 @@ def main():
     bwd_ms = statistics.mean([a + b + c for a, b, c in zip(per["fa_bwd_preprocess_kernel"],
                                                            per["fa_bwd_dkdv_kernel"], per["fa_bwd_dq_kernel"])])
     peaks = load_peaks()
+    unsplit = None
+    if n_split:
+        # The same forward without splitting the keys, for comparison (same protocol).
+        ts = []
+        for i in range(args.warmup + 20):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            st = fa.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, S, D,
+                           w.causal, w.scale, dt_code, sp)
+            e1.record(stream)
+            if st:
+                raise RuntimeError(f"fa_fwd: {fa.fa_status_string(st)} {fa.fa_last_error_detail()}")
+            if i >= args.warmup:
+                ts.append((e0, e1))
+        torch.cuda.synchronize()
+        unsplit = {"ms": statistics.mean(a.elapsed_time(b) for a, b in ts), "shards": n_split}
     work = kernel_work(w)
     avg = {n: statistics.mean(per[n]) for n in names}
     dom = max(names, key=lambda n: avg[n])
@@ -546,7 +575,9 @@ def main():
                            global_batch=(w.batch if packed else w.B) * world,
                            seq_len=w.max_seqlen if packed else w.S,
                            parallelism=f"independent x{world}",
-                           step=("fa_fwd_varlen + fa_bwd_varlen" if packed else
+                           step=(f"fa_fwd_splitkv ({n_split} shards, merge included in the forward kernel time) + fa_bwd"
+                                 if n_split else
+                                 "fa_fwd_varlen + fa_bwd_varlen" if packed else
                                  "fa_fwd_window + fa_bwd_window" if win is not None else
                                  "fa_fwd + fa_bwd" if w.kv_heads == w.H else "fa_fwd_gqa + fa_bwd_gqa"),
                            l2="flushed between timed steps (256 MiB write)",
@@ -557,11 +588,12 @@ def main():
             "bwd": {"ms": bwd_ms, "TFLOP/s": f_bwd / (bwd_ms * 1e-3) / 1e12,
                     "frac_of_tensor_peak": f_bwd / (bwd_ms * 1e-3) / 1e12 / peaks["tensor_tflops"]},
             "kernels": kernels,
+            **({"fwd_unsplit": unsplit} if unsplit else {}),
             "roofline": roof,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "clocks": clocks,
-            "gpu_launches": 4 * args.steps,
+            "gpu_launches": launches_per_step * args.steps,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:

@@ -6,7 +6,8 @@ the library's CUDA kernels.  PyTorch supplies device memory and streams.
 The raw entry points keep the C names and signatures (pointers as ints):
 ``fa_fwd``, ``fa_fwd_gqa``, ``fa_bwd``, ``fa_bwd_marked``, ``fa_bwd_gqa``,
 ``fa_bwd_gqa_marked``, ``fa_bwd_noalloc``, ``fa_bwd_workspace_size``, ``fa_bwd_gqa_workspace_size``,
-``fa_fwd_window``, ``fa_bwd_window``, ``fa_bwd_window_marked``,
+``fa_fwd_window``, ``fa_bwd_window``, ``fa_bwd_window_marked``, ``fa_fwd_splitkv``,
+``fa_fwd_splitkv_workspace_size``, ``fa_splitkv_num_splits``, ``fa_merge_lse``,
 ``fa_fwd_varlen``, ``fa_bwd_varlen``, ``fa_bwd_varlen_marked``,
 ``fa_bwd_varlen_workspace_size``, ``fa_status_string``, ``fa_last_error_detail``,
 ``fa_check_device_errors``.  ``forward`` and ``backward`` wrap them for
@@ -31,7 +32,8 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "lib
 __all__ = ["fa_fwd", "fa_fwd_gqa", "fa_bwd", "fa_bwd_marked", "fa_bwd_gqa", "fa_bwd_gqa_marked", "fa_bwd_noalloc",
            "fa_bwd_workspace_size", "fa_bwd_gqa_workspace_size", "fa_fwd_varlen", "fa_bwd_varlen",
            "fa_bwd_varlen_marked", "fa_bwd_varlen_workspace_size", "forward_varlen", "backward_varlen",
-           "fa_fwd_window", "fa_bwd_window", "fa_bwd_window_marked", "fa_status_string", "fa_last_error_detail",
+           "fa_fwd_window", "fa_bwd_window", "fa_bwd_window_marked", "fa_fwd_splitkv",
+           "fa_fwd_splitkv_workspace_size", "fa_splitkv_num_splits", "fa_merge_lse", "forward_splitkv", "merge_lse", "fa_status_string", "fa_last_error_detail",
            "fa_check_device_errors", "forward", "backward", "FAError", "FA_FP16", "FA_BF16", "STATUS",
            "library_path", "load_library"]
 
@@ -86,6 +88,14 @@ def _load():
     lib.fa_bwd_window_marked.restype = i32
     lib.fa_bwd_window_marked.argtypes = [vp] * 9 + [i64] * 5 + [i32, i64, i64, f32, i32, vp, sz, vp,
                                                                 ctypes.POINTER(vp)]
+    lib.fa_fwd_splitkv.restype = i32
+    lib.fa_fwd_splitkv.argtypes = [vp] * 5 + [i64] * 5 + [i32, i64, f32, i32, vp, sz, vp]
+    lib.fa_fwd_splitkv_workspace_size.restype = sz
+    lib.fa_fwd_splitkv_workspace_size.argtypes = [i64] * 5
+    lib.fa_splitkv_num_splits.restype = i64
+    lib.fa_splitkv_num_splits.argtypes = [i64] * 4
+    lib.fa_merge_lse.restype = i32
+    lib.fa_merge_lse.argtypes = [vp] * 4 + [i64] * 3 + [i32, vp]
     lib.fa_bwd_noalloc.restype = i32
     lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i32, f32, i32, vp]
     lib.fa_status_string.restype = ctypes.c_char_p
@@ -166,6 +176,24 @@ def fa_bwd_window_marked(q, k, v, o, dout, lse, dq, dk, dv, B, H, H_kv, S, D, ca
     return _load().fa_bwd_window_marked(q, k, v, o, dout, lse, dq, dk, dv, B, H, H_kv, S, D, int(causal),
                                         int(window_left), int(window_right), float(scale), int(dtype), workspace,
                                         workspace_bytes, stream, arr)
+
+
+def fa_fwd_splitkv(q, k, v, o, lse, B, H, H_kv, S, D, causal, num_splits, scale, dtype, workspace, workspace_bytes,
+                   stream) -> int:
+    return _load().fa_fwd_splitkv(q, k, v, o, lse, B, H, H_kv, S, D, int(causal), int(num_splits), float(scale),
+                                  int(dtype), workspace, workspace_bytes, stream)
+
+
+def fa_fwd_splitkv_workspace_size(B, H, S, D, num_splits) -> int:
+    return _load().fa_fwd_splitkv_workspace_size(B, H, S, D, num_splits)
+
+
+def fa_splitkv_num_splits(B, H, S, D) -> int:
+    return _load().fa_splitkv_num_splits(B, H, S, D)
+
+
+def fa_merge_lse(o_part, lse_part, o, lse, shards, rows, D, dtype, stream) -> int:
+    return _load().fa_merge_lse(o_part, lse_part, o, lse, shards, rows, D, int(dtype), stream)
 
 
 def fa_fwd_varlen(q, k, v, o, lse, cu_seqlens, batch, max_seqlen, total, H, H_kv, D, causal, scale, dtype,
@@ -401,3 +429,39 @@ def backward_varlen(q, k, v, o, do, lse, cu_seqlens, max_seqlen: int, causal: bo
                          T, H, hk, D, causal, scale, _dtype_code(q), workspace.data_ptr(),
                          workspace.numel() * workspace.element_size(), _stream_ptr(stream)), "fa_bwd_varlen")
     return dq, dk, dv
+
+
+def forward_splitkv(q, k, v, causal: bool = False, scale: float | None = None, num_splits: int | None = None,
+                    workspace=None, stream=None):
+    """O and L of exact attention computed as key shards merged by logsumexp ([B, H, S, D] tensors)."""
+    import torch
+    q, k, v = _bhsd(q, "q"), _bhsd(k, "k"), _bhsd(v, "v")
+    B, H, S, D = q.shape
+    hk = _kv_heads(q, k, v)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    n = fa_splitkv_num_splits(B, H, S, D) if num_splits is None else int(num_splits)
+    o = torch.empty_like(q)
+    l = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
+    need = fa_fwd_splitkv_workspace_size(B, H, S, D, n)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _check(fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), l.data_ptr(), B, H, hk, S, D, causal,
+                          n, scale, _dtype_code(q), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                          _stream_ptr(stream)), "fa_fwd_splitkv")
+    return o, l
+
+
+def merge_lse(o_part, lse_part, dtype, stream=None):
+    """Merge fp32 partials o_part [P, rows, D], lse_part [P, rows] into (O [rows, D] of `dtype`, L [rows])."""
+    import torch
+    if o_part.dtype != torch.float32 or lse_part.dtype != torch.float32 or o_part.dim() != 3 \
+            or lse_part.shape != o_part.shape[:2] or not o_part.is_contiguous() or not lse_part.is_contiguous():
+        raise ValueError("o_part must be contiguous fp32 [P, rows, D] and lse_part fp32 [P, rows]")
+    P, rows, D = o_part.shape
+    o = torch.empty((rows, D), dtype=dtype, device=o_part.device)
+    l = torch.empty((rows,), dtype=torch.float32, device=o_part.device)
+    code = FA_FP16 if dtype == torch.float16 else FA_BF16
+    _check(fa_merge_lse(o_part.data_ptr(), lse_part.data_ptr(), o.data_ptr(), l.data_ptr(), P, rows, D, code,
+                        _stream_ptr(stream)), "fa_merge_lse")
+    return o, l

@@ -225,8 +225,26 @@ fa_status encode_input(CUtensorMap* map, const void* base, bool bf16, const Shap
   return FA_OK;
 }
 
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Split-KV: keys per shard (a multiple of 128) and shard count for a request of n splits.
+void splitkv_layout(int64_t S, int64_t n, int* chunk, int* shards) {
+  const int64_t per = (S + n - 1) / n;
+  const int64_t c = ((per + 127) / 128) * 128;
+  *chunk = static_cast<int>(c);
+  *shards = static_cast<int>((S + c - 1) / c);
+}
+
+size_t splitkv_bytes(const Shape& sh, int shards) {
+  return round256(static_cast<size_t>(shards) * static_cast<size_t>(sh.B * sh.H * sh.S) *
+                  static_cast<size_t>(sh.D + 1) * sizeof(float));
+}
+
+// Forward; with split > 0 (general kernels, fixed layout) the keys are cut
+// into shards whose fp32 partials go to `workspace`, then merged by L.
 fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, const Shape& sh, int causal,
-                   float scale, fa_dtype dtype, void* stream) {
+                   float scale, fa_dtype dtype, void* stream, int64_t split = 0, void* workspace = nullptr,
+                   size_t workspace_bytes = 0) {
   g_detail[0] = 0;
   fa_status st = check_shape(sh, scale, dtype);
   if (st != FA_OK) return st;
@@ -235,6 +253,18 @@ fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* 
       (st = check_ptr(o, "o")) || (st = check_ptr(lse, "lse")))
     return st;
   if (sh.packed() && !sh.cu) return fail(FA_ERR_INVALID_ARG, "cu_seqlens is NULL");
+  int chunk = 0, shards = 1;
+  if (split > 0) {
+    splitkv_layout(sh.S, split, &chunk, &shards);
+    const size_t need = splitkv_bytes(sh, shards);
+    if (!workspace) return fail(FA_ERR_WORKSPACE, "workspace is NULL (%zu bytes needed)", need);
+    if (workspace_bytes < need) return fail(FA_ERR_WORKSPACE, "workspace has %zu bytes, %zu needed", workspace_bytes, need);
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+      return fail(FA_ERR_ALIGNMENT, "workspace is not 256-byte aligned");
+    if (static_cast<int64_t>(shards) * sh.B * sh.H > 65535 * 65535LL)
+      return fail(FA_ERR_UNSUPPORTED, "too many shards");
+    if (shards > 65535) return fail(FA_ERR_UNSUPPORTED, "at most 65535 shards");
+  }
   const bool bf16 = dtype == FA_BF16;
   // Q in 128-row boxes (a CTA's own tiles); K and V in 64-row boxes.
   CUtensorMap tq, tk, tv;
@@ -254,16 +284,23 @@ fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* 
   p.win_left = sh.kernel_left();
   p.win_right = sh.kernel_right(causal != 0);
   p.group = static_cast<int>(sh.H / sh.H_kv);
+  p.kv_chunk = chunk;
+  const int64_t rows = sh.B * sh.H * sh.S;
+  p.o_part = split > 0 ? static_cast<float*>(workspace) : nullptr;
+  p.lse_part = split > 0 ? static_cast<float*>(workspace) + static_cast<size_t>(shards) * rows * sh.D : nullptr;
   p.scale_log2 = scale * kLog2e;
   p.err = fa::device_error_word();
   if (!p.err) return fail(FA_ERR_CUDA, "cannot resolve the device error word on the current device");
-  return from_cuda(fa::launch_fwd(static_cast<int>(sh.D), bf16, sh.general(causal != 0), tq, tk, tv, p,
-                                  static_cast<int>(sh.B * sh.H),
-                                  static_cast<cudaStream_t>(stream)),
-                   "forward launch");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((st = from_cuda(fa::launch_fwd(static_cast<int>(sh.D), bf16, split > 0 || sh.general(causal != 0), tq, tk, tv,
+                                     p, static_cast<int>(sh.B * sh.H), s),
+                      "forward launch")))
+    return st;
+  if (split > 0)
+    return from_cuda(fa::launch_merge_lse(static_cast<int>(sh.D), bf16, p.o_part, p.lse_part, shards, rows, o, lse, s),
+                     "split-KV merge launch");
+  return FA_OK;
 }
-
-size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 // Backward workspace: the fp32 row vector Delta of every query row, then, when
 // the dK/dV pass splits a K/V head's query heads over several CTAs, their fp32
@@ -389,6 +426,54 @@ fa_status fa_fwd_window(const void* q, const void* k, const void* v, void* o, fl
                         float scale, fa_dtype dtype, void* stream) {
   return fwd_impl(q, k, v, o, lse, windowed(B, H, H_kv, S, D, window_left, window_right), causal, scale, dtype,
                   stream);
+}
+
+fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
+                         int64_t H_kv, int64_t S, int64_t D, int causal, int64_t num_splits, float scale,
+                         fa_dtype dtype, void* workspace, size_t workspace_bytes, void* stream) {
+  if (num_splits < 1) {
+    g_detail[0] = 0;
+    return fail(FA_ERR_INVALID_ARG, "num_splits=%lld must be at least 1", (long long)num_splits);
+  }
+  return fwd_impl(q, k, v, o, lse, fixed(B, H, H_kv, S, D), causal, scale, dtype, stream, num_splits, workspace,
+                  workspace_bytes);
+}
+
+size_t fa_fwd_splitkv_workspace_size(int64_t B, int64_t H, int64_t S, int64_t D, int64_t num_splits) {
+  if (B <= 0 || H <= 0 || S <= 0 || num_splits < 1) return 0;
+  int chunk = 0, shards = 1;
+  splitkv_layout(S, num_splits, &chunk, &shards);
+  return splitkv_bytes(fixed(B, H, H, S, D), shards);
+}
+
+int64_t fa_splitkv_num_splits(int64_t B, int64_t H, int64_t S, int64_t D) {
+  // Enough shards to give every SM of a 152-SM GPU two CTAs, no more than one
+  // shard per 128 keys.
+  if (B <= 0 || H <= 0 || S <= 0 || (D != 16 && D != 32 && D != 64 && D != 128)) return 1;
+  const int64_t rows_per_cta = fa::fwd_rows_per_cta(static_cast<int>(D));
+  const int64_t ctas = B * H * ((S + rows_per_cta - 1) / rows_per_cta);
+  const int64_t want = (2 * 152 + ctas - 1) / ctas;
+  const int64_t cap = (S + 127) / 128;
+  return want < 1 ? 1 : (want > cap ? cap : want);
+}
+
+fa_status fa_merge_lse(const float* o_part, const float* lse_part, void* o, float* lse, int64_t shards,
+                       int64_t rows, int64_t D, fa_dtype dtype, void* stream) {
+  g_detail[0] = 0;
+  if (shards < 1 || rows < 0) return fail(FA_ERR_INVALID_ARG, "shards must be >= 1 and rows >= 0");
+  if (dtype != FA_FP16 && dtype != FA_BF16) return fail(FA_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+  if (D != 16 && D != 32 && D != 64 && D != 128)
+    return fail(FA_ERR_UNSUPPORTED, "head dimension D=%lld is not one of 16, 32, 64, 128", (long long)D);
+  if (shards > (int64_t(1) << 31) || (rows > 0 && shards > (int64_t(1) << 60) / (rows * (D + 1))))
+    return fail(FA_ERR_UNSUPPORTED, "partials too large");
+  if (rows == 0) return FA_OK;
+  fa_status st;
+  if ((st = check_ptr(o_part, "o_part")) || (st = check_ptr(lse_part, "lse_part")) || (st = check_ptr(o, "o")) ||
+      (st = check_ptr(lse, "lse")))
+    return st;
+  return from_cuda(fa::launch_merge_lse(static_cast<int>(D), dtype == FA_BF16, o_part, lse_part,
+                                        static_cast<int>(shards), rows, o, lse, static_cast<cudaStream_t>(stream)),
+                   "merge launch");
 }
 
 fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,

@@ -153,12 +153,21 @@ __global__ void __launch_bounds__(kF4Threads, 1)
   const int wr = GENERAL ? p.win_right : 0;
   // Key blocks [first_blk(r), blocks_for(r)) of the 128-row tile starting at
   // row r (empty past S).
+  // Split-KV (general instantiation, kv_chunk > 0): the CTA's blockIdx.z
+  // takes keys [kv_lo, kv_hi) only; kv_chunk is a multiple of 128.
+  int kv_lo = 0, kv_hi = S;
+  if constexpr (GENERAL) {
+    if (p.kv_chunk > 0) {
+      kv_lo = static_cast<int>(blockIdx.z) * p.kv_chunk;
+      kv_hi = min(S, kv_lo + p.kv_chunk);
+    }
+  }
   auto first_blk = [&](int r) -> int {
-    if constexpr (GENERAL) return r >= S ? 0 : max(0, r - wl) / kBN;
+    if constexpr (GENERAL) return r >= S ? 0 : max(kv_lo, r - wl) / kBN;
     else return 0;
   };
   auto blocks_for = [&](int r) -> int {
-    if constexpr (GENERAL) return r >= S ? 0 : min(n_kv, min(S - 1, r + kBlockM - 1 + wr) / kBN + 1);
+    if constexpr (GENERAL) return r >= S ? 0 : min((kv_hi + kBN - 1) / kBN, min(S - 1, r + kBlockM - 1 + wr) / kBN + 1);
     else return r >= S ? 0 : (p.causal ? min(n_kv, (r + kBlockM + kBN - 1) / kBN) : n_kv);
   };
   const int kb_cta = first_blk(row0);  // the CTA loads key blocks kb_cta, kb_cta + 1, ...
@@ -439,7 +448,29 @@ __global__ void __launch_bounds__(kF4Threads, 1)
       warp_arrive(&bar_pfull[t]);
     }
     // ------------------------------------------------------------ epilogue
-    if (alive && nb > 0 && warp_wait(&bar_ofinal[t], 0, abort_flag, p.err, kErrTimeoutSoftmax)) {
+    const bool have = alive && nb > 0 && warp_wait(&bar_ofinal[t], 0, abort_flag, p.err, kErrTimeoutSoftmax);
+    if (GENERAL && p.o_part != nullptr) {
+      // Split-KV partial of shard blockIdx.z: fp32 O / l and L into
+      // [shard][B*H*S] rows; a row that sees no key of the shard gets O = 0,
+      // L = -inf (it then carries no weight in the merge).
+      if (alive) {
+        if (have) tc_fence_after();
+        const bool row_ok = row_g < S;
+        const bool seen = have && l > 0.f;
+        const size_t prow = (static_cast<size_t>(blockIdx.z) * gridDim.x + bh) * S + (row_ok ? row_g : 0);
+        float* orow = p.o_part + prow * D;
+        const float inv_l = seen ? 1.f / l : 0.f;
+#pragma unroll
+        for (int c = 0; c < D; c += 16) {
+          uint32_t o16[16];
+          if (have) tmem_ld16(t_o + c, o16);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) o16[i] = seen ? o16[i] : 0u;
+          if (row_ok) store_row16_f32(orow + c, o16, inv_l);
+        }
+        if (row_ok) p.lse_part[prow] = seen ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+      }
+    } else if (have) {
       tc_fence_after();
       const float inv_l = 1.f / l;
       const bool row_ok = row_g < S;
@@ -482,7 +513,9 @@ cudaError_t launch_fwd4_t(const CUtensorMap& tq, const CUtensorMap& tk, const CU
   e = cudaFuncGetAttributes(&attr, kern);
   if (e != cudaSuccess) return e;
   if (attr.numRegs != kF4LaunchRegs) return cudaErrorInvalidConfiguration;
-  dim3 grid(BH, p.n_m_tiles);
+  // Split-KV: one grid slice per key shard.
+  const int shards = (GENERAL && p.kv_chunk > 0) ? (p.S + p.kv_chunk - 1) / p.kv_chunk : 1;
+  dim3 grid(BH, p.n_m_tiles, shards);
   kern<<<grid, kF4Threads, L::kSmemBytes, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }

@@ -29,6 +29,10 @@ struct FwdParams {
   int win_left;        // general kernels: key j visible to query i iff i - win_left <= j <= i + win_right
   int win_right;       // (kNoWindow = unlimited; causal sets win_right = 0)
   int group;           // query heads per K/V head: query head bh reads K/V head bh / group
+  int kv_chunk;        // general kernels, split-KV: keys per shard (a multiple of 128; 0 = no split);
+                       // shard z = blockIdx.z covers keys [z*kv_chunk, (z+1)*kv_chunk)
+  float* o_part;       // split-KV: fp32 O of each shard, [shards][B*H*S][D] (else nullptr)
+  float* lse_part;     // split-KV: fp32 natural-log L of each shard, [shards][B*H*S]
   float scale_log2;    // scale * log2(e): scores enter exp2 in base 2
   int* err;            // device error word (set when a pipeline wait times out)
 };
@@ -81,6 +85,10 @@ cudaError_t launch_fwd(int D, bool bf16, bool general, const CUtensorMap& tq, co
                        const CUtensorMap& tv, const FwdParams& p, int BH, cudaStream_t stream);
 
 // rows: query rows (B*H*S, or T*H packed).
+// Split-KV merge: O = sum_s exp(L_s - L) O_s, L = ln sum_s exp(L_s), per row.
+cudaError_t launch_merge_lse(int D, bool bf16, const float* o_part, const float* lse_part, int shards, int64_t rows,
+                             void* o, float* lse, cudaStream_t stream);
+
 cudaError_t launch_bwd_preprocess(int D, bool bf16, const BwdParams& p, int64_t rows, cudaStream_t stream);
 cudaError_t launch_bwd_dkdv(int D, bool bf16, bool general, const BwdMaps& maps, const BwdParams& p,
                             cudaStream_t stream);

@@ -200,6 +200,42 @@ fa_status fa_bwd_window_marked(const void* q, const void* k, const void* v, cons
                                void* const* marks);
 
 /*
+ * Split-KV forward with a logsumexp merge ("T5 讲解" §⑥: the stored
+ * L = m + log l is what lets shards be merged).  The keys are cut into shards
+ * of ceil(S / num_splits) keys rounded up to a multiple of 128; one launch
+ * computes, per (b, h, query tile, shard), the fp32 output normalised over the
+ * shard's keys and its logsumexp into `workspace`, and a second kernel merges
+ * the shards:  L = ln sum_s exp(L_s),  O = sum_s exp(L_s - L) O_s.  The result
+ * equals fa_fwd_gqa's up to fp32 rounding; it pays off where B*H*ceil(S/512)
+ * (ceil(S/256) for D = 128) query tiles alone cannot fill the GPU.  Layouts,
+ * heads and causal as in fa_fwd_gqa.  num_splits >= 1 (1 is legal: one
+ * shard); fa_splitkv_num_splits() proposes one.  workspace: at least
+ * fa_fwd_splitkv_workspace_size() bytes, 256-byte aligned, owned by the caller.
+ */
+fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
+                         int64_t H_kv, int64_t S, int64_t D, int causal, int64_t num_splits, float scale,
+                         fa_dtype dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace of fa_fwd_splitkv: shards * B*H*S * (D + 1) fp32 values, rounded up to 256 bytes. */
+size_t fa_fwd_splitkv_workspace_size(int64_t B, int64_t H, int64_t S, int64_t D, int64_t num_splits);
+
+/* A split count that gives a 152-SM GPU at least two CTAs per SM (1 when the
+ * query tiles already do; at most one shard per 128 keys). */
+int64_t fa_splitkv_num_splits(int64_t B, int64_t H, int64_t S, int64_t D);
+
+/*
+ * The merge on its own, for partials computed elsewhere (other GPUs' key
+ * shards, a cache of earlier keys):
+ *   o_part   : DEVICE fp32 [shards, rows, D], each shard's normalised output;
+ *   lse_part : DEVICE fp32 [shards, rows], each shard's natural-log L_s
+ *              (-inf for a row that sees no key of the shard; its O_s is ignored);
+ *   o        : [rows, D] 16-bit output (dtype);  lse : [rows] fp32 output.
+ * A row whose every L_s is -inf gets O = 0 and L = -inf.  D in {16,32,64,128}.
+ */
+fa_status fa_merge_lse(const float* o_part, const float* lse_part, void* o, float* lse, int64_t shards,
+                       int64_t rows, int64_t D, fa_dtype dtype, void* stream);
+
+/*
  * Packed variable-length batches ("Inside FlashAttention" §6.1, varlen: samples
  * of different lengths concatenated with no padding, a prefix-sum array
  * cu_seqlens marking their bounds, and no attention across samples).

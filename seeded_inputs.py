@@ -183,3 +183,8 @@ PACKED_CONFIGS = {
 # left of each query (the page's window_size=(left, 0) example form).
 CONFIGS["window"] = Workload("window_causal_fwdbwd_B4H16S4096D64_fp16_left1024", 4, 16, 4096, 64, "fp16", True,
                              backward=True, window=(1024, 0))
+
+# Split-KV: one long causal head, where the query tiles alone (32 CTAs of 512
+# rows) cannot fill the GPU.
+CONFIGS["splitkv"] = Workload("splitkv_causal_fwdbwd_B1H1S16384D64_fp16", 1, 1, 16384, 64, "fp16", True,
+                              backward=True)

@@ -212,6 +212,29 @@ def test_varlen_workspace_size(lib):
     assert fa.fa_bwd_varlen_workspace_size(3, 300, 700, 4, 3, 64) == 0
 
 
+def test_splitkv_sizes_and_checks(lib):
+    # S = 16384 in ten shards of 1664 keys (1639 rounded up to 128): 10 * 16384 * (64 + 1) floats
+    assert fa.fa_splitkv_num_splits(1, 1, 16384, 64) == 10
+    assert fa.fa_splitkv_num_splits(4, 16, 4096, 64) == 1
+    assert fa.fa_splitkv_num_splits(1, 1, 100, 64) == 1
+    assert fa.fa_fwd_splitkv_workspace_size(1, 1, 16384, 64, 10) == 10 * 16384 * 65 * 4
+    assert fa.fa_fwd_splitkv_workspace_size(1, 1, 16384, 64, 0) == 0
+    args = (P, P, P, P, P, 1, 2, 2, 256, 64, 1)
+    assert fa.fa_fwd_splitkv(*args, 0, 0.125, 0, P * 16, 1 << 20, None) == 1
+    assert fa.fa_fwd_splitkv(*args, 2, 0.125, 0, 0, 1 << 20, None) == 4
+    assert fa.fa_fwd_splitkv(*args, 2, 0.125, 0, P * 16, 16, None) == 4
+    assert fa.fa_fwd_splitkv(*args, 2, 0.125, 0, P * 16 + 8, 1 << 20, None) == 3
+    assert fa.fa_fwd_splitkv(P, P, P, P, P, 1, 2, 2, 256, 48, 1, 2, 0.125, 0, P * 16, 1 << 20, None) == 2
+
+
+def test_merge_checks(lib):
+    assert fa.fa_merge_lse(P, P, P, P, 0, 10, 64, 0, None) == 1
+    assert fa.fa_merge_lse(P, P, P, P, 2, 10, 80, 0, None) == 2
+    assert fa.fa_merge_lse(P, P, P, P, 2, 10, 64, 5, None) == 1
+    assert fa.fa_merge_lse(P + 4, P, P, P, 2, 10, 64, 0, None) == 3
+    assert fa.fa_merge_lse(0, 0, 0, 0, 2, 0, 64, 0, None) == 0  # no rows: nothing to do
+
+
 def test_binding_has_no_fallback(monkeypatch):
     """Without the compiled library the binding raises instead of computing anything."""
     import importlib

@@ -7,7 +7,7 @@ import socket
 import pytest
 import torch
 
-from exact_attention_18_gb300.sharding import job_throughput, max_over_ranks, shard_heads
+from exact_attention_18_gb300.sharding import job_throughput, max_over_ranks, shard_heads, shard_keys
 
 
 @pytest.mark.parametrize("bh", [0, 1, 2, 7, 64, 1001])
@@ -74,6 +74,57 @@ def test_two_gloo_ranks(tmp_path):
         assert got == [(0, 4), (4, 3)]
         assert t_max == 2.0
         assert rate == pytest.approx(world * 2.0 * 3 / 2e-3)
+
+
+@pytest.mark.parametrize("S", [0, 1, 127, 128, 1000, 4096])
+@pytest.mark.parametrize("world", [1, 2, 3, 8])
+def test_key_shards_cover_in_aligned_ranges(S, world):
+    spans = [shard_keys(S, r, world) for r in range(world)]
+    pos = 0
+    for k0, k1 in spans:
+        assert k0 == pos or k0 == k1 == S
+        assert k0 % 128 == 0 or k0 == S
+        pos = max(pos, k1)
+    assert pos == S
+    with pytest.raises(ValueError):
+        shard_keys(10, 3, 3)
+
+
+def _context_rank(rank, world, port, out_dir):
+    """Context-parallel forward on the CPU: each rank attends every query to its key shard
+    (the fp64 oracle stands in for the kernels), the partials are all-gathered, and the
+    logsumexp merge must give the unsplit result."""
+    import torch.distributed as dist
+    import oracle
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        g = torch.Generator().manual_seed(5)
+        q, k, v = (torch.randn(2, 300, 16, generator=g, dtype=torch.float64) for _ in range(3))
+        k0, k1 = shard_keys(300, rank, world)
+        o_s, l_s = oracle.forward_shards(q, k, v, True, 0.25, [(k0, k1)])
+        o_all = [torch.empty_like(o_s) for _ in range(world)]
+        l_all = [torch.empty_like(l_s) for _ in range(world)]
+        dist.all_gather(o_all, o_s)
+        dist.all_gather(l_all, l_s)
+        o, lse = oracle.merge_lse(torch.cat(o_all), torch.cat(l_all))
+        ref_o, ref_l = oracle.forward(q, k, v, True, 0.25)
+        err = max(float((o - ref_o).abs().max()), float((lse - ref_l).abs().max()))
+        with open(os.path.join(out_dir, f"ctx{rank}.txt"), "w") as f:
+            f.write(repr((k0, k1, err)))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_context_parallel_two_gloo_ranks(tmp_path):
+    import torch.multiprocessing as mp
+    world = 2
+    mp.spawn(_context_rank, args=(world, _free_port(), str(tmp_path)), nprocs=world, join=True)
+    results = [eval((tmp_path / f"ctx{r}.txt").read_text()) for r in range(world)]
+    assert [(a, b) for a, b, _ in results] == [(0, 256), (256, 300)]
+    for _, _, err in results:
+        assert err < 1e-12
 
 
 @pytest.mark.gpu
