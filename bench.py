@@ -43,7 +43,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "attention fwd/bwd TFLOPS and % of GB300 FP16 tensor peak (B4 H16 S4096 D64 causal)"
 WORKLOAD = "c2"
-WORKLOADS = ("c2", "gqa", "mqa", "varlen", "window", "splitkv")
+WORKLOADS = ("c2", "c4", "c5", "gqa", "mqa", "varlen", "window", "splitkv")
 FLUSH_BYTES = 256 << 20  # > 129 MB L2
 KERNEL_SOURCES = ["exact_attention_18_gb300/csrc/fa_fwd.cu", "exact_attention_18_gb300/csrc/fa_fwd4.cu",
                   "exact_attention_18_gb300/csrc/fa_bwd.cu", "exact_attention_18_gb300/csrc/fa_softmax.cuh",
@@ -132,8 +132,9 @@ def load_peaks():
     return {"hbm_gbs": 6800.0, "tensor_tflops": 1900.0, "tensor_tflops_sustained": 1700.0, "source": "fallback"}
 
 
-def load_traffic():
-    """DRAM bytes per launch from the committed ncu summary, if it matches the current kernels."""
+def load_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this workload
+    and matches the current kernels."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(path):
         return {}
@@ -141,7 +142,7 @@ def load_traffic():
         d = json.load(f)
     if d.get("sources_digest") != sources_digest():
         return {}
-    return d.get("bytes_per_launch", {})
+    return d.get("bytes_per_launch", {}).get(workload, {})
 
 
 class ClockSampler:
@@ -463,7 +464,7 @@ def main():
     avg = {n: statistics.mean(per[n]) for n in names}
     dom = max(names, key=lambda n: avg[n])
     kind, amount = work[dom]
-    traffic = load_traffic().get(dom)
+    traffic = load_traffic(args.workload).get(dom)
     if kind == "tensor":
         achieved = amount / (avg[dom] * 1e-3) / 1e12
         roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peaks["tensor_tflops"],
@@ -570,7 +571,7 @@ def main():
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "fp16", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
             "config": dict(workload_config(w),
                            global_batch=(w.batch if packed else w.B) * world,
                            seq_len=w.max_seqlen if packed else w.S,

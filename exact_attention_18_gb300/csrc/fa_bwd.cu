@@ -320,8 +320,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // the dQ pass.  K/V head h serves query heads h*group .. h*group+group-1; in
   // the dK/dV pass kv_splits CTAs share a K/V head, CTA `kv_part` taking the
   // group's heads kv_part*hpc .. kv_part*hpc+hpc-1.
-  const int bh = KV_OUTER ? static_cast<int>(blockIdx.x) / p.kv_splits : static_cast<int>(blockIdx.x);
-  const int kv_part = KV_OUTER ? static_cast<int>(blockIdx.x) - bh * p.kv_splits : 0;
+  int cx, cy;
+  cta_coords(!p.causal, &cx, &cy);
+  const int bh = KV_OUTER ? cx / p.kv_splits : cx;
+  const int kv_part = KV_OUTER ? cx - bh * p.kv_splits : 0;
   const int hpc = KV_OUTER ? p.group / p.kv_splits : 1;
   // General instantiation: the sample of a packed batch.  Head indices are
   // global (b*H + h) in the fixed-length layout and within a token when
@@ -348,8 +350,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int loff = tok0;
   // Own tile; heavy tiles first under the causal mask (key tile 0 and query
   // tile nt-1 see the most partners).
-  const int own = KV_OUTER ? static_cast<int>(blockIdx.y)
-                           : (p.causal ? nt - 1 - static_cast<int>(blockIdx.y) : static_cast<int>(blockIdx.y));
+  const int own = KV_OUTER ? cy : (p.causal ? nt - 1 - cy : cy);
   const int own0 = own * 128;
   if constexpr (GENERAL) {
     if (own0 >= S) return;  // packed batch: this CTA lies past its sample

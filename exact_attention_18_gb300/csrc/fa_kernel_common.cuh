@@ -85,6 +85,24 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, int* 
   }
 }
 
+// Coordinates (x = head, y = tile) of this CTA in a (gridDim.x, gridDim.y)
+// grid.  Without a causal mask every tile of a head costs the same, so the
+// launch order is taken y-fastest: one head's tiles run as consecutive CTAs
+// and the CTAs resident at one time stream the keys and values (or queries
+// and output gradients) of a few heads, which stay in L2.  Under the causal
+// mask the order stays x-fastest so that every head's heaviest tile comes
+// before any lighter one.
+__device__ __forceinline__ void cta_coords(bool y_fastest, int* x, int* y) {
+  int cx = static_cast<int>(blockIdx.x), cy = static_cast<int>(blockIdx.y);
+  if (y_fastest) {
+    const int lin = cx + cy * static_cast<int>(gridDim.x);
+    cx = lin / static_cast<int>(gridDim.y);
+    cy = lin - cx * static_cast<int>(gridDim.y);
+  }
+  *x = cx;
+  *y = cy;
+}
+
 // Packed batch: first token and length of sample b from cu_seqlens (read by
 // every thread).  Returns false, and records kErrBadSeqlens, when the entries
 // contradict the call (negative start, decreasing offsets, a sample longer
