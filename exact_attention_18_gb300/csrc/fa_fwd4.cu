@@ -125,9 +125,7 @@ __global__ void __launch_bounds__(kF4Threads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  int cx, cy;
-  cta_coords(!p.causal, &cx, &cy);
-  const int bh = cx;
+  const int bh = blockIdx.x;
   // General instantiation: the sample of a packed batch (the layouts of
   // FwdParams); q_head / kvh are then heads within a token.
   int S_ = p.S, kvh_ = bh / p.group, q_head = bh, tok0 = 0;
@@ -144,7 +142,7 @@ __global__ void __launch_bounds__(kF4Threads, 1)
   const int kvh = kvh_;  // K/V head shared by this query head's group
   const int S = S_;
   // Under the causal mask the heaviest CTAs are launched first.
-  const int cta = p.causal ? p.n_m_tiles - 1 - cy : cy;
+  const int cta = p.causal ? p.n_m_tiles - 1 - static_cast<int>(blockIdx.y) : static_cast<int>(blockIdx.y);
   const int row0 = cta * kF4RowsPerCta;
   if constexpr (GENERAL) {
     if (row0 >= S) return;  // packed batch: this CTA lies past its sample
