@@ -65,13 +65,20 @@ template <int D>
 struct FwdLayout : TileGeom<D> {
   using G = TileGeom<D>;
   static constexpr bool kSepP = D <= 64;  // P in its own TMEM columns
-  static constexpr int kStages = D <= 64 ? 3 : 2;
+  // K and V blocks travel through separate rings: a K stage is released once
+  // both tiles' score products on it are done, a V stage only after both
+  // tiles' P V, about half a block later.  With one ring for both, a stage
+  // came free so late that the next K block's copy had a few hundred cycles
+  // to land; a third K stage adds a whole block of lead.
+  static constexpr int kStagesK = 3;
+  static constexpr int kStagesV = D <= 64 ? 3 : 2;
   static constexpr int kOffQ = 0;  // two query tiles
   static constexpr int kOffK = kOffQ + 2 * G::kTileBytes;
-  static constexpr int kOffV = kOffK + kStages * G::kTileBytes;
-  static constexpr int kOffBar = kOffV + kStages * G::kTileBytes;
-  // q, kfull[S], vfull[S], empty[S], sfull[2], sfree[2], pfull[2], pvdone[2], ofinal[2], drain[2], turn[8]
-  static constexpr int kNumBars = 1 + 3 * kStages + 10 + 2 + 8;
+  static constexpr int kOffV = kOffK + kStagesK * G::kTileBytes;
+  static constexpr int kOffBar = kOffV + kStagesV * G::kTileBytes;
+  // q, kfull[SK], kempty[SK], vfull[SV], vempty[SV], sfull[2], sfree[2], pfull[2], pvdone[2], ofinal[2],
+  // drain[2], turn[8]
+  static constexpr int kNumBars = 1 + 2 * kStagesK + 2 * kStagesV + 10 + 2 + 8;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemUsed = kOffMisc + 16;
   // Tensor memory is allocated whole (512 columns), so at most one CTA may
@@ -123,9 +130,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
   uint64_t* bar_q = bars;
   uint64_t* bar_kfull = bars + 1;
-  uint64_t* bar_vfull = bar_kfull + L::kStages;
-  uint64_t* bar_empty = bar_vfull + L::kStages;
-  uint64_t* bar_sfull = bar_empty + L::kStages;  // [2] per tile: S_t(j) computed
+  uint64_t* bar_kempty = bar_kfull + L::kStagesK;
+  uint64_t* bar_vfull = bar_kempty + L::kStagesK;
+  uint64_t* bar_vempty = bar_vfull + L::kStagesV;
+  uint64_t* bar_sfull = bar_vempty + L::kStagesV;  // [2] per tile: S_t(j) computed
   uint64_t* bar_sfree = bar_sfull + 2;           // [2] S_t(j) loaded by its warpgroup (separate-P layout)
   uint64_t* bar_pfull = bar_sfree + 2;           // [2] P_t(j) stored, O_t rescaled
   uint64_t* bar_pvdone = bar_pfull + 2;          // [2] O_t += P_t(j) V(j) done (separate-P layout)
@@ -204,10 +212,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
-    for (int s = 0; s < L::kStages; ++s) {
+    for (int s = 0; s < L::kStagesK; ++s) {
       mbar_init(&bar_kfull[s], 1);
+      mbar_init(&bar_kempty[s], 2);  // released by both MMA warps
+    }
+    for (int s = 0; s < L::kStagesV; ++s) {
       mbar_init(&bar_vfull[s], 1);
-      mbar_init(&bar_empty[s], 2);  // released by both MMA warps
+      mbar_init(&bar_vempty[s], 2);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bar_sfull[t], 1);
@@ -251,33 +262,39 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                      ch * (L::kRowBytes / 2), row0 + t * kBlockM, q_head);
         // K and V blocks, each as two 64-row half-block copies.
         constexpr int kHalfBytes = (kBlockN / 2) * L::kRowBytes;
-        int it = 0;
-        for (; it < nbp; ++it) {
-          const int st = it % L::kStages;
-          const int use = it / L::kStages;
-          if (use > 0 && !mbar_wait(&bar_empty[st], (use - 1) & 1, abort_flag, p.err, kErrTimeoutLoad)) break;
-          mbar_arrive_expect_tx(&bar_kfull[st], L::kTileBytes);
+        // nk, nv: K and V blocks whose copies were started.
+        int nk = 0, nv = 0;
+        for (; nv < nbp; ++nv) {
+          const int sk = nk % L::kStagesK;
+          const int uk = nk / L::kStagesK;
+          if (uk > 0 && !mbar_wait(&bar_kempty[sk], (uk - 1) & 1, abort_flag, p.err, kErrTimeoutLoad)) break;
+          mbar_arrive_expect_tx(&bar_kfull[sk], L::kTileBytes);
 #pragma unroll
           for (int ch = 0; ch < L::kChunks; ++ch)
 #pragma unroll
             for (int h = 0; h < 2; ++h)
-              tma_rows(smem + L::kOffK + st * L::kTileBytes + ch * L::kChunkBytes + h * kHalfBytes, &tm_k,
-                       &bar_kfull[st], ch * (L::kRowBytes / 2), (kb_cta + it) * kBlockN + h * (kBlockN / 2), kvh);
-          mbar_arrive_expect_tx(&bar_vfull[st], L::kTileBytes);
+              tma_rows(smem + L::kOffK + sk * L::kTileBytes + ch * L::kChunkBytes + h * kHalfBytes, &tm_k,
+                       &bar_kfull[sk], ch * (L::kRowBytes / 2), (kb_cta + nk) * kBlockN + h * (kBlockN / 2), kvh);
+          ++nk;
+          const int sv = nv % L::kStagesV;
+          const int uv = nv / L::kStagesV;
+          if (uv > 0 && !mbar_wait(&bar_vempty[sv], (uv - 1) & 1, abort_flag, p.err, kErrTimeoutLoad)) break;
+          mbar_arrive_expect_tx(&bar_vfull[sv], L::kTileBytes);
 #pragma unroll
           for (int ch = 0; ch < L::kChunks; ++ch)
 #pragma unroll
             for (int h = 0; h < 2; ++h)
-              tma_rows(smem + L::kOffV + st * L::kTileBytes + ch * L::kChunkBytes + h * kHalfBytes, &tm_v,
-                       &bar_vfull[st], ch * (L::kRowBytes / 2), (kb_cta + it) * kBlockN + h * (kBlockN / 2), kvh);
+              tma_rows(smem + L::kOffV + sv * L::kTileBytes + ch * L::kChunkBytes + h * kHalfBytes, &tm_v,
+                       &bar_vfull[sv], ch * (L::kRowBytes / 2), (kb_cta + nv) * kBlockN + h * (kBlockN / 2), kvh);
         }
-        // Teardown: every copy this thread started must land before the CTA exits.
+        // Teardown: every copy this thread started must land before the CTA
+        // exits (older copies of a ring were consumed before their stage was
+        // reused).
         drain_wait(bar_q, 0, p.err);
-        for (int x = (it > L::kStages ? it - L::kStages : 0); x < it; ++x) {
-          const int st = x % L::kStages;
-          drain_wait(&bar_kfull[st], (x / L::kStages) & 1, p.err);
-          drain_wait(&bar_vfull[st], (x / L::kStages) & 1, p.err);
-        }
+        for (int x = (nk > L::kStagesK ? nk - L::kStagesK : 0); x < nk; ++x)
+          drain_wait(&bar_kfull[x % L::kStagesK], (x / L::kStagesK) & 1, p.err);
+        for (int x = (nv > L::kStagesV ? nv - L::kStagesV : 0); x < nv; ++x)
+          drain_wait(&bar_vfull[x % L::kStagesV], (x / L::kStagesV) & 1, p.err);
       }
     } else if (warp == 9 || warp == 10) {
       // ------------------------------------------------------------ MMA issuers
@@ -299,7 +316,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           return false;
         tc_fence_after();
         const uint64_t k_desc =
-            make_sdesc(sK + (j % L::kStages) * L::kTileBytes, 16, 8 * L::kRowBytes, L::kSwz);
+            make_sdesc(sK + (j % L::kStagesK) * L::kTileBytes, 16, 8 * L::kRowBytes, L::kSwz);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           mma_ss_warp(tmem + L::kColS + 128u * t, desc_plus(q_desc, kmajor_step_bytes<D>(kk)),
@@ -309,9 +326,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       };
       // O_t += P_t(jl) V(j) once P_t(jl) is stored and O_t rescaled.
       auto pv = [&](int j, int jl) -> bool {
-        const int st = j % L::kStages;
+        const int st = j % L::kStagesV;
         if (!warp_wait(&bar_pfull[t], jl & 1, abort_flag, p.err, kErrTimeoutMma)) return false;
-        if (!warp_wait(&bar_vfull[st], (j / L::kStages) & 1, abort_flag, p.err, kErrTimeoutMma)) return false;
+        if (!warp_wait(&bar_vfull[st], (j / L::kStagesV) & 1, abort_flag, p.err, kErrTimeoutMma)) return false;
         tc_fence_after();
         const uint64_t v_desc = make_sdesc(sV + st * L::kTileBytes, L::kChunkBytes, 8 * L::kRowBytes, L::kSwz);
         const uint32_t t_p = tmem + L::kColP + L::kStrideP * t;
@@ -323,32 +340,36 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (j == nbt - 1) mma_commit_warp(&bar_ofinal[t]);
         return true;
       };
-      // This warp is done with block x once V(x) has landed and its MMAs on
-      // K(x), V(x) are issued: it releases the stage.
-      auto release = [&](int x) -> bool {
-        const int st = x % L::kStages;
-        if (!warp_wait(&bar_vfull[st], (x / L::kStages) & 1, abort_flag, p.err, kErrTimeoutMma)) return false;
-        mma_commit_warp(&bar_empty[st]);
+      // This warp is done with V(x) once it has landed and its P V on it is
+      // issued: it releases the stage (the arrival comes when the MMAs end).
+      auto release_v = [&](int x) -> bool {
+        const int st = x % L::kStagesV;
+        if (!warp_wait(&bar_vfull[st], (x / L::kStagesV) & 1, abort_flag, p.err, kErrTimeoutMma)) return false;
+        mma_commit_warp(&bar_vempty[st]);
         return true;
       };
       bool ok = warp_wait(bar_q, 0, abort_flag, p.err, kErrTimeoutMma);
       for (int j = 0; ok && j < nbp; ++j) {
-        ok = warp_wait(&bar_kfull[j % L::kStages], (j / L::kStages) & 1, abort_flag, p.err, kErrTimeoutMma);
+        const int sk = j % L::kStagesK;
+        ok = warp_wait(&bar_kfull[sk], (j / L::kStagesK) & 1, abort_flag, p.err, kErrTimeoutMma);
         if (!ok) break;
         tc_fence_after();
         const bool q_in = j >= beg && j < nbt;              // S_t of loaded block j
         const bool p_in = j >= 1 && j - 1 >= beg && j - 1 < nbt;  // P_t V of loaded block j - 1
         if (L::kSepP) {  // S_t(j) first, then O_t += P_t(j-1) V(j-1)
           if (q_in && !(ok = qk(j, j - beg))) break;
+          mma_commit_warp(&bar_kempty[sk]);
           if (p_in && !(ok = pv(j - 1, j - 1 - beg))) break;
+          if (j >= 1 && !(ok = release_v(j - 1))) break;
         } else {  // P_t(j-1) lives in S_t: its P V must precede S_t(j)
           if (p_in && !(ok = pv(j - 1, j - 1 - beg))) break;
+          if (j >= 1 && !(ok = release_v(j - 1))) break;
           if (q_in && !(ok = qk(j, j - beg))) break;
+          mma_commit_warp(&bar_kempty[sk]);  // K(j): this warp's score products on it are issued
         }
-        if (j >= 1 && !(ok = release(j - 1))) break;
       }
       if (ok && nbp - 1 >= beg && nbp - 1 < nbt) ok = pv(nbp - 1, nbp - 1 - beg);
-      if (ok && nbp > 0) release(nbp - 1);  // (split-KV: a CTA may load no block)
+      if (ok && nbp > 0) release_v(nbp - 1);  // (split-KV: a CTA may load no block)
       // Teardown: wait for every MMA this warp issued.
       mma_commit_warp(&bar_drain[t]);
       drain_wait(&bar_drain[t], 0, p.err);
