@@ -1,0 +1,76 @@
+"""Tensors of 2^31 elements.
+
+Every 16-bit input and output here holds 2^31 elements (4 GiB), so a 32-bit
+element offset anywhere in the forward, the backward or their epilogues
+would wrap.  Only the first head (offset 0) and the last head (the top of the
+range) carry seeded N(0, 1) values and are compared with the fp64 oracle: the
+last in full, forward and backward, the first in the forward.  Every other
+head is zero, which keeps the input draw cheap and gives it a closed form
+from the definition of the softmax: with q = k = 0 all visible scores are
+equal, so O_i is the mean of the visible V rows (= 0) and L_i = ln(i + 1)
+under the causal mask; with dO = 0 there, dQ = dK = dV = 0 exactly.
+"""
+import math
+
+import pytest
+import torch
+
+import oracle
+from seeded_inputs import randn
+from tests.parity import assert_close, assert_lse
+
+pytestmark = pytest.mark.gpu
+
+GIB = 1 << 30
+
+
+@pytest.fixture(scope="module")
+def fa():
+    import exact_attention_18_gb300 as m
+    m.load_library()
+    return m
+
+
+@pytest.mark.parametrize("B,H,S,D", [(16, 128, 8192, 128), (32, 128, 8192, 64)])
+def test_tensors_of_2_31_elements(fa, B, H, S, D):
+    assert B * H * S * D == 2 ** 31
+    torch.cuda.empty_cache()
+    if torch.cuda.mem_get_info()[0] < 40 * GIB:
+        pytest.skip("needs 40 GiB of free device memory")
+    dt = torch.float16
+    scale = 1.0 / math.sqrt(D)
+    dev = torch.device("cuda")
+    q, k, v, do = (torch.zeros(B, H, S, D, dtype=dt, device=dev) for _ in range(4))
+    seeded = [(0, 0), (B - 1, H - 1)]
+    host = {}
+    for i, (b, h) in enumerate(seeded):
+        host[b, h] = [randn((S, D), 1000 + 4 * i + j, dt) for j in range(4)]
+        for t, x in zip((q, k, v, do), host[b, h]):
+            t[b, h].copy_(x)
+    o, lse = fa.forward(q, k, v, causal=True, scale=scale)
+    dq, dk, dv = fa.backward(q, k, v, o, do, lse, causal=True, scale=scale)
+    torch.cuda.synchronize()
+    assert fa.fa_check_device_errors(None) == 0
+
+    # A zero head in the middle: the closed form, exactly for O and the gradients.
+    zb, zh = B // 2, H // 2
+    assert float(o[zb, zh].abs().max()) == 0.0
+    for g in (dq, dk, dv):
+        assert float(g[zb, zh].abs().max()) == 0.0
+    ln = torch.log(torch.arange(1, S + 1, dtype=torch.float64))
+    assert_lse(lse[zb, zh].cpu(), ln)
+
+    # The seeded heads against the oracle.
+    for b, h in seeded:
+        hq, hk, hv, hdo = host[b, h]
+        o_ref, l_ref = oracle.forward(hq, hk, hv, True, scale, row_block=2048)
+        assert_close(f"O[{b},{h}]", o[b, h], o_ref)
+        assert_lse(lse[b, h], l_ref)
+    b, h = seeded[-1]
+    hq, hk, hv, hdo = host[b, h]
+    r = oracle.backward(hq, hk, hv, hdo, True, scale, row_block=2048)
+    assert_close(f"dQ[{b},{h}]", dq[b, h], r[0])
+    assert_close(f"dK[{b},{h}]", dk[b, h], r[1])
+    assert_close(f"dV[{b},{h}]", dv[b, h], r[2])
+    del q, k, v, do, o, lse, dq, dk, dv
+    torch.cuda.empty_cache()
