@@ -155,10 +155,11 @@ struct BwdLayout {
   static constexpr uint32_t kColAcc1 = 128 * kXYBufs;      // dV (dK/dV pass) or dQ
   static constexpr uint32_t kColAcc2 = 128 * kXYBufs + D;  // dK (dK/dV pass)
   static_assert(kColAcc2 + D <= kTmemCols, "TMEM layout");
-  // dQ pass with D <= 64: the resident tiles A1 = Q, A2 = dO are copied into
-  // TMEM (D/2 columns each, after dQ) and the score products read A from
-  // there instead of shared memory (32 instead of 48 cycles per MMA).
-  static constexpr bool kTmemA = D <= 64;
+  // dQ pass: the resident tiles A1 = Q, A2 = dO are copied into TMEM (D/2
+  // columns each, after dQ; at D = 128 they take the columns dK would use in
+  // the dK/dV pass) and the score products read A from there instead of
+  // shared memory (32 instead of 48 cycles per M128 N64 K16 MMA).
+  static constexpr bool kTmemA = true;
   static constexpr uint32_t kColA1 = kColAcc1 + D;
   static constexpr uint32_t kColA2 = kColA1 + D / 2;
   static_assert(!kTmemA || kColA2 + D / 2 <= kTmemCols, "TMEM layout");
