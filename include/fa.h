@@ -6,7 +6,8 @@
  *     O = softmax(scale * Q K^T) V
  *
  * FlashAttention-2 style: an outer loop over 128-row query blocks and an inner
- * loop over 128-row key/value blocks with an online softmax (running row
+ * loop over key/value blocks (64 rows for D <= 64, 128 for D = 128 in the
+ * forward pass) with an online softmax (running row
  * maximum m and running sum l), so the [S, S] score matrix never reaches
  * memory.  Only O and the per-row logsumexp L are written.  The backward pass
  * recomputes the probabilities from L.  Definitions followed:
