@@ -45,10 +45,17 @@ METRIC = "attention fwd/bwd TFLOPS and % of GB300 FP16 tensor peak (B4 H16 S4096
 WORKLOAD = "c2"
 WORKLOADS = ("c2", "c4", "c5", "gqa", "mqa", "varlen", "window", "splitkv")
 FLUSH_BYTES = 256 << 20  # > 129 MB L2
-KERNEL_SOURCES = ["exact_attention_18_gb300/csrc/fa_fwd.cu", "exact_attention_18_gb300/csrc/fa_fwd4.cu",
-                  "exact_attention_18_gb300/csrc/fa_bwd.cu", "exact_attention_18_gb300/csrc/fa_softmax.cuh",
-                  "exact_attention_18_gb300/csrc/fa_kernel_common.cuh", "exact_attention_18_gb300/csrc/sm103_ptx.cuh",
-                  "exact_attention_18_gb300/csrc/fa_internal.cuh"]
+_CSRC = "exact_attention_18_gb300/csrc/"
+_COMMON = [_CSRC + f for f in ("fa_kernel_common.cuh", "sm103_ptx.cuh", "fa_internal.cuh")]
+# The sources each kernel is compiled from: a committed ncu traffic figure is used only while
+# these are unchanged since its capture.
+KERNEL_SOURCES = {
+    "fa_fwd4_kernel": [_CSRC + "fa_fwd4.cu", _CSRC + "fa_softmax.cuh"] + _COMMON,
+    "fa_fwd_kernel": [_CSRC + "fa_fwd.cu", _CSRC + "fa_softmax.cuh"] + _COMMON,
+    "fa_bwd_preprocess_kernel": [_CSRC + "fa_bwd.cu"] + _COMMON,
+    "fa_bwd_dkdv_kernel": [_CSRC + "fa_bwd.cu"] + _COMMON,
+    "fa_bwd_dq_kernel": [_CSRC + "fa_bwd.cu"] + _COMMON,
+}
 
 
 def is_packed(w):
@@ -114,9 +121,10 @@ def kernel_work(w):
     }
 
 
-def sources_digest():
+def sources_digest(kernel):
+    """Digest of the sources `kernel` is compiled from."""
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -133,16 +141,18 @@ def load_peaks():
 
 
 def load_traffic(workload):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on this workload
-    and matches the current kernels."""
+    """DRAM bytes per launch from the committed ncu summaries: the kernels captured on this
+    workload whose sources are unchanged since the capture."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(path):
         return {}
     with open(path) as f:
         d = json.load(f)
-    if d.get("sources_digest") != sources_digest():
-        return {}
-    return d.get("bytes_per_launch", {}).get(workload, {})
+    out = {}
+    for kernel, rec in d.get("bytes_per_launch", {}).get(workload, {}).items():
+        if kernel in KERNEL_SOURCES and rec.get("sources_digest") == sources_digest(kernel):
+            out[kernel] = rec["bytes"]
+    return out
 
 
 class ClockSampler:

@@ -61,12 +61,22 @@ def test_kernel_work_names_the_launched_forward():
 
 def test_traffic_is_dropped_when_the_kernel_sources_change(monkeypatch):
     with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
-        table = json.load(f)
-    monkeypatch.setattr(bench, "sources_digest", lambda: table["sources_digest"])
-    assert bench.load_traffic("c2") == table["bytes_per_launch"]["c2"]
+        table = json.load(f)["bytes_per_launch"]["c2"]
+    monkeypatch.setattr(bench, "sources_digest", lambda k: table[k]["sources_digest"])
+    assert bench.load_traffic("c2") == {k: r["bytes"] for k, r in table.items()}
     assert bench.load_traffic("no-such-workload") == {}
-    monkeypatch.setattr(bench, "sources_digest", lambda: "0000000000000000")
-    assert bench.load_traffic("c2") == {}
+    # A change to one kernel's sources drops that kernel's figure only.
+    monkeypatch.setattr(bench, "sources_digest",
+                        lambda k: "0000000000000000" if k == "fa_fwd4_kernel" else table[k]["sources_digest"])
+    got = bench.load_traffic("c2")
+    assert "fa_fwd4_kernel" not in got and got["fa_bwd_dkdv_kernel"] == table["fa_bwd_dkdv_kernel"]["bytes"]
+
+
+def test_every_kernel_lists_existing_sources():
+    for kernel, files in bench.KERNEL_SOURCES.items():
+        for rel in files:
+            assert os.path.exists(os.path.join(ROOT, rel)), (kernel, rel)
+        assert len(bench.sources_digest(kernel)) == 16
 
 
 def test_clock_summary_reports_throttle_reasons():
