@@ -43,7 +43,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "attention fwd/bwd TFLOPS and % of GB300 FP16 tensor peak (B4 H16 S4096 D64 causal)"
 WORKLOAD = "c2"
-WORKLOADS = ("c2", "c4", "c5", "gqa", "mqa", "varlen", "window", "splitkv")
+WORKLOADS = ("c2", "c4", "c5", "leaderboard", "gqa", "mqa", "varlen", "window", "splitkv")
 FLUSH_BYTES = 256 << 20  # > 129 MB L2
 _CSRC = "exact_attention_18_gb300/csrc/"
 _COMMON = [_CSRC + f for f in ("fa_kernel_common.cuh", "sm103_ptx.cuh", "fa_internal.cuh")]
@@ -240,17 +240,83 @@ def head_flops(w, heads):
     return 3.5 * f
 
 
-def cpu_baseline(inp, w, n_heads: int):
+def time_oracle_heads(inp, w, heads):
+    """Wall time of the fp64 oracle's forward + backward over `heads`, one head per call,
+    after one untimed head (thread pool and allocator warm-up).  The cpu_baseline leg and the
+    reference arm both time the oracle this way."""
+    cpu_oracle_step(inp, w, heads[:1])
+    t0 = time.perf_counter()
+    for hd in heads:
+        cpu_oracle_step(inp, w, [hd])
+    return time.perf_counter() - t0
+
+
+def cpu_threads():
     import torch
+    return {"cores": torch.get_num_threads(), "host_cpus": os.cpu_count()}
+
+
+def cpu_baseline(inp, w, n_heads: int):
     all_heads = head_list(w)
     heads = [all_heads[i % len(all_heads)] for i in range(n_heads)]
-    t0 = time.perf_counter()
-    cpu_oracle_step(inp, w, heads)
-    dt = time.perf_counter() - t0
-    return {"value": head_flops(w, heads) / dt / 1e12, "unit": "TFLOP/s", "cores": torch.get_num_threads(),
-            "kind": "oracle",
-            "sample": f"fp64 oracle fwd+bwd on {n_heads} of the {len(all_heads)} heads of {w.describe()}, "
-                      f"{dt:.2f} s; convention FLOPs of those heads / wall time"}
+    dt = time_oracle_heads(inp, w, heads)
+    return {"value": head_flops(w, heads) / dt / 1e12, "unit": "TFLOP/s", **cpu_threads(), "kind": "oracle",
+            "sample": f"fp64 oracle fwd+bwd, one head at a time, on {n_heads} of the {len(all_heads)} heads of "
+                      f"{w.describe()}, {dt:.2f} s; convention FLOPs of those heads / wall time"}
+
+
+def cpu_table():
+    """The fp64 oracle on the configured workloads' shapes (bounded samples), TFLOP/s by the
+    convention FLOPs of what was computed: forward of c1 (all threads and one thread), of one
+    c2 head, of 512 sampled rows of one c5 head; forward + backward of one c4 head and of one
+    batch entry of c3 at D = 64 and S = 256, 1024, 4096."""
+    import torch
+    import oracle
+    from seeded_inputs import CONFIGS, make_inputs
+    rows_out = []
+
+    def timed(case, fn, flops, threads=None):
+        old = torch.get_num_threads()
+        if threads:
+            torch.set_num_threads(threads)
+        try:
+            fn()  # untimed warm-up
+            t0 = time.perf_counter()
+            fn()
+            dt = time.perf_counter() - t0
+        finally:
+            torch.set_num_threads(old)
+        rows_out.append({"case": case, "TFLOP/s": flops / dt / 1e12, "s": dt, "threads": threads or old})
+
+    def head(w, b=0, h=0):
+        inp = make_inputs(w, with_dout=True)
+        return [inp[n][b, h] for n in ("q", "k", "v", "do")]
+
+    w = CONFIGS["c1"]
+    q, k, v, do = head(w)
+    f = 4.0 * w.S * w.S * w.D
+    timed("c1 fwd", lambda: oracle.forward(q, k, v, False, w.scale), f)
+    timed("c1 fwd, 1 thread", lambda: oracle.forward(q, k, v, False, w.scale), f, threads=1)
+    w = CONFIGS["c2"]
+    q, k, v, do = head(w)
+    timed("c2 fwd, one head", lambda: oracle.forward(q, k, v, True, w.scale), 4.0 * w.S * w.S * w.D / 2)
+    w = CONFIGS["c5"]
+    q, k, v, do = head(w)
+    rows = list(range(w.S - 512, w.S))
+    timed("c5 fwd, 512 rows of one head", lambda: oracle.forward_rows(q, k, v, True, w.scale, rows),
+          4.0 * w.D * sum(r + 1 for r in rows))
+    w = CONFIGS["c4"]
+    q, k, v, do = head(w)
+    timed("c4 fwd+bwd, one head",
+          lambda: (oracle.forward(q, k, v, False, w.scale, row_block=2048),
+                   oracle.backward(q, k, v, do, False, w.scale, row_block=2048)), 3.5 * 4.0 * w.S * w.S * w.D)
+    for S in (256, 1024, 4096):
+        w = CONFIGS[f"c3_d64_s{S}"]
+        q, k, v, do = head(w)
+        timed(f"c3 D64 S{S} fwd+bwd, one batch entry",
+              lambda: (oracle.forward(q, k, v, True, w.scale), oracle.backward(q, k, v, do, True, w.scale)),
+              3.5 * 4.0 * S * S * w.D / 2)
+    return rows_out
 
 
 def workload_inputs(w):
@@ -279,12 +345,10 @@ def run_reference(args, w):
     nh = len(all_heads)
     for i in range(args.warmup):
         cpu_oracle_step(inp, w, [all_heads[i % nh]])
-    done = []
+    done = [all_heads[(args.warmup + i) % nh] for i in range(args.steps)]
     t0 = time.perf_counter()
-    for i in range(args.steps):
-        hd = all_heads[(args.warmup + i) % nh]
+    for hd in done:
         cpu_oracle_step(inp, w, [hd])
-        done.append(hd)
     dt = time.perf_counter() - t0
     value = head_flops(w, done) / dt / 1e12
     sample = f"fp64 CPU oracle fwd+bwd of one head of {w.describe()} per step"
@@ -292,7 +356,7 @@ def run_reference(args, w):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": dict(workload_config(w), sample_per_step="one (b,h) head"),
-            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": torch.get_num_threads(), "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", **cpu_threads(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -307,6 +371,8 @@ def main():
     ap.add_argument("--cpu-heads", type=int, default=16, help="heads in the CPU oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-table", action="store_true",
+                    help="add the oracle timed on the configured workloads' shapes to cpu_baseline")
     ap.add_argument("--workload", default=WORKLOAD, choices=WORKLOADS)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -576,6 +642,8 @@ def main():
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(inp, w, args.cpu_heads)
+        if args.cpu_table:
+            cpu["table"] = cpu_table()
 
     if rank == 0:
         line = {

@@ -10,7 +10,7 @@ The raw entry points keep the C names and signatures (pointers as ints):
 ``fa_fwd_splitkv_workspace_size``, ``fa_splitkv_num_splits``, ``fa_merge_lse``,
 ``fa_fwd_varlen``, ``fa_bwd_varlen``, ``fa_bwd_varlen_marked``,
 ``fa_bwd_varlen_workspace_size``, ``fa_status_string``, ``fa_last_error_detail``,
-``fa_check_device_errors``.  ``forward`` and ``backward`` wrap them for
+``fa_check_device_errors``, ``fa_set_wait_limit_ns``.  ``forward`` and ``backward`` wrap them for
 contiguous [B, H, S, D] CUDA tensors; K and V (and dK, dV) may have fewer heads
 H_kv dividing H (grouped-query and multi-query attention), in which case they
 call the ``_gqa`` entry points; ``window=(left, right)`` selects the
@@ -34,7 +34,7 @@ __all__ = ["fa_fwd", "fa_fwd_gqa", "fa_bwd", "fa_bwd_marked", "fa_bwd_gqa", "fa_
            "fa_bwd_varlen_marked", "fa_bwd_varlen_workspace_size", "forward_varlen", "backward_varlen",
            "fa_fwd_window", "fa_bwd_window", "fa_bwd_window_marked", "fa_fwd_splitkv",
            "fa_fwd_splitkv_workspace_size", "fa_splitkv_num_splits", "fa_merge_lse", "forward_splitkv", "merge_lse", "fa_status_string", "fa_last_error_detail",
-           "fa_check_device_errors", "forward", "backward", "FAError", "FA_FP16", "FA_BF16", "STATUS",
+           "fa_check_device_errors", "fa_set_wait_limit_ns", "forward", "backward", "FAError", "FA_FP16", "FA_BF16", "STATUS",
            "library_path", "load_library"]
 
 FA_FP16, FA_BF16 = 0, 1
@@ -104,6 +104,8 @@ def _load():
     lib.fa_last_error_detail.argtypes = []
     lib.fa_check_device_errors.restype = i32
     lib.fa_check_device_errors.argtypes = [vp]
+    lib.fa_set_wait_limit_ns.restype = ctypes.c_uint64
+    lib.fa_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     _lib = lib
     return lib
 
@@ -246,6 +248,11 @@ def fa_last_error_detail() -> str:
 
 def fa_check_device_errors(stream=None) -> int:
     return _load().fa_check_device_errors(stream)
+
+
+def fa_set_wait_limit_ns(ns: int) -> int:
+    """Limit of each kernel pipeline wait from now on (0 = the 2 s default); returns the previous one."""
+    return _load().fa_set_wait_limit_ns(ns)
 
 
 # ----------------------------------------------------------------------- tensor wrappers

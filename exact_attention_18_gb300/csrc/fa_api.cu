@@ -3,6 +3,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -28,6 +29,11 @@ int* device_error_word() {
   }
   return addr[dev];
 }
+
+// Limit of each pipeline wait in the kernels launched from now on.
+static std::atomic<unsigned long long> g_wait_limit_ns{ptx::kWaitLimitNs};
+
+unsigned long long wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
 
 }  // namespace fa
 
@@ -291,6 +297,7 @@ fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* 
   p.scale_log2 = scale * kLog2e;
   p.err = fa::device_error_word();
   if (!p.err) return fail(FA_ERR_CUDA, "cannot resolve the device error word on the current device");
+  p.wait_ns = fa::wait_limit_ns();
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if ((st = from_cuda(fa::launch_fwd(static_cast<int>(sh.D), bf16, split > 0 || sh.general(causal != 0), tq, tk, tv,
                                      p, static_cast<int>(sh.B * sh.H), s),
@@ -371,6 +378,7 @@ fa_status bwd_impl(const void* q, const void* k, const void* v, const void* o, c
   p.scale_log2 = scale * kLog2e;
   p.err = fa::device_error_word();
   if (!p.err) return fail(FA_ERR_CUDA, "cannot resolve the device error word on the current device");
+  p.wait_ns = fa::wait_limit_ns();
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int Di = static_cast<int>(sh.D);
   const int64_t q_rows = sh.q_rows(), kv_rows = sh.kv_rows();
@@ -604,6 +612,11 @@ const char* fa_status_string(fa_status status) {
 }
 
 const char* fa_last_error_detail(void) { return g_detail; }
+
+uint64_t fa_set_wait_limit_ns(uint64_t ns) {
+  const unsigned long long v = ns == 0 ? fa::ptx::kWaitLimitNs : static_cast<unsigned long long>(ns);
+  return static_cast<uint64_t>(fa::g_wait_limit_ns.exchange(v));
+}
 
 fa_status fa_check_device_errors(void* stream) {
   g_detail[0] = 0;

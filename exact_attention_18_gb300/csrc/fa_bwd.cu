@@ -439,7 +439,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       const int st = it % L::kStages;
       const int use = it / L::kStages;
-      if (use > 0 && !warp_wait(&bar_empty[st], (use - 1) & 1, abort_flag, p.err, kErrTimeoutLoad)) break;
+      if (use > 0 && !warp_wait(&bar_empty[st], (use - 1) & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutLoad)) break;
       const int r0 = pblk * kPN;
       if (lane == 0) {
         mbar_arrive_expect_tx(&bar_bfull[st], 2 * GB::kTileBytes);
@@ -492,7 +492,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (warp == kMmaWarp) {
       const uint64_t a1_desc = make_sdesc(sA1, 16, 8 * GA::kRowBytes, GA::kSwz);
       const uint64_t a2_desc = make_sdesc(sA2, 16, 8 * GA::kRowBytes, GA::kSwz);
-      ok = warp_wait(bar_afull, 0, abort_flag, p.err, kErrTimeoutMma);
+      ok = warp_wait(bar_afull, 0, abort_flag, p.err, p.wait_ns, kErrTimeoutMma);
       constexpr bool kAFromTmem = !KV_OUTER && L::kTmemA;
       if (kAFromTmem && ok) {
         tc_fence_after();
@@ -505,9 +505,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int i = 0; ok && i < niter; ++i) {
         const int st = i % L::kStages;
         const int b = i % L::kXYBufs;
-        ok = warp_wait(&bar_bfull[st], (i / L::kStages) & 1, abort_flag, p.err, kErrTimeoutMma);
+        ok = warp_wait(&bar_bfull[st], (i / L::kStages) & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutMma);
         if (ok && i >= L::kXYBufs)
-          ok = warp_wait(&bar_accissued[b], ((i / L::kXYBufs) - 1) & 1, abort_flag, p.err, kErrTimeoutMma);
+          ok = warp_wait(&bar_accissued[b], ((i / L::kXYBufs) - 1) & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutMma);
         if (!ok) break;
         tc_fence_after();
         const uint32_t tb = tmem + 128u * b;
@@ -540,7 +540,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int x = 0; ok && x < niter; ++x) {
         const int st = x % L::kStages;
         const int b = x % L::kXYBufs;
-        ok = warp_wait(&bar_pfull[x & 1], (x >> 1) & 1, abort_flag, p.err, kErrTimeoutMma);
+        ok = warp_wait(&bar_pfull[x & 1], (x >> 1) & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutMma);
         if (!ok) break;
         tc_fence_after();
         const uint32_t tb = tmem + 128u * b;
@@ -607,8 +607,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         while (pi >= nper) pi -= nper;
       }
       bool ok = true;
-      if constexpr (KV_OUTER) ok = warp_wait(&bar_bfull[st], (i / L::kStages) & 1, abort_flag, p.err, kErrTimeoutSoftmax);
-      ok = ok && warp_wait(&bar_xyfull[i % L::kXYBufs], (i / L::kXYBufs) & 1, abort_flag, p.err, kErrTimeoutSoftmax);
+      if constexpr (KV_OUTER) ok = warp_wait(&bar_bfull[st], (i / L::kStages) & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutSoftmax);
+      ok = ok && warp_wait(&bar_xyfull[i % L::kXYBufs], (i / L::kXYBufs) & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutSoftmax);
       if (!ok) {
         alive = false;
         break;
@@ -667,7 +667,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (lane == 0) mbar_arrive(&bar_pfull[g]);
     }
     // ------------------------------------------------------------ epilogue
-    const bool done = alive && mbar_wait(bar_accfinal, 0, abort_flag, p.err, kErrTimeoutSoftmax);
+    const bool done = alive && mbar_wait(bar_accfinal, 0, abort_flag, p.err, p.wait_ns, kErrTimeoutSoftmax);
     // The 16 warps split the accumulator columns of their 32 rows into up to
     // four parts of at least 16 columns.
     constexpr int kParts = D >= 64 ? 4 : D / 16;

@@ -267,7 +267,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (; nv < nbp; ++nv) {
           const int sk = nk % L::kStagesK;
           const int uk = nk / L::kStagesK;
-          if (uk > 0 && !mbar_wait(&bar_kempty[sk], (uk - 1) & 1, abort_flag, p.err, kErrTimeoutLoad)) break;
+          if (uk > 0 && !mbar_wait(&bar_kempty[sk], (uk - 1) & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutLoad)) break;
           mbar_arrive_expect_tx(&bar_kfull[sk], L::kTileBytes);
 #pragma unroll
           for (int ch = 0; ch < L::kChunks; ++ch)
@@ -278,7 +278,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           ++nk;
           const int sv = nv % L::kStagesV;
           const int uv = nv / L::kStagesV;
-          if (uv > 0 && !mbar_wait(&bar_vempty[sv], (uv - 1) & 1, abort_flag, p.err, kErrTimeoutLoad)) break;
+          if (uv > 0 && !mbar_wait(&bar_vempty[sv], (uv - 1) & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutLoad)) break;
           mbar_arrive_expect_tx(&bar_vfull[sv], L::kTileBytes);
 #pragma unroll
           for (int ch = 0; ch < L::kChunks; ++ch)
@@ -312,7 +312,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       // S_t = Q_t K(j)^T (the tile's block jl); with separate P, first wait
       // until the warpgroup has loaded S_t(jl-1).
       auto qk = [&](int j, int jl) -> bool {
-        if (L::kSepP && jl > 0 && !warp_wait(&bar_sfree[t], (jl - 1) & 1, abort_flag, p.err, kErrTimeoutMma))
+        if (L::kSepP && jl > 0 && !warp_wait(&bar_sfree[t], (jl - 1) & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutMma))
           return false;
         tc_fence_after();
         const uint64_t k_desc =
@@ -327,8 +327,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       // O_t += P_t(jl) V(j) once P_t(jl) is stored and O_t rescaled.
       auto pv = [&](int j, int jl) -> bool {
         const int st = j % L::kStagesV;
-        if (!warp_wait(&bar_pfull[t], jl & 1, abort_flag, p.err, kErrTimeoutMma)) return false;
-        if (!warp_wait(&bar_vfull[st], (j / L::kStagesV) & 1, abort_flag, p.err, kErrTimeoutMma)) return false;
+        if (!warp_wait(&bar_pfull[t], jl & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutMma)) return false;
+        if (!warp_wait(&bar_vfull[st], (j / L::kStagesV) & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutMma)) return false;
         tc_fence_after();
         const uint64_t v_desc = make_sdesc(sV + st * L::kTileBytes, L::kChunkBytes, 8 * L::kRowBytes, L::kSwz);
         const uint32_t t_p = tmem + L::kColP + L::kStrideP * t;
@@ -344,14 +344,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       // issued: it releases the stage (the arrival comes when the MMAs end).
       auto release_v = [&](int x) -> bool {
         const int st = x % L::kStagesV;
-        if (!warp_wait(&bar_vfull[st], (x / L::kStagesV) & 1, abort_flag, p.err, kErrTimeoutMma)) return false;
+        if (!warp_wait(&bar_vfull[st], (x / L::kStagesV) & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutMma)) return false;
         mma_commit_warp(&bar_vempty[st]);
         return true;
       };
-      bool ok = warp_wait(bar_q, 0, abort_flag, p.err, kErrTimeoutMma);
+      bool ok = warp_wait(bar_q, 0, abort_flag, p.err, p.wait_ns, kErrTimeoutMma);
       for (int j = 0; ok && j < nbp; ++j) {
         const int sk = j % L::kStagesK;
-        ok = warp_wait(&bar_kfull[sk], (j / L::kStagesK) & 1, abort_flag, p.err, kErrTimeoutMma);
+        ok = warp_wait(&bar_kfull[sk], (j / L::kStagesK) & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutMma);
         if (!ok) break;
         tc_fence_after();
         const bool q_in = j >= beg && j < nbt;              // S_t of loaded block j
@@ -400,7 +400,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     bool alive = true;
     for (int j = 0; j < nb && alive; ++j) {
       uint32_t sr[kBlockN];
-      if (!warp_wait(&bar_sfull[t], j & 1, abort_flag, p.err, kErrTimeoutSoftmax)) {
+      if (!warp_wait(&bar_sfull[t], j & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutSoftmax)) {
         alive = false;
         break;
       }
@@ -419,7 +419,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       // The two tiles' warps of one sub-partition take turns at the
       // exponentials, so one's loads, stores and waits overlap the other's.
       if (kTurns && (t == 0 ? j >= 1 && j - 1 < nb_other : j < nb_other) &&
-          !warp_wait(&bar_turn[t * 4 + q4], (t == 0 ? j - 1 : j) & 1, abort_flag, p.err, kErrTimeoutSoftmax)) {
+          !warp_wait(&bar_turn[t * 4 + q4], (t == 0 ? j - 1 : j) & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutSoftmax)) {
         alive = false;
         break;
       }
@@ -451,7 +451,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       // With separate P, P_t(j-1) V(j-1) must be done before P_t is rewritten
       // and before O_t is rescaled.  (With P over S, S_t(j) being ready already
       // implies it: its commit covers the earlier P V.)
-      if (L::kSepP && j > 0 && !warp_wait(&bar_pvdone[t], (j - 1) & 1, abort_flag, p.err, kErrTimeoutSoftmax)) {
+      if (L::kSepP && j > 0 && !warp_wait(&bar_pvdone[t], (j - 1) & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutSoftmax)) {
         alive = false;
         break;
       }
@@ -478,7 +478,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       warp_arrive(&bar_pfull[t]);
     }
     // ------------------------------------------------------------ epilogue
-    const bool have = alive && nb > 0 && warp_wait(&bar_ofinal[t], 0, abort_flag, p.err, kErrTimeoutSoftmax);
+    const bool have = alive && nb > 0 && warp_wait(&bar_ofinal[t], 0, abort_flag, p.err, p.wait_ns, kErrTimeoutSoftmax);
     if (GENERAL && p.o_part != nullptr) {
       // Split-KV partial of shard blockIdx.z: fp32 O / l and L into
       // [shard][B*H*S] rows; a row that sees no key of the shard gets O = 0,

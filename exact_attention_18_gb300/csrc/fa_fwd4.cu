@@ -227,7 +227,7 @@ __global__ void __launch_bounds__(kF4Threads, 1)
         for (; it < nbp; ++it) {
           const int st = it % L::kStages;
           const int use = it / L::kStages;
-          if (use > 0 && !mbar_wait(&bar_empty[st], (use - 1) & 1, abort_flag, p.err, kErrTimeoutLoad)) break;
+          if (use > 0 && !mbar_wait(&bar_empty[st], (use - 1) & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutLoad)) break;
           mbar_arrive_expect_tx(&bar_kfull[st], GK::kTileBytes);
           tma_rows(smem + L::kOffK + st * GK::kTileBytes, &tm_k, &bar_kfull[st], (kb_cta + it) * kBN, kvh);
           mbar_arrive_expect_tx(&bar_vfull[st], GK::kTileBytes);
@@ -279,8 +279,8 @@ __global__ void __launch_bounds__(kF4Threads, 1)
           mma_ts_warp(tmem + 128u * t + L::kColO, tmem + 128u * t + kk * 8,
                       desc_plus(v_desc, mnmajor_step_bytes<D>(kk)), idesc_pv, (jl > 0 || kk > 0) ? acc.on : acc.off);
       };
-      bool ok = warp_wait(bar_q, 0, abort_flag, p.err, kErrTimeoutMma);
-      if (ok && nbw > 0) ok = warp_wait(&bar_kfull[0], 0, abort_flag, p.err, kErrTimeoutMma);
+      bool ok = warp_wait(bar_q, 0, abort_flag, p.err, p.wait_ns, kErrTimeoutMma);
+      if (ok && nbw > 0) ok = warp_wait(&bar_kfull[0], 0, abort_flag, p.err, p.wait_ns, kErrTimeoutMma);
       if (ok) {
         tc_fence_after();
 #pragma unroll
@@ -294,10 +294,10 @@ __global__ void __launch_bounds__(kF4Threads, 1)
       int j = 0;
       for (; ok && j < nbw; ++j) {
         const int st = j % L::kStages;
-        ok = warp_wait(&bar_vfull[st], (j / L::kStages) & 1, abort_flag, p.err, kErrTimeoutMma);
+        ok = warp_wait(&bar_vfull[st], (j / L::kStages) & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutMma);
         // K(j+1) for the next score products (if a tile of this warp goes on).
         if (ok && j + 1 < nbw)
-          ok = warp_wait(&bar_kfull[(j + 1) % L::kStages], ((j + 1) / L::kStages) & 1, abort_flag, p.err,
+          ok = warp_wait(&bar_kfull[(j + 1) % L::kStages], ((j + 1) / L::kStages) & 1, abort_flag, p.err, p.wait_ns,
                          kErrTimeoutMma);
 #pragma unroll
         for (int h = 0; h < kF4TilesPerMma; ++h) {
@@ -315,7 +315,7 @@ __global__ void __launch_bounds__(kF4Threads, 1)
             }
           }
           const int jl = GENERAL ? j - beg[h] : j;
-          ok = warp_wait(&bar_pfull[t], jl & 1, abort_flag, p.err, kErrTimeoutMma);
+          ok = warp_wait(&bar_pfull[t], jl & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutMma);
           if (!ok) break;
           tc_fence_after();
           pv(t, j, jl);
@@ -332,8 +332,8 @@ __global__ void __launch_bounds__(kF4Threads, 1)
       // it has landed (so the arrival counts toward the right phase).
       for (; ok && j < nbp; ++j) {
         const int st = j % L::kStages;
-        ok = warp_wait(&bar_vfull[st], (j / L::kStages) & 1, abort_flag, p.err, kErrTimeoutMma) &&
-             warp_wait(&bar_kfull[st], (j / L::kStages) & 1, abort_flag, p.err, kErrTimeoutMma);
+        ok = warp_wait(&bar_vfull[st], (j / L::kStages) & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutMma) &&
+             warp_wait(&bar_kfull[st], (j / L::kStages) & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutMma);
         if (ok) mma_commit_warp(&bar_empty[st]);
       }
       // Teardown: wait for every MMA this warp issued.
@@ -363,7 +363,7 @@ __global__ void __launch_bounds__(kF4Threads, 1)
     float l = 0.f;
     bool alive = true;
     for (int j = 0; j < nb; ++j) {
-      if (!warp_wait(&bar_sfull[t], j & 1, abort_flag, p.err, kErrTimeoutSoftmax)) {
+      if (!warp_wait(&bar_sfull[t], j & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutSoftmax)) {
         alive = false;
         break;
       }
@@ -448,7 +448,7 @@ __global__ void __launch_bounds__(kF4Threads, 1)
       warp_arrive(&bar_pfull[t]);
     }
     // ------------------------------------------------------------ epilogue
-    const bool have = alive && nb > 0 && warp_wait(&bar_ofinal[t], 0, abort_flag, p.err, kErrTimeoutSoftmax);
+    const bool have = alive && nb > 0 && warp_wait(&bar_ofinal[t], 0, abort_flag, p.err, p.wait_ns, kErrTimeoutSoftmax);
     if (GENERAL && p.o_part != nullptr) {
       // Split-KV partial of shard blockIdx.z: fp32 O / l and L into
       // [shard][B*H*S] rows; a row that sees no key of the shard gets O = 0,

@@ -35,6 +35,7 @@ struct FwdParams {
   float* lse_part;     // split-KV: fp32 natural-log L of each shard, [shards][B*H*S]
   float scale_log2;    // scale * log2(e): scores enter exp2 in base 2
   int* err;            // device error word (set when a pipeline wait times out)
+  unsigned long long wait_ns;  // limit of each pipeline wait (fa_set_wait_limit_ns)
 };
 
 struct BwdParams {
@@ -61,6 +62,7 @@ struct BwdParams {
   float scale;         // softmax scale (dQ, dK factor)
   float scale_log2;    // scale * log2(e)
   int* err;            // device error word
+  unsigned long long wait_ns;  // limit of each pipeline wait (fa_set_wait_limit_ns)
 };
 
 // Tensor maps of the backward's four inputs, each viewed as 3-D {D, S, heads}
@@ -105,6 +107,9 @@ int bwd_kv_splits(int64_t BHkv, int64_t n_tiles, int group);
 
 // Address of this process's device error word on the current device.
 int* device_error_word();
+
+// Limit the kernels launched next give each pipeline wait (nanoseconds).
+unsigned long long wait_limit_ns();
 
 // Bytes per swizzled shared-memory row for head dimension D (16-bit elements):
 // 32 for D = 16, 64 for D = 32, 128 for D >= 64 (D = 128 uses two column chunks).

@@ -67,13 +67,16 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
 
 // All 32 lanes wait; the outcome is made warp-uniform (any failure = failure),
 // so the warp-collective tcgen05 loads and stores that follow never diverge.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* err, int code) {
-  const bool ok = ptx::mbar_wait(bar, parity, abort, err, code);
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* err,
+                                          unsigned long long limit_ns, int code) {
+  const bool ok = ptx::mbar_wait(bar, parity, abort, err, limit_ns, code);
   return __all_sync(0xffffffffu, ok);
 }
 
 // Bounded wait that ignores the abort flag: used at teardown for the CTA's
-// own copies and MMAs, which complete without help from other warps.
+// own copies and MMAs, which complete without help from other warps.  Its
+// limit is always kWaitLimitNs, whatever limit the pipeline waits have: the
+// CTA must not exit while a copy into its shared memory is still in flight.
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, int* err) {
   if (ptx::mbar_try_wait(bar, parity)) return;
   const unsigned long long t0 = ptx::globaltimer();

@@ -2,8 +2,9 @@
 // copies, and the tcgen05 tensor-core path (TMEM allocation, MMA, commit,
 // TMEM loads and stores, descriptors).
 //
-// Every wait in this file is bounded: it gives up after kWaitLimitNs of
-// wall time, records an error code in the library's device error word (whose
+// Every wait in this file is bounded: a pipeline wait gives up after the
+// limit its kernel was launched with (2 s unless the caller set another),
+// a teardown wait after kWaitLimitNs; either records an error code in the library's device error word (whose
 // address each kernel receives as a parameter) and returns false, so a kernel
 // whose pipeline stalls ends instead of hanging.
 #pragma once
@@ -27,6 +28,8 @@ enum DeviceErrorCode : int {
 
 namespace ptx {
 
+// Limit of the teardown waits (a CTA's own copies and MMAs), and the default
+// limit of the pipeline waits.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -72,6 +75,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking: whether the phase with the given parity has completed, now.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // As mbar_try_wait, but a thread whose phase is not complete is suspended
 // until it completes or `hint_ns` nanoseconds pass, so waiting warps do not
 // take issue slots from the warps they wait for.
@@ -89,17 +105,24 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
 
 constexpr uint32_t kSleepHintNs = 20000;  // 20 us per suspended try
 
+// Limits below this are test settings: such a wait polls without blocking
+// (mbarrier.try_wait may suspend the thread for a system-dependent time, and
+// a suspended try may outlast its hint, both longer than such a limit), so
+// that a phase that is not complete when the limit passes is noticed.
+constexpr unsigned long long kShortWaitLimitNs = 100000;  // 100 us
+
 // Wait until the phase with the given parity has completed.  Returns false
-// (after recording `code`) if that takes longer than kWaitLimitNs, or at once
+// (after recording `code`) if that takes longer than `limit_ns`, or at once
 // if another thread of the CTA has already given up (*abort != 0).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* err,
-                                          int code) {
-  if (mbar_try_wait(bar, parity)) return true;
+                                          unsigned long long limit_ns, int code) {
+  const bool poll = limit_ns < kShortWaitLimitNs;
+  if (poll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
   while (true) {
-    if (mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
+    if (poll ? mbar_test_wait(bar, parity) : mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
     if (*abort) return false;
-    if (globaltimer() - t0 > kWaitLimitNs) {
+    if (globaltimer() - t0 > limit_ns) {
       *abort = 1;
       record_error(err, code);
       return false;
@@ -136,30 +159,6 @@ __device__ __forceinline__ void cp_async_4(void* dst, const void* src, bool vali
 // landed; the arrival counts toward the barrier's expected count.
 __device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-// Multicast variant: the box lands at the same shared-memory offset in every
-// CTA of the cluster named in `cta_mask`, and each destination CTA's
-// mbarrier at `bar`'s offset receives the transaction bytes.
-__device__ __forceinline__ void tma_load_3d_multicast(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
-                                                      int z, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster "
-      "[%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "h"(cta_mask)
-      : "memory");
-}
-
-// ------------------------------------------------------------------ clusters
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-// All threads of every CTA in the cluster (a hardware barrier, like __syncthreads).
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // ------------------------------------------------------------------ tcgen05
@@ -233,16 +232,6 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
                : "memory");
 }
 
-// As mma_commit, arriving on the mbarrier at `bar`'s offset in every CTA of
-// the cluster named in `cta_mask`.
-__device__ __forceinline__ void mma_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          smem_u32(bar)),
-      "h"(cta_mask)
-      : "memory");
-}
-
 // Warp-collective issue variants: the whole warp executes the statement
 // (converged, so descriptors stay warp-uniform) and elect.sync lets exactly
 // one lane issue.  Issuing from converged code is what keeps the MMA issue
@@ -272,15 +261,6 @@ __device__ __forceinline__ void mma_commit_warp(uint64_t* bar) {
       "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
       : "memory");
 }
-__device__ __forceinline__ void mma_commit_multicast_warp(uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "{\n\t.reg .pred e;\n\t.reg .b32 r;\n\telect.sync r|e, 0xffffffff;\n\t"
-      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}" ::"r"(
-          smem_u32(bar)),
-      "h"(cta_mask)
-      : "memory");
-}
-
 // 32 lanes x 32 consecutive 32-bit columns; thread i of the warp receives lane
 // (warp's lane quarter base + i).  The wait is in the same statement, so the
 // registers are valid when the statement ends.

@@ -43,8 +43,9 @@
  *   and returns FA_OK or an fa_status code; nothing is launched on error.
  *   fa_last_error_detail() gives a one-line description of the last failure
  *   on the calling thread.  Kernels never trap: a device-side pipeline wait
- *   that exceeds its time limit (2 s) ends the kernel and sets a device error
- *   word that fa_check_device_errors() reads.
+ *   that exceeds its time limit (2 s by default, see fa_set_wait_limit_ns)
+ *   ends the kernel and sets a device error word that fa_check_device_errors()
+ *   reads.
  */
 #ifndef FA_GB300_H
 #define FA_GB300_H
@@ -317,6 +318,21 @@ const char* fa_last_error_detail(void);
  * tests and debugging; the compute entry points never synchronise.
  */
 fa_status fa_check_device_errors(void* stream);
+
+/*
+ * Sets the time limit, in nanoseconds, of every pipeline wait in the kernels
+ * launched after this call (a wait on a barrier that another warp of the same
+ * CTA completes: operands landed, scores computed, a stage freed).  0 restores
+ * the default of 2 s.  Returns the previous limit.  Process-wide, not tied to
+ * a stream or device.  A wait that runs past its limit makes its CTA stop
+ * early: it drains its own copies and MMAs (those waits keep the 2 s limit),
+ * frees its tensor memory and exits, and fa_check_device_errors() returns
+ * FA_ERR_TIMEOUT; the outputs of that call are then undefined.  A limit far
+ * below the kernels' own latencies (nanoseconds) makes that happen on purpose,
+ * which is how the tests exercise this path.  Not part of the pages' interface:
+ * failure handling for callers that must not hang.
+ */
+uint64_t fa_set_wait_limit_ns(uint64_t ns);
 
 #ifdef __cplusplus
 }

@@ -99,6 +99,11 @@ for _d in C3_D:
         CONFIGS[f"c3_d{_d}_s{_s}"] = Workload(
             f"c3_causal_fwdbwd_B8H1S{_s}D{_d}_bf16", 8, 1, _s, _d, "bf16", True, backward=True)
 
+# The leaderboard shape of "CS336 Assignment 2" §6 (causal forward + backward
+# at 16 heads, head dimension 64, sequence length 16384, bf16), batch 1.
+CONFIGS["leaderboard"] = Workload("leaderboard_causal_fwdbwd_B1H16S16384D64_bf16", 1, 16, 16384, 64, "bf16", True,
+                                  backward=True)
+
 # Grouped-query attention: the forward+backward of the causal B4 H16 S4096 D64
 # fp16 shape with 8 query heads per K/V head (H_kv = 2), and multi-query
 # attention (H_kv = 1) on the same shape.

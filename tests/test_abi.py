@@ -43,6 +43,16 @@ def test_status_strings(lib):
     assert fa.fa_status_string(99) == "FA_ERR_UNKNOWN"
 
 
+def test_wait_limit_setter_round_trip(lib):
+    """0 restores the 2 s default; the setter returns the limit it replaces (no launch involved)."""
+    old = fa.fa_set_wait_limit_ns(12345)
+    try:
+        assert fa.fa_set_wait_limit_ns(0) == 12345
+        assert fa.fa_set_wait_limit_ns(0) == 2_000_000_000
+    finally:
+        fa.fa_set_wait_limit_ns(old)
+
+
 def test_workspace_size(lib):
     assert fa.fa_bwd_workspace_size(2, 32, 8192, 128) == 2 * 32 * 8192 * 4
     assert fa.fa_bwd_workspace_size(1, 1, 3, 64) == 256  # rounded up to 256 bytes

@@ -1,5 +1,6 @@
 """Backward parity: the CUDA recompute backward (through the C ABI) against the
 fp64 oracle's closed-form gradients, on the library's own forward outputs."""
+import dataclasses
 import math
 
 import pytest
@@ -7,8 +8,8 @@ import torch
 
 import oracle
 from seeded_inputs import C3_D, C3_S, CONFIGS, Workload, make_inputs
-from tests.parity import (assert_close, assert_lse, check_backward_heads, check_forward_heads, run_backward,
-                          run_forward)
+from tests.parity import (assert_close, assert_lse, assert_within_bound, backward_rounding_bounds,
+                          check_backward_heads, check_forward_heads, run_backward, run_forward)
 
 pytestmark = pytest.mark.gpu
 
@@ -58,7 +59,7 @@ def test_config_c4_sampled_heads(fa):
     w = CONFIGS["c4"]
     inp = make_inputs(w)
     o, lse, grads = fwd_bwd(fa, w, inp)
-    heads = [(0, 0), (1, 31)]
+    heads = [(0, 0), (0, 17), (1, 5), (1, 31)]
     check_forward_heads(inp, o, lse, False, w.scale, heads, row_block=2048)
     check_backward_heads(inp, grads, False, w.scale, heads, row_block=2048)
 
@@ -67,27 +68,46 @@ def test_std2_variant(fa):
     """The other reading of "N(0, 2)": standard deviation 2, an extra stress case.
 
     The configured workload reads N(0, 2) as variance 2 and meets the absolute
-    bars.  With standard deviation 2 the forward still does (checked here), but
-    the backward's max-abs error is set by bf16 itself: the gradients reach
-    |6.6|, where one bf16 rounding alone costs up to 0.015, and an emulation of
-    the 16-bit pipeline on exact inputs (P and dS rounded to bf16 as MMA
-    operands, Delta taken from the bf16 output O) reaches 0.040 in dQ.  So the
-    backward is held to the stated mean-abs bar (2e-3) and to a norm-wise
-    relative error ||got - ref|| / ||ref|| <= 1e-2 (about 2.5 bf16 unit
-    roundoffs; the emulation gives 0.0037), both against the fp64 oracle.
+    bars.  With standard deviation 2 the forward still does (checked here),
+    but the exact gradients reach |6.6|, where one bf16 rounding of the
+    stored result alone costs up to 0.015: no backward that rounds P, dS and
+    its outputs to bf16 can meet 2e-2 max-abs there.  The backward is held,
+    element by element, to the first-order bound of its bf16 roundings
+    (tests.parity.backward_rounding_bounds, u = 2^-8), computed from the fp64
+    oracle's own P, dS and gradients, and to the stated 2e-3 mean bar.
     """
     w = Workload("c4_std2", 1, 2, 2048, 128, "bf16", False, qk_std=2.0, backward=True, seed=0)
     inp = make_inputs(w)
     o, lse, (dq, dk, dv) = fwd_bwd(fa, w, inp)
     check_forward_heads(inp, o, lse, False, w.scale, [(0, 0), (0, 1)])
     for h in (0, 1):
-        ref = oracle.backward(inp["q"][0, h], inp["k"][0, h], inp["v"][0, h], inp["do"][0, h], False, w.scale)
-        for name, got, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
-            d = got[0, h].double().cpu() - r
-            rel = float(d.norm() / r.norm())
-            mean = float(d.abs().mean())
-            assert rel <= 1e-2 and mean <= 2e-3, \
-                f"{name}[0,{h}]: relative error {rel:.2e}, mean abs {mean:.2e}, max abs {float(d.abs().max()):.2e}"
+        args = [inp[n][0, h] for n in ("q", "k", "v", "do")]
+        ref = oracle.backward(*args, False, w.scale)
+        bounds = backward_rounding_bounds(*args, False, w.scale, u=2.0 ** -8)
+        for name, got, r, bnd in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref, bounds):
+            assert_within_bound(f"{name}[0,{h}]", got[0, h], r, bnd)
+
+
+def test_config_c2_backward_sampled_heads(fa):
+    """The benchmark's own backward: causal B4 H16 S4096 D64 fp16, first, middle and last heads,
+    every row, at the stated bars."""
+    w = dataclasses.replace(CONFIGS["c2"], backward=True)
+    inp = make_inputs(w)
+    o, lse, grads = fwd_bwd(fa, w, inp)
+    heads = [(0, 0), (1, 7), (2, 12), (3, 15)]
+    check_forward_heads(inp, o, lse, True, w.scale, heads, row_block=1024)
+    check_backward_heads(inp, grads, True, w.scale, heads, row_block=1024)
+
+
+def test_leaderboard_workload_sampled_heads(fa):
+    """Causal B1 H16 S16384 D64 bf16 ("CS336 Assignment 2" §6 leaderboard shape): first,
+    a middle and the last head, every row, forward and backward, at the stated bars."""
+    w = CONFIGS["leaderboard"]
+    inp = make_inputs(w)
+    o, lse, grads = fwd_bwd(fa, w, inp)
+    heads = [(0, 0), (0, 9), (0, 15)]
+    check_forward_heads(inp, o, lse, True, w.scale, heads, row_block=2048)
+    check_backward_heads(inp, grads, True, w.scale, heads, row_block=2048)
 
 
 def test_zero_dout_rows_give_exact_zero_dk_dv(fa):
