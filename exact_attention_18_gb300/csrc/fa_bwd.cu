@@ -315,7 +315,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 4);
   float* vecs = reinterpret_cast<float*>(smem + L::kOffVec);
 
-  const int warp = threadIdx.x >> 5;
+  const int warp = warp_index();
   const int lane = threadIdx.x & 31;
   // Head of the CTA's own tiles: a K/V head in the dK/dV pass, a query head in
   // the dQ pass.  K/V head h serves query heads h*group .. h*group+group-1; in

@@ -123,7 +123,7 @@ __global__ void __launch_bounds__(kF4Threads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 4);
 
-  const int warp = threadIdx.x >> 5;
+  const int warp = warp_index();
   const int lane = threadIdx.x & 31;
   const int bh = blockIdx.x;
   // General instantiation: the sample of a packed batch (the layouts of
