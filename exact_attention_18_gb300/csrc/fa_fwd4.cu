@@ -74,12 +74,15 @@ constexpr uint32_t kF4RegsLow = kF4Threads == 640 ? 64 : 48;
 static_assert(512 * kF4RegsHigh + (kF4Threads - 512) * kF4RegsLow <= kF4Threads * kF4LaunchRegs, "register split");
 constexpr float kF4SumLimit = 256.0f;
 
-template <int D>
+template <int D, bool GENERAL>
 struct F4Layout {
   static_assert(D <= 64, "four-tile forward is for D <= 64");
   using GQ = TileGeom<D, 128>;
   using GK = TileGeom<D, kF4BlockN>;
-  static constexpr int kStages = D <= 32 ? 8 : 5;
+  // The general instantiation's tiles may run through blocks up to 6 apart
+  // (window bands of consecutive 128-row tiles start 2 blocks apart), so it
+  // keeps 8 stages in flight.
+  static constexpr int kStages = (D <= 32 || GENERAL) ? 8 : 5;
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kF4Tiles * GQ::kTileBytes;
   static constexpr int kOffV = kOffK + kStages * GK::kTileBytes;
@@ -103,7 +106,7 @@ template <int D, bool BF16, bool GENERAL>
 __global__ void __launch_bounds__(kF4Threads, 1)
     fa_fwd4_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
-  using L = F4Layout<D>;
+  using L = F4Layout<D, GENERAL>;
   using GQ = typename L::GQ;
   using GK = typename L::GK;
   using elem_t = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
@@ -279,62 +282,129 @@ __global__ void __launch_bounds__(kF4Threads, 1)
           mma_ts_warp(tmem + 128u * t + L::kColO, tmem + 128u * t + kk * 8,
                       desc_plus(v_desc, mnmajor_step_bytes<D>(kk)), idesc_pv, (jl > 0 || kk > 0) ? acc.on : acc.off);
       };
-      bool ok = warp_wait(bar_q, 0, abort_flag, p.err, p.wait_ns, kErrTimeoutMma);
-      if (ok && nbw > 0) ok = warp_wait(&bar_kfull[0], 0, abort_flag, p.err, p.wait_ns, kErrTimeoutMma);
-      if (ok) {
-        tc_fence_after();
+      if constexpr (GENERAL) {
+        // Each tile runs through its own blocks beg[h] .. nbt[h]-1 one step at a
+        // time, so under a window band (tiles' bands shifted by 128 rows) every
+        // tile is busy at every step instead of waiting while the CTA streams
+        // blocks outside its band.  The warp releases a block's stage after the
+        // last of its tiles to use it has issued its P V (a tile whose band
+        // starts earlier uses a block at a later step; at the same step, the
+        // tile issued last), and releases blocks neither tile uses once they
+        // have landed.
+        bool ok = warp_wait(bar_q, 0, abort_flag, p.err, p.wait_ns, kErrTimeoutMma);
+        int n[kF4TilesPerMma];
+        int nsteps = 0, lo_used = nbp, hi_used = 0;
 #pragma unroll
         for (int h = 0; h < kF4TilesPerMma; ++h) {
-          if (nbt[h] == 0 || beg[h] != 0) continue;
-          const int t = w * kF4TilesPerMma + h;
-          qk(t, 0);
-          mma_commit_warp(&bar_sfull[t]);
-        }
-      }
-      int j = 0;
-      for (; ok && j < nbw; ++j) {
-        const int st = j % L::kStages;
-        ok = warp_wait(&bar_vfull[st], (j / L::kStages) & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutMma);
-        // K(j+1) for the next score products (if a tile of this warp goes on).
-        if (ok && j + 1 < nbw)
-          ok = warp_wait(&bar_kfull[(j + 1) % L::kStages], ((j + 1) / L::kStages) & 1, abort_flag, p.err, p.wait_ns,
-                         kErrTimeoutMma);
-#pragma unroll
-        for (int h = 0; h < kF4TilesPerMma; ++h) {
-          if (!ok) break;
-          if (j >= nbt[h]) continue;
-          const int t = w * kF4TilesPerMma + h;
-          if constexpr (GENERAL) {
-            if (j < beg[h]) {  // the tile's band starts later: its first scores once K(beg) is in
-              if (j + 1 == beg[h]) {
-                tc_fence_after();
-                qk(t, j + 1);
-                mma_commit_warp(&bar_sfull[t]);
-              }
-              continue;
-            }
+          n[h] = nbt[h] - beg[h];
+          nsteps = max(nsteps, n[h]);
+          if (n[h] > 0) {
+            lo_used = min(lo_used, beg[h]);
+            hi_used = max(hi_used, nbt[h]);
           }
-          const int jl = GENERAL ? j - beg[h] : j;
-          ok = warp_wait(&bar_pfull[t], jl & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutMma);
+        }
+        if (hi_used == 0) lo_used = 0;
+        auto release_landed = [&](int x) {  // a block this warp does not use
+          const int sx = x % L::kStages;
+          ok = ok && warp_wait(&bar_vfull[sx], (x / L::kStages) & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutMma) &&
+               warp_wait(&bar_kfull[sx], (x / L::kStages) & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutMma);
+          if (ok) mma_commit_warp(&bar_empty[sx]);
+        };
+        for (int x = 0; ok && x < lo_used; ++x) release_landed(x);
+#pragma unroll
+        for (int h = 0; h < kF4TilesPerMma; ++h) {
+          if (!ok || n[h] <= 0) continue;
+          const int x = beg[h];
+          ok = warp_wait(&bar_kfull[x % L::kStages], (x / L::kStages) & 1, abort_flag, p.err, p.wait_ns,
+                         kErrTimeoutMma);
           if (!ok) break;
           tc_fence_after();
-          pv(t, j, jl);
-          if (j + 1 < nbt[h]) {
-            qk(t, j + 1);
-            mma_commit_warp(&bar_sfull[t]);
-          } else {
-            mma_commit_warp(&bar_ofinal[t]);
+          qk(w * kF4TilesPerMma + h, x);
+          mma_commit_warp(&bar_sfull[w * kF4TilesPerMma + h]);
+        }
+        for (int k = 0; ok && k < nsteps; ++k) {
+#pragma unroll
+          for (int h = 0; h < kF4TilesPerMma; ++h) {
+            if (!ok) break;
+            if (k >= n[h]) continue;
+            const int t = w * kF4TilesPerMma + h;
+            const int x = beg[h] + k;
+            ok = warp_wait(&bar_vfull[x % L::kStages], (x / L::kStages) & 1, abort_flag, p.err, p.wait_ns,
+                           kErrTimeoutMma);
+            if (ok && k + 1 < n[h])
+              ok = warp_wait(&bar_kfull[(x + 1) % L::kStages], ((x + 1) / L::kStages) & 1, abort_flag, p.err,
+                             p.wait_ns, kErrTimeoutMma);
+            ok = ok && warp_wait(&bar_pfull[t], k & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutMma);
+            if (!ok) break;
+            tc_fence_after();
+            pv(t, x, k);
+            if (k + 1 < n[h]) {
+              qk(t, x + 1);
+              mma_commit_warp(&bar_sfull[t]);
+            } else {
+              mma_commit_warp(&bar_ofinal[t]);
+            }
+            // The last of this warp's tiles to use block x releases it: a tile
+            // whose band starts earlier uses a block at a later step.
+            bool last_user = true;
+#pragma unroll
+            for (int e = 0; e < kF4TilesPerMma; ++e)
+              if (e != h && beg[e] <= x && x < nbt[e] && x - beg[e] > k) last_user = false;
+#pragma unroll
+            for (int e = h + 1; e < kF4TilesPerMma; ++e)  // same step: the tile issued last releases
+              if (beg[e] <= x && x < nbt[e] && x - beg[e] == k) last_user = false;
+            if (last_user) mma_commit_warp(&bar_empty[x % L::kStages]);
           }
         }
-        if (ok) mma_commit_warp(&bar_empty[st]);  // this warp's MMAs on K(j), V(j) are issued
-      }
-      // Blocks the CTA loads but no tile of this warp uses: release each once
-      // it has landed (so the arrival counts toward the right phase).
-      for (; ok && j < nbp; ++j) {
-        const int st = j % L::kStages;
-        ok = warp_wait(&bar_vfull[st], (j / L::kStages) & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutMma) &&
-             warp_wait(&bar_kfull[st], (j / L::kStages) & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutMma);
-        if (ok) mma_commit_warp(&bar_empty[st]);
+        for (int x = hi_used; ok && x < nbp; ++x) release_landed(x);
+      } else {
+        bool ok = warp_wait(bar_q, 0, abort_flag, p.err, p.wait_ns, kErrTimeoutMma);
+        if (ok && nbw > 0) ok = warp_wait(&bar_kfull[0], 0, abort_flag, p.err, p.wait_ns, kErrTimeoutMma);
+        if (ok) {
+          tc_fence_after();
+  #pragma unroll
+          for (int h = 0; h < kF4TilesPerMma; ++h) {
+            if (nbt[h] == 0) continue;
+            const int t = w * kF4TilesPerMma + h;
+            qk(t, 0);
+            mma_commit_warp(&bar_sfull[t]);
+          }
+        }
+        int j = 0;
+        for (; ok && j < nbw; ++j) {
+          const int st = j % L::kStages;
+          ok = warp_wait(&bar_vfull[st], (j / L::kStages) & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutMma);
+          // K(j+1) for the next score products (if a tile of this warp goes on).
+          if (ok && j + 1 < nbw)
+            ok = warp_wait(&bar_kfull[(j + 1) % L::kStages], ((j + 1) / L::kStages) & 1, abort_flag, p.err, p.wait_ns,
+                           kErrTimeoutMma);
+  #pragma unroll
+          for (int h = 0; h < kF4TilesPerMma; ++h) {
+            if (!ok) break;
+            if (j >= nbt[h]) continue;
+            const int t = w * kF4TilesPerMma + h;
+            const int jl = j;
+            ok = warp_wait(&bar_pfull[t], jl & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutMma);
+            if (!ok) break;
+            tc_fence_after();
+            pv(t, j, jl);
+            if (j + 1 < nbt[h]) {
+              qk(t, j + 1);
+              mma_commit_warp(&bar_sfull[t]);
+            } else {
+              mma_commit_warp(&bar_ofinal[t]);
+            }
+          }
+          if (ok) mma_commit_warp(&bar_empty[st]);  // this warp's MMAs on K(j), V(j) are issued
+        }
+        // Blocks the CTA loads but no tile of this warp uses: release each once
+        // it has landed (so the arrival counts toward the right phase).
+        for (; ok && j < nbp; ++j) {
+          const int st = j % L::kStages;
+          ok = warp_wait(&bar_vfull[st], (j / L::kStages) & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutMma) &&
+               warp_wait(&bar_kfull[st], (j / L::kStages) & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutMma);
+          if (ok) mma_commit_warp(&bar_empty[st]);
+        }
       }
       // Teardown: wait for every MMA this warp issued.
       mma_commit_warp(&bar_drain[w]);
@@ -503,7 +573,7 @@ namespace {
 template <int D, bool BF16, bool GENERAL>
 cudaError_t launch_fwd4_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
                           int BH, cudaStream_t stream) {
-  using L = F4Layout<D>;
+  using L = F4Layout<D, GENERAL>;
   auto kern = fa_fwd4_kernel<D, BF16, GENERAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
   if (e != cudaSuccess) return e;
