@@ -299,6 +299,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   using elem_t = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
   constexpr int kPN = kPartnerRows;
   constexpr float kLog2e = 1.4426950408889634f;
+  // Barrier tests before a wait blocks (mbar_wait): measured per pass at
+  // causal B4 H16 S4096 D64 and B2 H32 S8192 D128 (a blocking try returns
+  // some hundred cycles after the phase completes when the SM is busy): the
+  // MMA warps gain in both passes except the D = 128 dQ pass, the other
+  // waits only in the D <= 64 dK/dV pass; the dK/dV pass runs its tests
+  // unrolled, the dQ pass eight per loop iteration.
+  constexpr int kSpinMma = (D <= 64 || KV_OUTER) ? 64 : 0;
+  constexpr int kSpinOther = (D <= 64 && KV_OUTER) ? 64 : 0;
+  constexpr int kUnrollMma = (kSpinMma > 0 && KV_OUTER) ? kSpinMma : (kSpinMma > 0 ? 8 : 1);
+  constexpr int kUnrollOther = kSpinOther > 0 ? kSpinOther : 1;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -439,7 +449,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       const int st = it % L::kStages;
       const int use = it / L::kStages;
-      if (use > 0 && !warp_wait(&bar_empty[st], (use - 1) & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutLoad)) break;
+      if (use > 0 && !warp_wait<kSpinOther, kUnrollOther>(&bar_empty[st], (use - 1) & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutLoad)) break;
       const int r0 = pblk * kPN;
       if (lane == 0) {
         mbar_arrive_expect_tx(&bar_bfull[st], 2 * GB::kTileBytes);
@@ -505,9 +515,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int i = 0; ok && i < niter; ++i) {
         const int st = i % L::kStages;
         const int b = i % L::kXYBufs;
-        ok = warp_wait(&bar_bfull[st], (i / L::kStages) & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutMma);
+        ok = warp_wait<kSpinMma, kUnrollMma>(&bar_bfull[st], (i / L::kStages) & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutMma);
         if (ok && i >= L::kXYBufs)
-          ok = warp_wait(&bar_accissued[b], ((i / L::kXYBufs) - 1) & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutMma);
+          ok = warp_wait<kSpinMma, kUnrollMma>(&bar_accissued[b], ((i / L::kXYBufs) - 1) & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutMma);
         if (!ok) break;
         tc_fence_after();
         const uint32_t tb = tmem + 128u * b;
@@ -540,7 +550,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int x = 0; ok && x < niter; ++x) {
         const int st = x % L::kStages;
         const int b = x % L::kXYBufs;
-        ok = warp_wait(&bar_pfull[x & 1], (x >> 1) & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutMma);
+        ok = warp_wait<kSpinMma, kUnrollMma>(&bar_pfull[x & 1], (x >> 1) & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutMma);
         if (!ok) break;
         tc_fence_after();
         const uint32_t tb = tmem + 128u * b;
@@ -607,8 +617,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         while (pi >= nper) pi -= nper;
       }
       bool ok = true;
-      if constexpr (KV_OUTER) ok = warp_wait(&bar_bfull[st], (i / L::kStages) & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutSoftmax);
-      ok = ok && warp_wait(&bar_xyfull[i % L::kXYBufs], (i / L::kXYBufs) & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutSoftmax);
+      if constexpr (KV_OUTER) ok = warp_wait<kSpinOther, kUnrollOther>(&bar_bfull[st], (i / L::kStages) & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutSoftmax);
+      ok = ok && warp_wait<kSpinOther, kUnrollOther>(&bar_xyfull[i % L::kXYBufs], (i / L::kXYBufs) & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutSoftmax);
       if (!ok) {
         alive = false;
         break;
@@ -667,7 +677,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (lane == 0) mbar_arrive(&bar_pfull[g]);
     }
     // ------------------------------------------------------------ epilogue
-    const bool done = alive && mbar_wait(bar_accfinal, 0, abort_flag, p.err, p.wait_ns, kErrTimeoutSoftmax);
+    const bool done = alive && mbar_wait<kSpinOther, kUnrollOther>(bar_accfinal, 0, abort_flag, p.err, p.wait_ns, kErrTimeoutSoftmax);
     // The 16 warps split the accumulator columns of their 32 rows into up to
     // four parts of at least 16 columns.
     constexpr int kParts = D >= 64 ? 4 : D / 16;

@@ -79,9 +79,10 @@ __device__ __forceinline__ int warp_index() {
 
 // All 32 lanes wait; the outcome is made warp-uniform (any failure = failure),
 // so the warp-collective tcgen05 loads and stores that follow never diverge.
+template <int kSpin = 0, int kUnroll = 1>
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* err,
                                           unsigned long long limit_ns, int code) {
-  const bool ok = ptx::mbar_wait(bar, parity, abort, err, limit_ns, code);
+  const bool ok = ptx::mbar_wait<kSpin, kUnroll>(bar, parity, abort, err, limit_ns, code);
   return __all_sync(0xffffffffu, ok);
 }
 

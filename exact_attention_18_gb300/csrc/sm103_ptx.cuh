@@ -114,9 +114,17 @@ constexpr unsigned long long kShortWaitLimitNs = 100000;  // 100 us
 // Wait until the phase with the given parity has completed.  Returns false
 // (after recording `code`) if that takes longer than `limit_ns`, or at once
 // if another thread of the CTA has already given up (*abort != 0).
+// kSpin > 0: first test the phase up to kSpin times without blocking (a
+// blocking try returns some hundred cycles after the phase completes when the
+// SM sub-partition is busy), kUnroll tests per loop iteration.
+template <int kSpin = 0, int kUnroll = 1>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* err,
                                           unsigned long long limit_ns, int code) {
+  static_assert(kSpin % kUnroll == 0, "spin count");
   const bool poll = limit_ns < kShortWaitLimitNs;
+#pragma unroll kUnroll
+  for (int i = 0; i < kSpin; ++i)
+    if (mbar_test_wait(bar, parity)) return true;
   if (poll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
   while (true) {
