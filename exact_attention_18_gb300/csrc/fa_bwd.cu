@@ -128,6 +128,17 @@ constexpr int kProducerWarp = 8 * kBwdGroups;
 constexpr int kMmaWarp = kProducerWarp + 1;  // issues the score products X, Y
 constexpr int kAccWarp = kMmaWarp + 1;       // issues the accumulations
 constexpr int kBwdThreads = (kAccWarp + 1) * 32;
+// "P and dS of block i stored" barriers, block i on bar_pfull[i % 4] (8
+// arrivals, one per warp of group i % 2).  With three X/Y buffers a warp of a
+// group may finish block i and move on to the group's next block, i + 2,
+// before another warp of the group has finished block i: X, Y(i + 2) wait only
+// for the accumulation of block i - 1, the other group's.  With one barrier
+// per group the fast warp's next arrival would count toward block i's phase,
+// which could then complete before all of block i's P and dS are stored; with
+// two per group it lands on the other barrier.  No warp gets two blocks ahead:
+// X, Y(i + 4) wait for an accumulation issued after block i's, which waits
+// for all eight arrivals of block i.
+constexpr int kPFullBars = 2 * kBwdGroups;
 
 template <int D>
 struct BwdLayout {
@@ -145,8 +156,8 @@ struct BwdLayout {
   // X/Y buffers in TMEM (128 columns each): three when the accumulators
   // leave room (D <= 64), so the MMA warp can compute X, Y two blocks ahead.
   static constexpr int kXYBufs = D <= 64 ? 3 : 2;
-  // a_full, b_full[S], empty[S], xy_full[buffers], acc_issued[buffers], p_full[2], acc_final, drain[2]
-  static constexpr int kNumBars = 1 + 2 * kStages + 2 * kXYBufs + 2 + 1 + 2;
+  // a_full, b_full[S], empty[S], xy_full[buffers], acc_issued[buffers], p_full[4], acc_final, drain[2]
+  static constexpr int kNumBars = 1 + 2 * kStages + 2 * kXYBufs + kPFullBars + 1 + 2;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemUsed = kOffMisc + 16;
   static constexpr int kSmemBytes = (kSmemUsed + 1024) > 116 * 1024 ? (kSmemUsed + 1024) : 116 * 1024;
@@ -318,8 +329,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint64_t* bar_empty = bar_bfull + L::kStages;
   uint64_t* bar_xyfull = bar_empty + L::kStages;  // [buffers]
   uint64_t* bar_accissued = bar_xyfull + L::kXYBufs;  // [buffers] accumulation reading it issued
-  uint64_t* bar_pfull = bar_accissued + L::kXYBufs;     // [2] one per group
-  uint64_t* bar_accfinal = bar_pfull + 2;
+  uint64_t* bar_pfull = bar_accissued + L::kXYBufs;     // [4] block i's P, dS stored: bar_pfull[i % 4]
+  uint64_t* bar_accfinal = bar_pfull + kPFullBars;
   uint64_t* bar_drain = bar_accfinal + 1;               // [2] one per MMA warp
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 4);
@@ -397,8 +408,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(&bar_xyfull[b], 1);
       mbar_init(&bar_accissued[b], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&bar_pfull[b], 8);  // one arrival per warp of the group
+    for (int b = 0; b < kPFullBars; ++b) {
+      mbar_init(&bar_pfull[b], 8);  // one arrival per warp of the block's group
     }
     mbar_init(bar_accfinal, 1);
     mbar_init(&bar_drain[0], 1);
@@ -550,7 +561,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int x = 0; ok && x < niter; ++x) {
         const int st = x % L::kStages;
         const int b = x % L::kXYBufs;
-        ok = warp_wait<kSpinMma, kUnrollMma>(&bar_pfull[x & 1], (x >> 1) & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutMma);
+        ok = warp_wait<kSpinMma, kUnrollMma>(&bar_pfull[x % kPFullBars], (x / kPFullBars) & 1, abort_flag, p.err, p.wait_ns,
+                                             kErrTimeoutMma);
         if (!ok) break;
         tc_fence_after();
         const uint32_t tb = tmem + 128u * b;
@@ -674,7 +686,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_pfull[g]);
+      if (lane == 0) mbar_arrive(&bar_pfull[i % kPFullBars]);
     }
     // ------------------------------------------------------------ epilogue
     const bool done = alive && mbar_wait<kSpinOther, kUnrollOther>(bar_accfinal, 0, abort_flag, p.err, p.wait_ns, kErrTimeoutSoftmax);

@@ -50,7 +50,8 @@ def test_tensors_of_2_31_elements(fa, B, H, S, D):
     o, lse = fa.forward(q, k, v, causal=True, scale=scale)
     dq, dk, dv = fa.backward(q, k, v, o, do, lse, causal=True, scale=scale)
     torch.cuda.synchronize()
-    assert fa.fa_check_device_errors(None) == 0
+    st = fa.fa_check_device_errors(None)
+    assert st == 0, fa.fa_last_error_detail()
 
     # A zero head in the middle: the closed form, exactly for O and the gradients.
     zb, zh = B // 2, H // 2

@@ -1,0 +1,59 @@
+"""Repeated calls give the same bits.
+
+Every kernel of the library sums in a fixed order (no atomics, no split
+reductions whose order depends on timing), so calling the forward and the
+backward again on the same inputs must reproduce their outputs bit for bit.
+A race between the warps of a CTA (a barrier phase completing before all the
+data it guards is written, say) shows up here as a call whose results differ
+from the first call's, or as a device error; timing varies from call to call,
+so each case runs many times.  The first call is also checked against the
+fp64 oracle on sampled heads, so the repeated result is the right one.
+"""
+import pytest
+import torch
+
+import oracle
+from seeded_inputs import Workload, make_inputs
+from tests.parity import assert_close, assert_lse
+
+pytestmark = pytest.mark.gpu
+
+REPEATS = 30
+
+
+@pytest.fixture(scope="module")
+def fa():
+    import exact_attention_18_gb300 as m
+    m.load_library()
+    return m
+
+
+def _call(fa, w, q, k, v, do):
+    o, lse = fa.forward(q, k, v, causal=w.causal, scale=w.scale)
+    dq, dk, dv = fa.backward(q, k, v, o, do, lse, causal=w.causal, scale=w.scale)
+    st = fa.fa_check_device_errors(None)
+    assert st == 0, fa.fa_last_error_detail()
+    return o, lse, dq, dk, dv
+
+
+@pytest.mark.parametrize("D,dtype,causal", [(64, "fp16", True), (64, "bf16", False), (32, "fp16", True),
+                                            (128, "bf16", True)])
+def test_repeated_calls_are_bitwise_equal(fa, D, dtype, causal):
+    w = Workload("repeat", 4, 16, 2048, D, dtype, causal, backward=True, seed=77)
+    inp = make_inputs(w)
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+    first = _call(fa, w, q, k, v, do)
+    names = ("O", "L", "dQ", "dK", "dV")
+    for rep in range(REPEATS):
+        again = _call(fa, w, q, k, v, do)
+        for name, a, b in zip(names, first, again):
+            assert torch.equal(a, b), f"call {rep + 1}: {name} differs from the first call"
+    o, lse, dq, dk, dv = first
+    for b, h in ((0, 0), (w.B - 1, w.H - 1)):
+        args = [inp[n][b, h] for n in ("q", "k", "v", "do")]
+        o_ref, l_ref = oracle.forward(*args[:3], causal, w.scale)
+        assert_close(f"O[{b},{h}]", o[b, h], o_ref)
+        assert_lse(lse[b, h], l_ref)
+        g_ref = oracle.backward(*args, causal, w.scale)
+        for name, got, ref in zip(("dQ", "dK", "dV"), (dq[b, h], dk[b, h], dv[b, h]), g_ref):
+            assert_close(f"{name}[{b},{h}]", got, ref)
