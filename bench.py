@@ -368,7 +368,8 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-heads", type=int, default=16, help="heads in the CPU oracle baseline sample")
+    ap.add_argument("--cpu-heads", type=int, default=48,
+                    help="heads in the CPU oracle baseline sample (48 of c2's 64: about 10-15 s of CPU work)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-table", action="store_true",
