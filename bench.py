@@ -51,6 +51,7 @@ _COMMON = [_CSRC + f for f in ("fa_kernel_common.cuh", "sm103_ptx.cuh", "fa_inte
 # these are unchanged since its capture.
 KERNEL_SOURCES = {
     "fa_fwd4_kernel": [_CSRC + "fa_fwd4.cu", _CSRC + "fa_softmax.cuh"] + _COMMON,
+    "fa_fwd4p_kernel": [_CSRC + "fa_fwd4p.cu", _CSRC + "fa_softmax.cuh"] + _COMMON,
     "fa_fwd_kernel": [_CSRC + "fa_fwd.cu", _CSRC + "fa_softmax.cuh"] + _COMMON,
     "fa_bwd_preprocess_kernel": [_CSRC + "fa_bwd.cu"] + _COMMON,
     "fa_bwd_dkdv_kernel": [_CSRC + "fa_bwd.cu"] + _COMMON,
@@ -104,17 +105,26 @@ def conv_flops(w):
     return f, 2.5 * f
 
 
-def fwd_kernel_name(w):
-    """The forward kernel the library launches for this head dimension."""
-    return "fa_fwd4_kernel" if w.D <= 64 else "fa_fwd_kernel"
+PERSISTENT_MAX_S = 6144  # the library's switch between its two D <= 64 forward kernels
 
 
-def kernel_work(w):
+def fwd_kernel_name(w, general=False):
+    """The forward kernel the library launches for this workload: at D <= 64 the persistent
+    two-pipeline kernel for fixed-length sequences of up to 6144 rows, the four-tile kernel for
+    longer ones and for packed batches, windows and split-KV (``general``)."""
+    if w.D > 64:
+        return "fa_fwd_kernel"
+    if general or is_packed(w) or getattr(w, "window", None) is not None or w.S > PERSISTENT_MAX_S:
+        return "fa_fwd4_kernel"
+    return "fa_fwd4p_kernel"
+
+
+def kernel_work(w, general=False):
     """Algorithmic work per launch of each kernel (FLOPs of its tensor-core GEMMs, or HBM bytes)."""
     units = pairs(w) * w.D
     rows = sum(n for _, _, n in head_list(w))
     return {
-        fwd_kernel_name(w): ("tensor", 4.0 * units),        # S = QK^T, O += PV
+        fwd_kernel_name(w, general): ("tensor", 4.0 * units),        # S = QK^T, O += PV
         "fa_bwd_preprocess_kernel": ("hbm", rows * w.D * 2 * 2 + rows * 4),  # read O, dO; write Delta
         "fa_bwd_dkdv_kernel": ("tensor", 8.0 * units),       # S^T, dP^T, dV, dK
         "fa_bwd_dq_kernel": ("tensor", 6.0 * units),         # S, dP, dQ
@@ -504,7 +514,7 @@ def main():
     if fa.fa_check_device_errors(sp) != 0:
         raise RuntimeError("device error during the timed steps: " + fa.fa_last_error_detail())
 
-    names = [fwd_kernel_name(w), "fa_bwd_preprocess_kernel", "fa_bwd_dkdv_kernel", "fa_bwd_dq_kernel"]
+    names = [fwd_kernel_name(w, n_split > 0), "fa_bwd_preprocess_kernel", "fa_bwd_dkdv_kernel", "fa_bwd_dq_kernel"]
     per = {n: [] for n in names}
     step_ms = []
     for e in evs:
@@ -537,7 +547,7 @@ def main():
                 ts.append((e0, e1))
         torch.cuda.synchronize()
         unsplit = {"ms": statistics.mean(a.elapsed_time(b) for a, b in ts), "shards": n_split}
-    work = kernel_work(w)
+    work = kernel_work(w, n_split > 0)
     avg = {n: statistics.mean(per[n]) for n in names}
     dom = max(names, key=lambda n: avg[n])
     kind, amount = work[dom]

@@ -20,7 +20,7 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB_DIR = os.path.join(PKG, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libfa_gb300.so")
 
-SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_fwd4.cu", "fa_bwd.cu", "fa_merge.cu"]
+SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_fwd4.cu", "fa_fwd4p.cu", "fa_bwd.cu", "fa_merge.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE,
                  "-diag-suppress", "177"]

@@ -38,6 +38,9 @@
 // element-wise mask runs only on the two blocks that cross the diagonal and
 // on a ragged last block ("fa-triton" §Causal Mask 的处理：off-band 与 on-band).
 //
+// Fixed-length calls of up to 6144 rows run the persistent two-pipeline
+// kernel of fa_fwd4p.cu instead, whose fixed cost per 256 rows is lower.
+//
 // GENERAL = true is the instantiation for packed variable-length batches and
 // sliding windows ("Inside FlashAttention" §6.1): the CTA finds its sample
 // from cu_seqlens, reads rows through {D, heads, T} tensor maps, and a tile
@@ -73,6 +76,10 @@ constexpr uint32_t kF4RegsHigh = kF4Threads == 640 ? 104 : 96;
 constexpr uint32_t kF4RegsLow = kF4Threads == 640 ? 64 : 48;
 static_assert(512 * kF4RegsHigh + (kF4Threads - 512) * kF4RegsLow <= kF4Threads * kF4LaunchRegs, "register split");
 constexpr float kF4SumLimit = 256.0f;
+// Measured causal fp16 D = 64 forwards (us), persistent two-pipeline kernel / this one:
+// S 1024 (B8 H16) 35.5 / 37.5, S 2048 (B4 H16) 46.3 / 50.9, S 4096 (B4 H16) 128.7 / 133.8,
+// S 8192 (B2 H16) 232.0 / 226.5, S 16384 (B1 H16) 437 / 422.6.
+constexpr int kPersistentMaxS = 6144;
 
 template <int D, bool GENERAL>
 struct F4Layout {
@@ -595,6 +602,10 @@ int fwd_rows_per_cta(int D) { return D <= 64 ? kF4RowsPerCta : 2 * kBlockM; }
 
 cudaError_t launch_fwd4(int D, bool bf16, bool general, const CUtensorMap& tq, const CUtensorMap& tk,
                         const CUtensorMap& tv, const FwdParams& p, int BH, cudaStream_t stream) {
+  // Fixed-length sequences up to kPersistentMaxS rows run the persistent
+  // two-pipeline kernel (fa_fwd4p.cu), whose lower fixed cost per 256 rows
+  // pays off there; longer ones this kernel, whose per-block cost is lower.
+  if (!general && p.S <= kPersistentMaxS) return launch_fwd4p(D, bf16, tq, tk, tv, p, BH, stream);
 #define FA_FWD4_CASE(DD)                                                                       \
   case DD:                                                                                     \
     if (general)                                                                               \

@@ -79,10 +79,13 @@ int fwd_rows_per_cta(int D);
 // Launchers (one per kernel family); they dispatch on D and dtype, and take
 // the general instantiation (packed batches, windows) when `general` is set;
 // the fixed-length full/causal calls run the specialised one.
-// launch_fwd4: the four-tile forward for D <= 64; launch_fwd: any D (passes
-// D <= 64 on to launch_fwd4).
+// launch_fwd4: the forward for D <= 64 (the persistent two-pipeline kernel,
+// launch_fwd4p, for fixed-length calls; the four-tile kernel for the general
+// ones); launch_fwd: any D (passes D <= 64 on to launch_fwd4).
 cudaError_t launch_fwd4(int D, bool bf16, bool general, const CUtensorMap& tq, const CUtensorMap& tk,
                         const CUtensorMap& tv, const FwdParams& p, int BH, cudaStream_t stream);
+cudaError_t launch_fwd4p(int D, bool bf16, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                         const FwdParams& p, int BH, cudaStream_t stream);
 cudaError_t launch_fwd(int D, bool bf16, bool general, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const FwdParams& p, int BH, cudaStream_t stream);
 

@@ -53,7 +53,10 @@ def test_window_flops_count_visible_pairs():
 
 
 def test_kernel_work_names_the_launched_forward():
-    assert "fa_fwd4_kernel" in bench.kernel_work(CONFIGS["c2"])
+    assert "fa_fwd4p_kernel" in bench.kernel_work(CONFIGS["c2"])           # fixed length, S <= 6144
+    assert "fa_fwd4_kernel" in bench.kernel_work(CONFIGS["leaderboard"])   # S = 16384
+    assert "fa_fwd4_kernel" in bench.kernel_work(CONFIGS["window"])        # a window band
+    assert "fa_fwd4_kernel" in bench.kernel_work(CONFIGS["c2"], general=True)  # split-KV
     assert "fa_fwd_kernel" in bench.kernel_work(CONFIGS["c4"])
     kind, amount = bench.kernel_work(CONFIGS["c2"])["fa_bwd_dkdv_kernel"]
     assert kind == "tensor" and amount == 2 * bench.conv_flops(CONFIGS["c2"])[0]
@@ -66,10 +69,11 @@ def test_traffic_is_dropped_when_the_kernel_sources_change(monkeypatch):
     assert bench.load_traffic("c2") == {k: r["bytes"] for k, r in table.items()}
     assert bench.load_traffic("no-such-workload") == {}
     # A change to one kernel's sources drops that kernel's figure only.
+    fwd = next(k for k in table if k.startswith("fa_fwd"))
     monkeypatch.setattr(bench, "sources_digest",
-                        lambda k: "0000000000000000" if k == "fa_fwd4_kernel" else table[k]["sources_digest"])
+                        lambda k: "0000000000000000" if k == fwd else table[k]["sources_digest"])
     got = bench.load_traffic("c2")
-    assert "fa_fwd4_kernel" not in got and got["fa_bwd_dkdv_kernel"] == table["fa_bwd_dkdv_kernel"]["bytes"]
+    assert fwd not in got and got["fa_bwd_dkdv_kernel"] == table["fa_bwd_dkdv_kernel"]["bytes"]
 
 
 def test_every_kernel_lists_existing_sources():

@@ -31,6 +31,28 @@ def test_small_shapes(fa, D, dtype, causal, S):
     assert_lse(lse, l_ref)
 
 
+@pytest.mark.parametrize("D", [32, 64])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("S", [6144, 6208])
+def test_both_d64_forward_kernels_at_their_switch(fa, D, causal, S):
+    """At D <= 64 fixed-length calls of up to 6144 rows run the persistent two-pipeline kernel,
+    longer ones the four-tile kernel: both sides of the switch, every row of two heads (one with
+    a ragged last item or tile)."""
+    w = Workload("switch", 1, 2, S, D, "bf16", causal, seed=S + D + causal)
+    inp = make_inputs(w)
+    q, k, v, o, lse = run_forward(fa, inp, causal, w.scale)
+    check_forward_heads(inp, o, lse, causal, w.scale, [(0, 0), (0, 1)], row_block=2048)
+
+
+def test_many_items_per_pipeline(fa):
+    """More 256-row items than pipelines several times over (B16 H16 S1024: 1024 items), so every
+    pipeline runs several items and carries its barrier phases across them."""
+    w = Workload("items", 16, 16, 1024, 64, "fp16", True, seed=5)
+    inp = make_inputs(w)
+    q, k, v, o, lse = run_forward(fa, inp, True, w.scale)
+    check_forward_heads(inp, o, lse, True, w.scale, [(0, 0), (7, 3), (15, 15)])
+
+
 def test_config_c1_full(fa):
     w = CONFIGS["c1"]
     inp = make_inputs(w)

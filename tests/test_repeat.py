@@ -13,7 +13,7 @@ import pytest
 import torch
 
 import oracle
-from seeded_inputs import Workload, make_inputs
+from seeded_inputs import PACKED_CONFIGS, Workload, make_inputs, make_packed_inputs
 from tests.parity import assert_close, assert_lse
 
 pytestmark = pytest.mark.gpu
@@ -57,3 +57,45 @@ def test_repeated_calls_are_bitwise_equal(fa, D, dtype, causal):
         g_ref = oracle.backward(*args, causal, w.scale)
         for name, got, ref in zip(("dQ", "dK", "dV"), (dq[b, h], dk[b, h], dv[b, h]), g_ref):
             assert_close(f"{name}[{b},{h}]", got, ref)
+
+
+def _same(first, again, names, rep):
+    for name, a, b in zip(names, first, again):
+        assert torch.equal(a, b), f"call {rep + 1}: {name} differs from the first call"
+
+
+@pytest.mark.parametrize("path", ["gqa", "window", "varlen"])
+def test_repeated_calls_of_the_other_paths(fa, path):
+    """The grouped-query, window and packed-batch entry points (their own tests cover parity)."""
+    names = ("O", "L", "dQ", "dK", "dV")
+    if path == "varlen":
+        w = PACKED_CONFIGS["varlen"]
+        inp = make_packed_inputs(w)
+        q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+        cu = inp["cu_seqlens"].cuda()
+
+        def call():
+            o, lse = fa.forward_varlen(q, k, v, cu, w.max_seqlen, causal=w.causal, scale=w.scale)
+            g = fa.backward_varlen(q, k, v, o, do, lse, cu, w.max_seqlen, causal=w.causal, scale=w.scale)
+            st = fa.fa_check_device_errors(None)
+            assert st == 0, fa.fa_last_error_detail()
+            return (o, lse, *g)
+    else:
+        if path == "gqa":
+            w = Workload("repeat_gqa", 2, 16, 2048, 64, "bf16", True, backward=True, seed=78, H_kv=4)
+            window = None
+        else:
+            w = Workload("repeat_window", 2, 8, 2048, 64, "fp16", True, backward=True, seed=79, window=(512, 0))
+            window = w.window
+        inp = make_inputs(w)
+        q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+
+        def call():
+            o, lse = fa.forward(q, k, v, causal=w.causal, scale=w.scale, window=window)
+            g = fa.backward(q, k, v, o, do, lse, causal=w.causal, scale=w.scale, window=window)
+            st = fa.fa_check_device_errors(None)
+            assert st == 0, fa.fa_last_error_detail()
+            return (o, lse, *g)
+    first = call()
+    for rep in range(REPEATS):
+        _same(first, call(), names, rep)
