@@ -156,8 +156,9 @@ struct BwdLayout {
   // X/Y buffers in TMEM (128 columns each): three when the accumulators
   // leave room (D <= 64), so the MMA warp can compute X, Y two blocks ahead.
   static constexpr int kXYBufs = D <= 64 ? 3 : 2;
-  // a_full, b_full[S], empty[S], xy_full[buffers], acc_issued[buffers], p_full[4], acc_final, drain[2]
-  static constexpr int kNumBars = 1 + 2 * kStages + 2 * kXYBufs + kPFullBars + 1 + 2;
+  // a_full, b_full[S], empty[S], xy_full[buffers], acc_issued[buffers], p_full[4], acc_final, drain[2],
+  // then (persistent kernel only) a_empty, acc_free.
+  static constexpr int kNumBars = 1 + 2 * kStages + 2 * kXYBufs + kPFullBars + 1 + 2 + 2;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemUsed = kOffMisc + 16;
   static constexpr int kSmemBytes = (kSmemUsed + 1024) > 116 * 1024 ? (kSmemUsed + 1024) : 116 * 1024;
@@ -751,6 +752,349 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
+
+// Persistent version of the dQ pass for fixed-length calls at D <= 64: a grid
+// of at most one CTA per SM, each running the pipeline of fa_bwd_main_kernel
+// (roles, TMEM layout, barriers; Q and dO copied into TMEM) over a sequence of
+// the non-persistent grid's query tiles ("work items", in that grid's launch
+// order: heaviest first under the causal mask), dealt to the CTAs in a snake
+// (round r gives item r*P + c to CTA c when r is even and r*P + P-1-c when it
+// is odd, P CTAs).  Between items nothing drains: the producer loads the next
+// item's first key blocks, then its Q and dO tiles as soon as the current
+// item's copies of them into TMEM are done (a_empty); the score-product warp
+// computes the next item's first X, Y while the softmax-gradient warps store
+// the current item's dQ; the accumulation warp starts the next item's dQ once
+// those stores have read it out of TMEM (acc_free).  Barrier phases run on
+// across items: key stages, X/Y buffers and the "P stored" barriers by a
+// running block count, the tile and accumulator barriers by item.  (The same
+// scheme for the dK/dV pass measured slower on long rows: causal B1 H16
+// S16384 D64 840 against 732 us.)
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    fa_bwd_dqp_kernel(const __grid_constant__ CUtensorMap tm_a1, const __grid_constant__ CUtensorMap tm_a2,
+                      const __grid_constant__ CUtensorMap tm_b1, const __grid_constant__ CUtensorMap tm_b2,
+                      const BwdParams p, int n_items) {
+  using L = BwdLayout<D>;
+  static_assert(D <= 64 && L::kTmemA, "persistent dQ pass: D <= 64, Q and dO in TMEM");
+  using GA = typename L::GA;
+  using GB = typename L::GB;
+  using elem_t = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+  constexpr int kPN = kPartnerRows;
+  constexpr float kLog2e = 1.4426950408889634f;
+  constexpr int kS = L::kStages;
+  constexpr int kB = L::kXYBufs;
+  // Barrier tests before blocking as in fa_bwd_main_kernel's dQ pass at D <= 64.
+  constexpr int kSpinMma = 64;
+  constexpr int kUnrollMma = 8;
+  constexpr int kPreBlocks = 4;  // key blocks of the next item loaded before its Q, dO tiles
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
+  uint64_t* bar_afull = bars;
+  uint64_t* bar_bfull = bars + 1;
+  uint64_t* bar_empty = bar_bfull + kS;
+  uint64_t* bar_xyfull = bar_empty + kS;         // [buffers]
+  uint64_t* bar_accissued = bar_xyfull + kB;     // [buffers] accumulation reading it issued
+  uint64_t* bar_pfull = bar_accissued + kB;      // [4] block i's dS stored: bar_pfull[i % 4]
+  uint64_t* bar_accfinal = bar_pfull + kPFullBars;
+  uint64_t* bar_drain = bar_accfinal + 1;        // [2] one per MMA warp
+  uint64_t* bar_aempty = bar_drain + 2;          // the item's Q, dO copies into TMEM done
+  uint64_t* bar_accfree = bar_aempty + 1;        // the item's dQ read out by all 16 warps
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 4);
+
+  const int warp = warp_index();
+  const int lane = threadIdx.x & 31;
+  const int S = p.S;
+  const int nt = p.n_tiles;
+  const int np = (S + kPN - 1) / kPN;
+  const int gx = p.BH;
+  const int P = static_cast<int>(gridDim.x);
+  const int c = static_cast<int>(blockIdx.x);
+  auto item_at = [&](int r) -> int {
+    const int k = r * P + ((r & 1) ? (P - 1 - c) : c);
+    return k < n_items ? k : -1;
+  };
+  // One work item: query head bh, its 128-row tile at own0, key blocks 0 .. nb-1.
+  struct Item {
+    int bh, kvh, own0, nb;
+  };
+  auto decode = [&](int k) -> Item {
+    int cx, cy;
+    if (p.causal) {  // x fastest: every head's heaviest tile first
+      cy = k / gx;
+      cx = k - cy * gx;
+    } else {         // y fastest: one head's tiles in a row
+      cx = k / nt;
+      cy = k - cx * nt;
+    }
+    Item it;
+    it.bh = cx;
+    it.kvh = cx / p.group;
+    it.own0 = (p.causal ? nt - 1 - cy : cy) * 128;
+    it.nb = p.causal ? min(np, (it.own0 + 127) / kPN + 1) : np;
+    return it;
+  };
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_afull, 1);
+    for (int s = 0; s < kS; ++s) {
+      mbar_init(&bar_bfull[s], 1);
+      mbar_init(&bar_empty[s], 1);
+    }
+    for (int b = 0; b < kB; ++b) {
+      mbar_init(&bar_xyfull[b], 1);
+      mbar_init(&bar_accissued[b], 1);
+    }
+    for (int b = 0; b < kPFullBars; ++b) mbar_init(&bar_pfull[b], 8);
+    mbar_init(bar_accfinal, 1);
+    mbar_init(&bar_drain[0], 1);
+    mbar_init(&bar_drain[1], 1);
+    mbar_init(bar_aempty, 1);
+    mbar_init(bar_accfree, 16);  // one arrival per softmax-gradient warp
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(tmem_slot, L::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t sA1 = smem_u32(smem + L::kOffA1);
+  const uint32_t sA2 = smem_u32(smem + L::kOffA2);
+  const uint32_t sB1 = smem_u32(smem + L::kOffB1);
+  const uint32_t sB2 = smem_u32(smem + L::kOffB2);
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer (lane 0)
+    if (lane == 0) {
+      prefetch_tmap(&tm_a1);
+      prefetch_tmap(&tm_a2);
+      prefetch_tmap(&tm_b1);
+      prefetch_tmap(&tm_b2);
+      bool ok = true;
+      int it = 0;  // key blocks loaded so far
+      int n = 0;   // items whose Q, dO tiles were loaded
+      for (int r = 0; ok; ++r) {
+        const int k = item_at(r);
+        if (k < 0) break;
+        const Item w = decode(k);
+        auto load_block = [&](int x) -> bool {
+          const int st = it % kS;
+          const int use = it / kS;
+          if (use > 0 && !mbar_wait(&bar_empty[st], (use - 1) & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutLoad))
+            return false;
+          mbar_arrive_expect_tx(&bar_bfull[st], 2 * GB::kTileBytes);
+#pragma unroll
+          for (int ch = 0; ch < GB::kChunks; ++ch) {
+            tma_load_3d(smem + L::kOffB1 + st * GB::kTileBytes + ch * GB::kChunkBytes, &tm_b1, &bar_bfull[st],
+                        ch * (GB::kRowBytes / 2), x * kPN, w.kvh);
+            tma_load_3d(smem + L::kOffB2 + st * GB::kTileBytes + ch * GB::kChunkBytes, &tm_b2, &bar_bfull[st],
+                        ch * (GB::kRowBytes / 2), x * kPN, w.kvh);
+          }
+          ++it;
+          return true;
+        };
+        const int pre = min(w.nb, kPreBlocks);
+        for (int x = 0; ok && x < pre; ++x) ok = load_block(x);
+        // Q and dO, once the previous item's copies of them into TMEM are done.
+        if (ok && n > 0) ok = mbar_wait(bar_aempty, (n - 1) & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutLoad);
+        if (!ok) break;
+        mbar_arrive_expect_tx(bar_afull, 2 * GA::kTileBytes);
+#pragma unroll
+        for (int ch = 0; ch < GA::kChunks; ++ch) {
+          tma_load_3d(smem + L::kOffA1 + ch * GA::kChunkBytes, &tm_a1, bar_afull, ch * (GA::kRowBytes / 2), w.own0,
+                      w.bh);
+          tma_load_3d(smem + L::kOffA2 + ch * GA::kChunkBytes, &tm_a2, bar_afull, ch * (GA::kRowBytes / 2), w.own0,
+                      w.bh);
+        }
+        ++n;
+        for (int x = pre; ok && x < w.nb; ++x) ok = load_block(x);
+      }
+      // Teardown: every copy issued must land before the CTA exits.
+      if (n > 0) drain_wait(bar_afull, (n - 1) & 1, p.err);
+      for (int x = (it > kS ? it - kS : 0); x < it; ++x) drain_wait(&bar_bfull[x % kS], (x / kS) & 1, p.err);
+    }
+  } else if (warp == kMmaWarp || warp == kAccWarp) {
+    // ------------------------------------------------------------ MMA issuers
+    constexpr uint32_t idesc_xy = make_idesc_f16(BF16, 128, kPN, false, false);
+    constexpr uint32_t idesc_acc = make_idesc_f16(BF16, 128, D, false, true);
+    const AccFlags accf = runtime_flags(S);
+    bool ok = true;
+    int i0 = 0;  // key blocks of the earlier items
+    int n = 0;   // items
+    if (warp == kMmaWarp) {
+      const uint64_t a1_desc = make_sdesc(sA1, 16, 8 * GA::kRowBytes, GA::kSwz);
+      const uint64_t a2_desc = make_sdesc(sA2, 16, 8 * GA::kRowBytes, GA::kSwz);
+      for (int r = 0; ok; ++r) {
+        const int k = item_at(r);
+        if (k < 0) break;
+        const Item w = decode(k);
+        ok = warp_wait(bar_afull, n & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutMma);
+        if (!ok) break;
+        // Q and dO into TMEM (after the previous item's score products, which
+        // read the columns they overwrite: the tensor core runs them in order).
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          tmem_cp_128x256b_warp(tmem + L::kColA1 + 8 * kk, desc_plus(a1_desc, kmajor_step_bytes<D, 128>(kk)));
+          tmem_cp_128x256b_warp(tmem + L::kColA2 + 8 * kk, desc_plus(a2_desc, kmajor_step_bytes<D, 128>(kk)));
+        }
+        mma_commit_warp(bar_aempty);  // the shared-memory Q, dO are free once the copies land
+        for (int x = 0; ok && x < w.nb; ++x) {
+          const int i = i0 + x;
+          const int st = i % kS;
+          const int b = i % kB;
+          ok = warp_wait<kSpinMma, kUnrollMma>(&bar_bfull[st], (i / kS) & 1, abort_flag, p.err, p.wait_ns,
+                                               kErrTimeoutMma);
+          if (ok && i >= kB)
+            ok = warp_wait<kSpinMma, kUnrollMma>(&bar_accissued[b], ((i / kB) - 1) & 1, abort_flag, p.err,
+                                                 p.wait_ns, kErrTimeoutMma);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t tb = tmem + 128u * b;
+          const uint64_t b1 = make_sdesc(sB1 + st * GB::kTileBytes, 16, 8 * GB::kRowBytes, GB::kSwz);
+          const uint64_t b2 = make_sdesc(sB2 + st * GB::kTileBytes, 16, 8 * GB::kRowBytes, GB::kSwz);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)  // X = S = Q K_j^T
+            mma_ts_warp(tb, tmem + L::kColA1 + 8 * kk, desc_plus(b1, kmajor_step_bytes<D, kPN>(kk)), idesc_xy,
+                        kk > 0 ? accf.on : accf.off);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)  // Y = dP = dO V_j^T
+            mma_ts_warp(tb + 64, tmem + L::kColA2 + 8 * kk, desc_plus(b2, kmajor_step_bytes<D, kPN>(kk)), idesc_xy,
+                        kk > 0 ? accf.on : accf.off);
+          mma_commit_warp(&bar_xyfull[b]);
+        }
+        i0 += w.nb;
+        ++n;
+      }
+      mma_commit_warp(&bar_drain[0]);
+      drain_wait(&bar_drain[0], 0, p.err);
+    } else {
+      for (int r = 0; ok; ++r) {
+        const int k = item_at(r);
+        if (k < 0) break;
+        const Item w = decode(k);
+        for (int x = 0; ok && x < w.nb; ++x) {
+          const int i = i0 + x;
+          const int st = i % kS;
+          const int b = i % kB;
+          ok = warp_wait<kSpinMma, kUnrollMma>(&bar_pfull[i % kPFullBars], (i / kPFullBars) & 1, abort_flag, p.err,
+                                               p.wait_ns, kErrTimeoutMma);
+          // The item's first accumulation overwrites dQ: the previous item's
+          // must have been read out.
+          if (ok && x == 0 && n > 0)
+            ok = warp_wait(bar_accfree, (n - 1) & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutMma);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t tb = tmem + 128u * b;
+          const uint64_t b1 = make_sdesc(sB1 + st * GB::kTileBytes, GB::kChunkBytes, 8 * GB::kRowBytes, GB::kSwz);
+#pragma unroll
+          for (int kk = 0; kk < kPN / 16; ++kk)  // dQ += dS K_j
+            mma_ts_warp(tmem + L::kColAcc1, tb + 64 + packed_col(kk), desc_plus(b1, mnmajor_step_bytes<D>(kk)),
+                        idesc_acc, (x > 0 || kk > 0) ? accf.on : accf.off);
+          mma_commit_warp(&bar_empty[st]);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar_accissued[b]);
+        }
+        if (!ok) break;
+        mma_commit_warp(bar_accfinal);  // the item's dQ is complete once this lands
+        i0 += w.nb;
+        ++n;
+      }
+      mma_commit_warp(&bar_drain[1]);
+      drain_wait(&bar_drain[1], 0, p.err);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax-gradient warps 0-15
+    const int g = warp >> 3;
+    const int q4 = warp & 3;
+    const int hf = (warp >> 2) & 1;
+    const int col0 = 32 * hf;
+    const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
+    const float sl2 = p.scale_log2;
+    const float2 c2 = make_float2(sl2, sl2);
+    constexpr int kParts = D >= 64 ? 4 : D / 16;
+    constexpr int kEpiCols = D / kParts;
+    const int col_part = warp >> 2;
+    bool alive = true;
+    int i0 = 0;
+    int n = 0;
+    for (int r = 0; alive; ++r) {
+      const int k = item_at(r);
+      if (k < 0) break;
+      const Item w = decode(k);
+      const int my = w.own0 + q4 * 32 + lane;  // this thread's query
+      const int64_t rowbase = static_cast<int64_t>(w.bh) * S;
+      // This row's L2 = L * log2 e and Delta (rows past S: L2 = +inf, so P = 0 exactly).
+      float my_l2 = INFINITY, my_delta = 0.f;
+      if (my < S) {
+        my_l2 = p.lse[rowbase + my] * kLog2e;
+        my_delta = p.delta[rowbase + my];
+      }
+      // This group's blocks of the item: global block indices i0 + x with (i0 + x) % 2 == g.
+      for (int x = (g - i0) & 1; x < w.nb; x += kBwdGroups) {
+        const int i = i0 + x;
+        const int partner0 = x * kPN;
+        if (!warp_wait(&bar_xyfull[i % kB], (i / kB) & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutSoftmax)) {
+          alive = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t tX = tmem + lane_base + 128u * (i % kB) + col0;
+        const uint32_t tY = tX + 64;
+        const int lim = my - partner0 - col0;
+        if (p.causal && partner0 + kPN - 1 > w.own0)  // the diagonal blocks: keys after the query masked
+          grad_block<BF16, false, true>(tX, tY, nullptr, nullptr, c2, my_l2, my_delta, lim);
+        else
+          grad_block<BF16, false, false>(tX, tY, nullptr, nullptr, c2, my_l2, my_delta, lim);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_pfull[i % kPFullBars]);
+      }
+      if (!alive) break;
+      // ---------------------------------------------------------- epilogue of the item
+      if (!warp_wait(bar_accfinal, n & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutSoftmax)) {
+        alive = false;
+        break;
+      }
+      tc_fence_after();
+      if (col_part < kParts) {
+        const int c_begin = col_part * kEpiCols;
+        const bool row_ok = my < S;
+        const size_t off = static_cast<size_t>(rowbase + (row_ok ? my : 0)) * D;
+        const uint32_t t_acc = tmem + lane_base;
+        elem_t* dq_row = reinterpret_cast<elem_t*>(p.dq) + off;
+#pragma unroll
+        for (int cc = c_begin; cc < c_begin + kEpiCols; cc += 16) {
+          uint32_t v16[16];
+          tmem_ld16(t_acc + L::kColAcc1 + cc, v16);
+          if (row_ok) store_row16<BF16>(dq_row + cc, v16, p.scale);
+        }
+      }
+      // dQ is read: the next item's accumulation may overwrite it.
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_accfree);
+      i0 += w.nb;
+      ++n;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, L::kTmemCols);
+  }
+}
+
 namespace {
 
 template <int D, bool BF16>
@@ -773,6 +1117,46 @@ cudaError_t launch_main_t(const CUtensorMap& a1, const CUtensorMap& a2, const CU
   dim3 grid(KV_OUTER ? p.BH / p.group * p.kv_splits : p.BH, p.n_tiles);
   kern<<<grid, kBwdThreads, L::kSmemBytes, stream>>>(a1, a2, b1, b2, p);
   return cudaGetLastError();
+}
+
+int bwd_sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+      n = v;
+    if (n <= 0) n = 1;
+  }
+  return n;
+}
+
+template <int D, bool BF16>
+cudaError_t launch_dq_persistent_t(const CUtensorMap& a1, const CUtensorMap& a2, const CUtensorMap& b1,
+                                   const CUtensorMap& b2, const BwdParams& p, cudaStream_t stream) {
+  using L = BwdLayout<D>;
+  auto kern = fa_bwd_dqp_kernel<D, BF16>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  // Work items: the query tiles of the non-persistent grid (B*H x n_tiles).
+  const int64_t n_items = static_cast<int64_t>(p.BH) * p.n_tiles;
+  if (n_items <= 0) return cudaSuccess;
+  if (n_items > (1LL << 30)) return cudaErrorInvalidValue;
+  const int grid = static_cast<int>(n_items < bwd_sm_count() ? n_items : bwd_sm_count());
+  kern<<<grid, kBwdThreads, L::kSmemBytes, stream>>>(a1, a2, b1, b2, p, static_cast<int>(n_items));
+  return cudaGetLastError();
+}
+
+// The dQ pass: the persistent kernel for fixed-length calls at D <= 64 (measured at causal
+// B4 H16 S4096 D64 185 -> 165 us, B1 H16 S16384 D64 547 -> 538 us); at D = 128 the per-tile
+// grid (the persistent kernel was as fast at B2 H32 S8192, 1.6 % slower at B1 H8 S32768).
+template <int D, bool BF16>
+cudaError_t launch_dq_t(bool general, const BwdMaps& m, const BwdParams& p, cudaStream_t stream) {
+  if (general) return launch_main_t<D, BF16, false, true>(m.q128, m.do128, m.k64, m.v64, p, stream);
+  if constexpr (D <= 64)
+    return launch_dq_persistent_t<D, BF16>(m.q128, m.do128, m.k64, m.v64, p, stream);
+  else
+    return launch_main_t<D, BF16, false, false>(m.q128, m.do128, m.k64, m.v64, p, stream);
 }
 
 template <int D, bool BF16>
@@ -826,9 +1210,7 @@ cudaError_t launch_bwd_dkv_reduce(int D, bool bf16, const BwdParams& p, int64_t 
 
 cudaError_t launch_bwd_dq(int D, bool bf16, bool general, const BwdMaps& m, const BwdParams& p,
                           cudaStream_t stream) {
-#define FA_DQ(DD, BB)                                                                         \
-  (general ? launch_main_t<DD, BB, false, true>(m.q128, m.do128, m.k64, m.v64, p, stream)     \
-           : launch_main_t<DD, BB, false, false>(m.q128, m.do128, m.k64, m.v64, p, stream))
+#define FA_DQ(DD, BB) launch_dq_t<DD, BB>(general, m, p, stream)
   FA_BWD_DISPATCH(FA_DQ)
 #undef FA_DQ
 }
