@@ -1095,6 +1095,404 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
+// Persistent version of the dK/dV pass for fixed-length calls at D <= 64 with
+// at most 32 partner blocks per work item on average (launch_dkdv_t decides):
+// a grid of at most one CTA per SM, each running the pipeline of
+// fa_bwd_main_kernel over a sequence of the per-tile grid's key tiles (work
+// items, in that grid's launch order, dealt in a snake as in the persistent
+// dQ pass).  Between items: the producer loads the next item's first partner
+// blocks, then its K and V tiles as soon as the current item's last score
+// products have read them (a_empty); the accumulation warp starts the next
+// item's dV, dK once all 16 softmax-gradient warps have read the current ones
+// out of TMEM (acc_free).  The per-block steps run slower inside this
+// kernel's item loops than in the per-tile kernel, so it pays only while the
+// per-item overlap outweighs that: measured (whole backward, causal fp16 D64)
+// B8 H16 S1024 111 -> 101 us, B4 H16 S2048 147 -> 139 us, B4 H16 S4096 417 ->
+// 411 us, but B2 H16 S8192 703 -> 724 us and grouped K/V heads at S4096
+// (hpc 2 or 4 query heads per item) 5-7 % slower.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    fa_bwd_dkdvp_kernel(const __grid_constant__ CUtensorMap tm_a1, const __grid_constant__ CUtensorMap tm_a2,
+                        const __grid_constant__ CUtensorMap tm_b1, const __grid_constant__ CUtensorMap tm_b2,
+                        const BwdParams p, int gx, int n_items) {
+  using L = BwdLayout<D>;
+  static_assert(D <= 64, "persistent dK/dV pass: D <= 64");
+  using GA = typename L::GA;
+  using GB = typename L::GB;
+  using elem_t = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+  constexpr int kPN = kPartnerRows;
+  constexpr int kS = L::kStages;
+  constexpr int kB = L::kXYBufs;
+  // Barrier tests before blocking as in fa_bwd_main_kernel's dK/dV pass, but
+  // not unrolled: this kernel's longer code ran faster with the small loops
+  // (c2 242 -> 234 us).
+  constexpr int kSpinMma = 64;
+  constexpr int kSpinOther = 64;
+  constexpr int kUnrollMma = 1;
+  constexpr int kUnrollOther = 1;
+  constexpr int kPreBlocks = 4;  // partner blocks of the next item loaded before its resident tiles
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
+  uint64_t* bar_afull = bars;
+  uint64_t* bar_bfull = bars + 1;
+  uint64_t* bar_empty = bar_bfull + kS;
+  uint64_t* bar_xyfull = bar_empty + kS;         // [buffers]
+  uint64_t* bar_accissued = bar_xyfull + kB;     // [buffers] accumulation reading it issued
+  uint64_t* bar_pfull = bar_accissued + kB;      // [4] block i's P, dS stored: bar_pfull[i % 4]
+  uint64_t* bar_accfinal = bar_pfull + kPFullBars;
+  uint64_t* bar_drain = bar_accfinal + 1;        // [2] one per MMA warp
+  uint64_t* bar_aempty = bar_drain + 2;          // the item's last score products (last reads of A1, A2) done
+  uint64_t* bar_accfree = bar_aempty + 1;        // the item's accumulators read out by all 16 warps
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 4);
+  float* vecs = reinterpret_cast<float*>(smem + L::kOffVec);
+
+  const int warp = warp_index();
+  const int lane = threadIdx.x & 31;
+  const int S = p.S;
+  const int nt = p.n_tiles;
+  const int np = (S + kPN - 1) / kPN;
+  const int hpc = p.group / p.kv_splits;  // query heads per CTA share of a K/V head
+  const int gy = nt;
+  const int P = static_cast<int>(gridDim.x);
+  const int c = static_cast<int>(blockIdx.x);
+  auto item_at = [&](int r) -> int {
+    const int k = r * P + ((r & 1) ? (P - 1 - c) : c);
+    return k < n_items ? k : -1;
+  };
+  // One work item: the tile the non-persistent grid's CTA number k took.
+  struct Item {
+    int bh, kv_part, pz0, own0, first, nper, niter;
+  };
+  auto decode = [&](int k) -> Item {
+    int cx, cy;
+    if (p.causal) {  // x fastest: every head's heaviest tile first
+      cy = k / gx;
+      cx = k - cy * gx;
+    } else {         // y fastest: one head's tiles in a row
+      cx = k / gy;
+      cy = k - cx * gy;
+    }
+    Item it;
+    it.bh = cx / p.kv_splits;  // K/V head
+    it.kv_part = cx - it.bh * p.kv_splits;
+    it.pz0 = it.bh * p.group + it.kv_part * hpc;  // first partner (query) head
+    it.own0 = cy * 128;
+    it.first = p.causal ? it.own0 / kPN : 0;
+    it.nper = np - it.first;
+    it.niter = hpc * it.nper;
+    return it;
+  };
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_afull, 1);
+    for (int s = 0; s < kS; ++s) {
+      mbar_init(&bar_bfull[s], 33);  // the TMA arrival + one cp.async arrival per producer lane
+      mbar_init(&bar_empty[s], 1);
+    }
+    for (int b = 0; b < kB; ++b) {
+      mbar_init(&bar_xyfull[b], 1);
+      mbar_init(&bar_accissued[b], 1);
+    }
+    for (int b = 0; b < kPFullBars; ++b) mbar_init(&bar_pfull[b], 8);
+    mbar_init(bar_accfinal, 1);
+    mbar_init(&bar_drain[0], 1);
+    mbar_init(&bar_drain[1], 1);
+    mbar_init(bar_aempty, 1);
+    mbar_init(bar_accfree, 16);  // one arrival per softmax-gradient warp
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(tmem_slot, L::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t sA1 = smem_u32(smem + L::kOffA1);
+  const uint32_t sA2 = smem_u32(smem + L::kOffA2);
+  const uint32_t sB1 = smem_u32(smem + L::kOffB1);
+  const uint32_t sB2 = smem_u32(smem + L::kOffB2);
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&tm_a1);
+      prefetch_tmap(&tm_a2);
+      prefetch_tmap(&tm_b1);
+      prefetch_tmap(&tm_b2);
+    }
+    bool ok = true;
+    int it = 0;  // partner blocks loaded so far
+    int n = 0;   // items whose resident tiles were loaded
+    for (int r = 0; ok; ++r) {
+      const int k = item_at(r);
+      if (k < 0) break;
+      const Item w = decode(k);
+      // Partner head and block of the next block to load, stepped without divisions.
+      int pz = w.pz0, pblk = w.first;
+      auto load_block = [&](int) -> bool {
+        const int st = it % kS;
+        const int use = it / kS;
+        if (use > 0 && !warp_wait<kSpinOther, kUnrollOther>(&bar_empty[st], (use - 1) & 1, abort_flag, p.err,
+                                                             p.wait_ns, kErrTimeoutLoad))
+          return false;
+        const int r0 = pblk * kPN;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bar_bfull[st], 2 * GB::kTileBytes);
+#pragma unroll
+          for (int ch = 0; ch < GB::kChunks; ++ch) {
+            tma_load_3d(smem + L::kOffB1 + st * GB::kTileBytes + ch * GB::kChunkBytes, &tm_b1, &bar_bfull[st],
+                        ch * (GB::kRowBytes / 2), r0, pz);
+            tma_load_3d(smem + L::kOffB2 + st * GB::kTileBytes + ch * GB::kChunkBytes, &tm_b2, &bar_bfull[st],
+                        ch * (GB::kRowBytes / 2), r0, pz);
+          }
+        }
+        // The block's L and Delta (partner queries past S read 0: their Q and
+        // dO rows are zero-filled, so P dO and dS vanish there).
+        float* v = vecs + st * 2 * kPN;
+#pragma unroll
+        for (int h = 0; h < kPN; h += 32) {
+          const int q = r0 + h + lane;
+          const int64_t src = static_cast<int64_t>(pz) * S + (q < S ? q : S - 1);
+          cp_async_4(v + h + lane, p.lse + src, q < S);
+          cp_async_4(v + kPN + h + lane, p.delta + src, q < S);
+        }
+        cp_async_mbar_arrive(&bar_bfull[st]);
+        if (++pblk == w.first + w.nper) {
+          pblk = w.first;
+          ++pz;
+        }
+        ++it;
+        return true;
+      };
+      const int pre = min(w.niter, kPreBlocks);
+      for (int x = 0; ok && x < pre; ++x) ok = load_block(x);
+      // The resident tiles, once the previous item's score products have read them.
+      if (ok && n > 0)
+        ok = warp_wait(bar_aempty, (n - 1) & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutLoad);
+      if (!ok) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar_afull, 2 * GA::kTileBytes);
+#pragma unroll
+        for (int ch = 0; ch < GA::kChunks; ++ch) {
+          tma_load_3d(smem + L::kOffA1 + ch * GA::kChunkBytes, &tm_a1, bar_afull, ch * (GA::kRowBytes / 2), w.own0,
+                      w.bh);
+          tma_load_3d(smem + L::kOffA2 + ch * GA::kChunkBytes, &tm_a2, bar_afull, ch * (GA::kRowBytes / 2), w.own0,
+                      w.bh);
+        }
+      }
+      ++n;
+      for (int x = pre; ok && x < w.niter; ++x) ok = load_block(x);
+    }
+    // Teardown: every copy issued must land before the CTA exits.
+    if (lane == 0 && n > 0) drain_wait(bar_afull, (n - 1) & 1, p.err);
+    for (int x = (it > kS ? it - kS : 0); x < it; ++x) drain_wait(&bar_bfull[x % kS], (x / kS) & 1, p.err);
+  } else if (warp == kMmaWarp || warp == kAccWarp) {
+    // ------------------------------------------------------------ MMA issuers
+    constexpr uint32_t idesc_xy = make_idesc_f16(BF16, 128, kPN, false, false);
+    constexpr uint32_t idesc_acc = make_idesc_f16(BF16, 128, D, false, true);
+    const AccFlags accf = runtime_flags(S);
+    bool ok = true;
+    int i0 = 0;  // partner blocks of the earlier items
+    int n = 0;   // items
+    if (warp == kMmaWarp) {
+      const uint64_t a1_desc = make_sdesc(sA1, 16, 8 * GA::kRowBytes, GA::kSwz);
+      const uint64_t a2_desc = make_sdesc(sA2, 16, 8 * GA::kRowBytes, GA::kSwz);
+      for (int r = 0; ok; ++r) {
+        const int k = item_at(r);
+        if (k < 0) break;
+        const Item w = decode(k);
+        ok = warp_wait(bar_afull, n & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutMma);
+        if (!ok) break;
+        for (int x = 0; ok && x < w.niter; ++x) {
+          const int i = i0 + x;
+          const int st = i % kS;
+          const int b = i % kB;
+          ok = warp_wait<kSpinMma, kUnrollMma>(&bar_bfull[st], (i / kS) & 1, abort_flag, p.err, p.wait_ns,
+                                               kErrTimeoutMma);
+          if (ok && i >= kB)
+            ok = warp_wait<kSpinMma, kUnrollMma>(&bar_accissued[b], ((i / kB) - 1) & 1, abort_flag, p.err,
+                                                 p.wait_ns, kErrTimeoutMma);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t tb = tmem + 128u * b;
+          const uint64_t b1 = make_sdesc(sB1 + st * GB::kTileBytes, 16, 8 * GB::kRowBytes, GB::kSwz);
+          const uint64_t b2 = make_sdesc(sB2 + st * GB::kTileBytes, 16, 8 * GB::kRowBytes, GB::kSwz);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)  // X = S^T = K Q_i^T
+            mma_ss_warp(tb, desc_plus(a1_desc, kmajor_step_bytes<D, 128>(kk)),
+                        desc_plus(b1, kmajor_step_bytes<D, kPN>(kk)), idesc_xy, kk > 0 ? accf.on : accf.off);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)  // Y = dP^T = V dO_i^T
+            mma_ss_warp(tb + 64, desc_plus(a2_desc, kmajor_step_bytes<D, 128>(kk)),
+                        desc_plus(b2, kmajor_step_bytes<D, kPN>(kk)), idesc_xy, kk > 0 ? accf.on : accf.off);
+          mma_commit_warp(&bar_xyfull[b]);
+        }
+        if (!ok) break;
+        mma_commit_warp(bar_aempty);  // the item's last reads of A1, A2 are issued
+        i0 += w.niter;
+        ++n;
+      }
+      mma_commit_warp(&bar_drain[0]);
+      drain_wait(&bar_drain[0], 0, p.err);
+    } else {
+      for (int r = 0; ok; ++r) {
+        const int k = item_at(r);
+        if (k < 0) break;
+        const Item w = decode(k);
+        for (int x = 0; ok && x < w.niter; ++x) {
+          const int i = i0 + x;
+          const int st = i % kS;
+          const int b = i % kB;
+          ok = warp_wait<kSpinMma, kUnrollMma>(&bar_pfull[i % kPFullBars], (i / kPFullBars) & 1, abort_flag, p.err,
+                                               p.wait_ns, kErrTimeoutMma);
+          // The item's first accumulation overwrites the accumulators: the
+          // previous item's must have been read out.
+          if (ok && x == 0 && n > 0)
+            ok = warp_wait(bar_accfree, (n - 1) & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutMma);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t tb = tmem + 128u * b;
+          const uint64_t b1 = make_sdesc(sB1 + st * GB::kTileBytes, GB::kChunkBytes, 8 * GB::kRowBytes, GB::kSwz);
+          const uint64_t b2 = make_sdesc(sB2 + st * GB::kTileBytes, GB::kChunkBytes, 8 * GB::kRowBytes, GB::kSwz);
+#pragma unroll
+          for (int kk = 0; kk < kPN / 16; ++kk)  // dV += P^T dO_i
+            mma_ts_warp(tmem + L::kColAcc1, tb + packed_col(kk), desc_plus(b2, mnmajor_step_bytes<D>(kk)), idesc_acc,
+                        (x > 0 || kk > 0) ? accf.on : accf.off);
+#pragma unroll
+          for (int kk = 0; kk < kPN / 16; ++kk)  // dK += dS^T Q_i
+            mma_ts_warp(tmem + L::kColAcc2, tb + 64 + packed_col(kk), desc_plus(b1, mnmajor_step_bytes<D>(kk)),
+                        idesc_acc, (x > 0 || kk > 0) ? accf.on : accf.off);
+          mma_commit_warp(&bar_empty[st]);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar_accissued[b]);
+        }
+        if (!ok) break;
+        mma_commit_warp(bar_accfinal);  // the item's accumulators are complete once this lands
+        i0 += w.niter;
+        ++n;
+      }
+      mma_commit_warp(&bar_drain[1]);
+      drain_wait(&bar_drain[1], 0, p.err);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax-gradient warps 0-15
+    const int g = warp >> 3;
+    const int q4 = warp & 3;
+    const int hf = (warp >> 2) & 1;
+    const int col0 = 32 * hf;
+    const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
+    const float sl2 = p.scale_log2;
+    const float2 c2 = make_float2(sl2, sl2);
+    constexpr int kParts = D >= 64 ? 4 : D / 16;
+    constexpr int kEpiCols = D / kParts;
+    const int col_part = warp >> 2;
+    bool alive = true;
+    int i0 = 0;
+    int n = 0;
+    for (int r = 0; alive; ++r) {
+      const int k = item_at(r);
+      if (k < 0) break;
+      const Item w = decode(k);
+      const int my = w.own0 + q4 * 32 + lane;  // this thread's key
+      const int64_t rowbase = static_cast<int64_t>(w.bh) * S;
+      // This group's blocks of the item: global block indices i0 + x with (i0 + x) % 2 == g.
+      const int x0 = (g - i0) & 1;
+      int pi = x0;  // x modulo nper (the partner block within its head), stepped without divisions
+      if (pi >= w.nper) pi -= w.nper;
+      for (int x = x0; x < w.niter; x += kBwdGroups) {
+        const int i = i0 + x;
+        const int st = i % kS;
+        const int partner0 = (w.first + pi) * kPN;
+        pi += kBwdGroups;
+        while (pi >= w.nper) pi -= w.nper;
+        bool ok = warp_wait<kSpinOther, kUnrollOther>(&bar_bfull[st], (i / kS) & 1, abort_flag, p.err, p.wait_ns,
+                                                      kErrTimeoutSoftmax);
+        ok = ok && warp_wait<kSpinOther, kUnrollOther>(&bar_xyfull[i % kB], (i / kB) & 1, abort_flag, p.err,
+                                                       p.wait_ns, kErrTimeoutSoftmax);
+        if (!ok) {
+          alive = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t tX = tmem + lane_base + 128u * (i % kB) + col0;
+        const uint32_t tY = tX + 64;
+        const float* lv = vecs + st * 2 * kPN + col0;
+        const float* dv = lv + kPN;
+        // Diagonal blocks: partner queries before this key are masked.
+        const int lim0 = w.own0 + q4 * 32 - partner0 - col0;
+        if (p.causal && partner0 < w.own0 + 128)
+          grad_block_kv<BF16, true>(tX, tY, lv, dv, c2, lim0);
+        else
+          grad_block_kv<BF16, false>(tX, tY, lv, dv, c2, lim0);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_pfull[i % kPFullBars]);
+      }
+      if (!alive) break;
+      // ---------------------------------------------------------- epilogue of the item
+      if (!warp_wait<kSpinOther, kUnrollOther>(bar_accfinal, n & 1, abort_flag, p.err, p.wait_ns,
+                                               kErrTimeoutSoftmax)) {
+        alive = false;
+        break;
+      }
+      tc_fence_after();
+      if (col_part < kParts) {
+        const int c_begin = col_part * kEpiCols;
+        const bool row_ok = my < S;
+        const int64_t orow = rowbase + (row_ok ? my : 0);
+        const size_t off = static_cast<size_t>(orow) * D;
+        const uint32_t t_acc = tmem + lane_base;
+        if (p.kv_splits == 1) {
+          elem_t* dv_row = reinterpret_cast<elem_t*>(p.dv) + off;
+          elem_t* dk_row = reinterpret_cast<elem_t*>(p.dk) + off;
+#pragma unroll
+          for (int cc = c_begin; cc < c_begin + kEpiCols; cc += 16) {
+            uint32_t v16[16];
+            tmem_ld16(t_acc + L::kColAcc1 + cc, v16);
+            if (row_ok) store_row16<BF16>(dv_row + cc, v16, 1.f);
+            tmem_ld16(t_acc + L::kColAcc2 + cc, v16);
+            if (row_ok) store_row16<BF16>(dk_row + cc, v16, p.scale);
+          }
+        } else {
+          // This CTA's share of the group: fp32 rows [dV | scale * dK] of partial kv_part.
+          const int64_t n_rows = static_cast<int64_t>(p.BH / p.group) * S;
+          float* prow = p.dkv_part + ((static_cast<int64_t>(w.kv_part) * n_rows + orow) * (2 * D));
+#pragma unroll
+          for (int cc = c_begin; cc < c_begin + kEpiCols; cc += 16) {
+            uint32_t v16[16];
+            tmem_ld16(t_acc + L::kColAcc1 + cc, v16);
+            if (row_ok) store_row16_f32(prow + cc, v16, 1.f);
+            tmem_ld16(t_acc + L::kColAcc2 + cc, v16);
+            if (row_ok) store_row16_f32(prow + D + cc, v16, p.scale);
+          }
+        }
+      }
+      // The accumulators are read: the next item's accumulation may overwrite them.
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_accfree);
+      i0 += w.niter;
+      ++n;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, L::kTmemCols);
+  }
+}
+
+
 namespace {
 
 template <int D, bool BF16>
@@ -1160,6 +1558,37 @@ cudaError_t launch_dq_t(bool general, const BwdMaps& m, const BwdParams& p, cuda
 }
 
 template <int D, bool BF16>
+cudaError_t launch_dkdv_persistent_t(const CUtensorMap& a1, const CUtensorMap& a2, const CUtensorMap& b1,
+                                     const CUtensorMap& b2, const BwdParams& p, cudaStream_t stream) {
+  using L = BwdLayout<D>;
+  auto kern = fa_bwd_dkdvp_kernel<D, BF16>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  // Work items: the key tiles of the per-tile grid (K/V heads x kv_splits x n_tiles).
+  const int gx = p.BH / p.group * p.kv_splits;
+  const int64_t n_items = static_cast<int64_t>(gx) * p.n_tiles;
+  if (n_items <= 0) return cudaSuccess;
+  if (n_items > (1LL << 30)) return cudaErrorInvalidValue;
+  const int grid = static_cast<int>(n_items < bwd_sm_count() ? n_items : bwd_sm_count());
+  kern<<<grid, kBwdThreads, L::kSmemBytes, stream>>>(a1, a2, b1, b2, p, gx, static_cast<int>(n_items));
+  return cudaGetLastError();
+}
+
+// The dK/dV pass: the persistent kernel for fixed-length calls at D <= 64 whose items average at
+// most 32 partner blocks (query heads per item x 64-row query blocks, halved under the causal
+// mask); the per-tile grid otherwise.
+template <int D, bool BF16>
+cudaError_t launch_dkdv_t(bool general, const BwdMaps& m, const BwdParams& p, cudaStream_t stream) {
+  if (general) return launch_main_t<D, BF16, true, true>(m.k128, m.v128, m.q64, m.do64, p, stream);
+  if constexpr (D <= 64) {
+    const int64_t blocks = static_cast<int64_t>(p.group / p.kv_splits) * ((p.S + kPartnerRows - 1) / kPartnerRows);
+    if ((p.causal ? blocks / 2 : blocks) <= 32)
+      return launch_dkdv_persistent_t<D, BF16>(m.k128, m.v128, m.q64, m.do64, p, stream);
+  }
+  return launch_main_t<D, BF16, true, false>(m.k128, m.v128, m.q64, m.do64, p, stream);
+}
+
+template <int D, bool BF16>
 cudaError_t launch_reduce_t(const BwdParams& p, int64_t rows, cudaStream_t stream) {
   const int64_t threads = rows * (2 * D / 8);
   const int64_t blocks = (threads + 255) / 256;
@@ -1195,9 +1624,7 @@ cudaError_t launch_bwd_preprocess(int D, bool bf16, const BwdParams& p, int64_t 
 
 cudaError_t launch_bwd_dkdv(int D, bool bf16, bool general, const BwdMaps& m, const BwdParams& p,
                             cudaStream_t stream) {
-#define FA_DKDV(DD, BB)                                                                      \
-  (general ? launch_main_t<DD, BB, true, true>(m.k128, m.v128, m.q64, m.do64, p, stream)     \
-           : launch_main_t<DD, BB, true, false>(m.k128, m.v128, m.q64, m.do64, p, stream))
+#define FA_DKDV(DD, BB) launch_dkdv_t<DD, BB>(general, m, p, stream)
   FA_BWD_DISPATCH(FA_DKDV)
 #undef FA_DKDV
 }

@@ -8,8 +8,9 @@ import torch
 
 import oracle
 from seeded_inputs import C3_D, C3_S, CONFIGS, Workload, make_inputs
-from tests.parity import (assert_close, assert_lse, assert_within_bound, backward_rounding_bounds,
-                          check_backward_heads, check_forward_heads, run_backward, run_forward)
+from tests.parity import (assert_close, assert_close_stored, assert_lse, assert_within_bound,
+                          backward_rounding_bounds, check_backward_heads, check_forward_heads, run_backward,
+                          run_forward)
 
 pytestmark = pytest.mark.gpu
 
@@ -97,6 +98,36 @@ def test_config_c2_backward_sampled_heads(fa):
     heads = [(0, 0), (1, 7), (2, 12), (3, 15)]
     check_forward_heads(inp, o, lse, True, w.scale, heads, row_block=1024)
     check_backward_heads(inp, grads, True, w.scale, heads, row_block=1024)
+
+
+@pytest.mark.parametrize("S,causal", [(4160, True), (4224, True), (2048, False), (2112, False)])
+def test_both_dkdv_kernels_at_their_switch(fa, S, causal):
+    """At D <= 64 the dK/dV pass runs its persistent kernel while a work item averages at most 32
+    partner blocks (64-row query blocks, halved under the causal mask) and the per-tile kernel
+    beyond: both sides of that switch, every row of two heads (the last tile ragged)."""
+    w = Workload("dkdv_switch", 1, 2, S, 64, "fp16", causal, backward=True, seed=S + causal)
+    inp = make_inputs(w)
+    o, lse, grads = fwd_bwd(fa, w, inp)
+    check_backward_heads(inp, grads, causal, w.scale, [(0, 0), (0, 1)], row_block=2048)
+
+
+def test_grouped_heads_in_persistent_dkdv_items(fa):
+    """Grouped K/V heads with short rows keep the persistent dK/dV pass (two query heads per
+    work item, and CTAs splitting a group when there are few K/V heads): every row of every K/V
+    head against the grouped oracle."""
+    for B, H, Hkv, S in ((2, 8, 4, 1024), (1, 8, 1, 512)):
+        w = Workload("gqa_persistent", B, H, S, 64, "bf16", True, backward=True, seed=S + Hkv, H_kv=Hkv)
+        inp = make_inputs(w)
+        q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+        o, lse = fa.forward(q, k, v, causal=True, scale=w.scale)
+        dq, dk, dv = fa.backward(q, k, v, o, do, lse, causal=True, scale=w.scale)
+        torch.cuda.synchronize()
+        assert fa.fa_check_device_errors(None) == 0
+        r = oracle.backward_gqa(inp["q"], inp["k"], inp["v"], inp["do"], True, w.scale)
+        g = H // Hkv
+        assert_close_stored("dQ", dq, r[0])
+        assert_close_stored("dK", dk, r[1], spread=math.sqrt(g))
+        assert_close_stored("dV", dv, r[2], spread=math.sqrt(g))
 
 
 def test_leaderboard_workload_sampled_heads(fa):
