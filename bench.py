@@ -1,8 +1,8 @@
 """Benchmark: exact attention forward + backward on one GB300 per process.
 
 One step = the whole hot path on one batch: fa_fwd (O, L) then fa_bwd
-(Delta, dK/dV, dQ) on the causal B4 H16 S4096 D64 fp16 workload, inputs
-resident in HBM.  Prints ONE JSON line (rank 0):
+(Delta, dK/dV, dQ; at D <= 64 the dQ pass computes Delta and runs first) on
+the causal B4 H16 S4096 D64 fp16 workload, inputs resident in HBM.  Prints ONE JSON line (rank 0):
 
   value     whole-job TFLOP/s over the timed steps, counting 4*B*H*S^2*D / 2
             (causal) for the forward and 2.5x that for the backward;
@@ -119,16 +119,32 @@ def fwd_kernel_name(w, general=False):
     return "fa_fwd4p_kernel"
 
 
+def bwd_fuses_delta(w):
+    """Whether the library's dQ pass computes Delta itself (D <= 64, fixed length, no window
+    band): the backward then runs the dQ pass first and the dK/dV pass after it, with no
+    separate Delta kernel."""
+    return w.D <= 64 and not is_packed(w) and getattr(w, "window", None) is None
+
+
+def bwd_intervals(w):
+    """The backward kernels between fa_bwd_marked's marks 0-1, 1-2 and 2-3 (None: no launch)."""
+    if bwd_fuses_delta(w):
+        return ["fa_bwd_dq_kernel", "fa_bwd_dkdv_kernel", None]
+    return ["fa_bwd_preprocess_kernel", "fa_bwd_dkdv_kernel", "fa_bwd_dq_kernel"]
+
+
 def kernel_work(w, general=False):
     """Algorithmic work per launch of each kernel (FLOPs of its tensor-core GEMMs, or HBM bytes)."""
     units = pairs(w) * w.D
     rows = sum(n for _, _, n in head_list(w))
-    return {
+    work = {
         fwd_kernel_name(w, general): ("tensor", 4.0 * units),        # S = QK^T, O += PV
-        "fa_bwd_preprocess_kernel": ("hbm", rows * w.D * 2 * 2 + rows * 4),  # read O, dO; write Delta
         "fa_bwd_dkdv_kernel": ("tensor", 8.0 * units),       # S^T, dP^T, dV, dK
-        "fa_bwd_dq_kernel": ("tensor", 6.0 * units),         # S, dP, dQ
+        "fa_bwd_dq_kernel": ("tensor", 6.0 * units),         # S, dP, dQ (and Delta's row sums when fused)
     }
+    if not bwd_fuses_delta(w):
+        work["fa_bwd_preprocess_kernel"] = ("hbm", rows * w.D * 2 * 2 + rows * 4)  # read O, dO; write Delta
+    return work
 
 
 def sources_digest(kernel):
@@ -440,10 +456,11 @@ def main():
     n_split = fa.fa_splitkv_num_splits(B, H, S, D) if args.workload == "splitkv" else 0
     split_bytes = fa.fa_fwd_splitkv_workspace_size(B, H, S, D, n_split) if n_split else 0
     split_ws = torch.empty(max(split_bytes, 256), dtype=torch.uint8, device=dev)
-    # Kernel launches per step: forward (+ merge when split), Delta, dK/dV (+ partial-sum
-    # reduction when the grouped pass splits), dQ.
+    # Kernel launches per step: forward (+ merge when split), Delta (unless the dQ pass computes
+    # it), dK/dV (+ partial-sum reduction when the grouped pass splits), dQ.
     delta_bytes = ((H * (w.total if packed else B * S) * 4) + 255) // 256 * 256
-    launches_per_step = 4 + (1 if n_split else 0) + (1 if ws_bytes > delta_bytes else 0)
+    launches_per_step = (3 + (0 if bwd_fuses_delta(w) else 1) + (1 if n_split else 0)
+                         + (1 if ws_bytes > delta_bytes else 0))
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     sp = stream.cuda_stream
@@ -514,21 +531,23 @@ def main():
     if fa.fa_check_device_errors(sp) != 0:
         raise RuntimeError("device error during the timed steps: " + fa.fa_last_error_detail())
 
-    names = [fwd_kernel_name(w, n_split > 0), "fa_bwd_preprocess_kernel", "fa_bwd_dkdv_kernel", "fa_bwd_dq_kernel"]
+    slots = [fwd_kernel_name(w, n_split > 0)] + bwd_intervals(w)
+    names = [n for n in slots if n is not None]
     per = {n: [] for n in names}
-    step_ms = []
+    step_ms, bwd_step_ms = [], []
     for e in evs:
-        # fwd = e0->e1 (the fa_fwd launch); bwd kernels between the marks e1..e4
+        # fwd = e0->e1 (the forward call); the backward's kernels between the marks e1..e4
         ts = [e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2]), e[2].elapsed_time(e[3]), e[3].elapsed_time(e[4])]
-        for n, t in zip(names, ts):
-            per[n].append(t)
+        for n, t in zip(slots, ts):
+            if n is not None:
+                per[n].append(t)
         step_ms.append(e[0].elapsed_time(e[4]))
+        bwd_step_ms.append(e[1].elapsed_time(e[4]))
     total_ms = max_over_ranks(sum(step_ms), dist, dev)
     f_fwd, f_bwd = conv_flops(w)
     value = job_throughput(f_fwd + f_bwd, args.steps, world, total_ms) / 1e12
     fwd_ms = statistics.mean(per[names[0]])
-    bwd_ms = statistics.mean([a + b + c for a, b, c in zip(per["fa_bwd_preprocess_kernel"],
-                                                           per["fa_bwd_dkdv_kernel"], per["fa_bwd_dq_kernel"])])
+    bwd_ms = statistics.mean(bwd_step_ms)
     peaks = load_peaks()
     unsplit = None
     if n_split:
@@ -571,6 +590,8 @@ def main():
         else:
             ach = amt / (avg[n] * 1e-3) / 1e9
             kernels[n] = {"ms": avg[n], "GB/s": ach, "frac_of_hbm_peak": ach / peaks["hbm_gbs"]}
+    if "fa_bwd_preprocess_kernel" not in names:
+        kernels["fa_bwd_dq_kernel"]["note"] = "computes Delta = rowsum(dO o O) too (no Delta kernel)"
 
     # ---------------------------------------------------------------- end to end through host buffers
     # Every step copies its inputs q, k, v, dO (and a packed batch's cu_seqlens) from pinned host

@@ -386,16 +386,24 @@ fa_status bwd_impl(const void* q, const void* k, const void* v, const void* o, c
     if (!marks || !marks[i]) return FA_OK;
     return from_cuda(cudaEventRecord(static_cast<cudaEvent_t>(marks[i]), s), "event record");
   };
-  if ((st = mark(0))) return st;
-  if ((st = from_cuda(fa::launch_bwd_preprocess(Di, bf16, p, q_rows, s), "backward preprocess launch"))) return st;
-  if ((st = mark(1))) return st;
   const bool general = sh.general(causal != 0);
+  const bool fused_delta = fa::bwd_dq_computes_delta(Di, general);
+  // Delta then dK/dV then dQ; or, when the dQ kernel computes Delta, dQ then dK/dV.
+  if ((st = mark(0))) return st;
+  if (fused_delta) {
+    if ((st = from_cuda(fa::launch_bwd_dq(Di, bf16, general, maps, p, s), "backward dQ launch"))) return st;
+  } else if ((st = from_cuda(fa::launch_bwd_preprocess(Di, bf16, p, q_rows, s), "backward preprocess launch"))) {
+    return st;
+  }
+  if ((st = mark(1))) return st;
   if ((st = from_cuda(fa::launch_bwd_dkdv(Di, bf16, general, maps, p, s), "backward dK/dV launch"))) return st;
   if (splits > 1 &&
       (st = from_cuda(fa::launch_bwd_dkv_reduce(Di, bf16, p, kv_rows, s), "backward dK/dV reduce launch")))
     return st;
   if ((st = mark(2))) return st;
-  if ((st = from_cuda(fa::launch_bwd_dq(Di, bf16, general, maps, p, s), "backward dQ launch"))) return st;
+  if (!fused_delta &&
+      (st = from_cuda(fa::launch_bwd_dq(Di, bf16, general, maps, p, s), "backward dQ launch")))
+    return st;
   return mark(3);
 }
 
@@ -592,8 +600,9 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void
   cudaError_t e = cudaSuccess;
   float* delta = fa::noalloc_delta_address(&e);
   if (!delta) return from_cuda(e, "fa_bwd_noalloc: address of the scratch array");
-  // The same three kernels as fa_bwd, with the scratch array as the workspace.
-  // The Delta kernel overwrites every row it uses, so nothing needs clearing.
+  // The same kernels as fa_bwd, with the scratch array as the workspace.
+  // Every row's Delta is written (by the Delta kernel or the dQ pass) before it
+  // is read, so nothing needs clearing.
   return fa_bwd_marked(q, k, v, o, dout, lse, dq, dk, dv, B, H, S, D, causal, scale, dtype, delta,
                        static_cast<size_t>(fa::kNoAllocMaxRows) * sizeof(float), stream, nullptr);
 }

@@ -48,8 +48,51 @@ using namespace ptx;
 __device__ const float g_pos_inf = __builtin_huge_valf();
 
 // ------------------------------------------------------------------ preprocess
-// Delta_i = sum_d dO_id * O_id in fp32.  D/8 threads share a row, each
-// reading 16 bytes of O and of dO; a shuffle tree sums the group.
+// Delta_i = sum_d dO_id * O_id in fp32.  D/8 lanes share a row, each reading
+// 16 bytes of O and of dO; a shuffle tree sums the group.  The whole warp
+// calls it (the shuffles need all 32 lanes); `valid` says whether this lane's
+// row exists.  Every lane of the group gets the row's sum.
+// This lane's part of the row's dot product: 8 elements of O (a) and of dO (b).
+template <bool BF16>
+__device__ __forceinline__ float chunk_dot(const uint4 a, const uint4 b) {
+  const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+  const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+  float acc = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 fa2, fb2;
+    if constexpr (BF16) {
+      fa2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&aw[i]));
+      fb2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bw[i]));
+    } else {
+      fa2 = __half22float2(*reinterpret_cast<const __half2*>(&aw[i]));
+      fb2 = __half22float2(*reinterpret_cast<const __half2*>(&bw[i]));
+    }
+    acc = fmaf(fa2.x, fb2.x, acc);
+    acc = fmaf(fa2.y, fb2.y, acc);
+  }
+  return acc;
+}
+
+// Sum over the row's D/8 lanes.
+template <int D>
+__device__ __forceinline__ float row_sum(float acc) {
+#pragma unroll
+  for (int off = D / 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  return acc;
+}
+
+template <int D, bool BF16>
+__device__ __forceinline__ float row_delta(const void* o, const void* dout, int64_t row, bool valid) {
+  float acc = 0.f;
+  if (valid) {
+    const int64_t off = (row * D + ((threadIdx.x & 31) % (D / 8)) * 8) * 2;  // this lane's 8 elements
+    acc = chunk_dot<BF16>(*reinterpret_cast<const uint4*>(static_cast<const char*>(o) + off),
+                          *reinterpret_cast<const uint4*>(static_cast<const char*>(dout) + off));
+  }
+  return row_sum<D>(acc);
+}
+
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) fa_bwd_preprocess_kernel(const BwdParams p, int64_t rows) {
   constexpr int kTpr = D / 8;           // threads per row
@@ -58,31 +101,10 @@ __global__ void __launch_bounds__(256) fa_bwd_preprocess_kernel(const BwdParams 
   const int sub = lane % kTpr;
   const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-  // Whole warps iterate together so the shuffles below always see 32 lanes.
+  // Whole warps iterate together so the shuffles always see 32 lanes.
   for (int64_t r0 = warp_id * kRowsPerWarp; r0 < rows; r0 += n_warps * kRowsPerWarp) {
     const int64_t row = r0 + lane / kTpr;
-    float acc = 0.f;
-    if (row < rows) {
-      const uint4 a = reinterpret_cast<const uint4*>(static_cast<const char*>(p.o) + (row * D + sub * 8) * 2)[0];
-      const uint4 b = reinterpret_cast<const uint4*>(static_cast<const char*>(p.dout) + (row * D + sub * 8) * 2)[0];
-      const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
-      const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        float2 fa2, fb2;
-        if constexpr (BF16) {
-          fa2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&aw[i]));
-          fb2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bw[i]));
-        } else {
-          fa2 = __half22float2(*reinterpret_cast<const __half2*>(&aw[i]));
-          fb2 = __half22float2(*reinterpret_cast<const __half2*>(&bw[i]));
-        }
-        acc = fmaf(fa2.x, fb2.x, acc);
-        acc = fmaf(fa2.y, fb2.y, acc);
-      }
-    }
-#pragma unroll
-    for (int off = kTpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    const float acc = row_delta<D, BF16>(p.o, p.dout, row, row < rows);
     // Row `row` of [B*H*S, D] (fixed length) or of [T*H, D] (packed: token
     // row / H, head row % H, whose Delta lives at [head, token]).
     if (row < rows && sub == 0)
@@ -128,6 +150,8 @@ constexpr int kProducerWarp = 8 * kBwdGroups;
 constexpr int kMmaWarp = kProducerWarp + 1;  // issues the score products X, Y
 constexpr int kAccWarp = kMmaWarp + 1;       // issues the accumulations
 constexpr int kBwdThreads = (kAccWarp + 1) * 32;
+constexpr int kDeltaWarp = kAccWarp + 1;  // persistent dQ pass: computes Delta
+constexpr int kDqpThreads = kBwdThreads + 32;
 // "P and dS of block i stored" barriers, block i on bar_pfull[i % 4] (8
 // arrivals, one per warp of group i % 2).  With three X/Y buffers a warp of a
 // group may finish block i and move on to the group's next block, i + 2,
@@ -157,8 +181,8 @@ struct BwdLayout {
   // leave room (D <= 64), so the MMA warp can compute X, Y two blocks ahead.
   static constexpr int kXYBufs = D <= 64 ? 3 : 2;
   // a_full, b_full[S], empty[S], xy_full[buffers], acc_issued[buffers], p_full[4], acc_final, drain[2],
-  // then (persistent kernel only) a_empty, acc_free.
-  static constexpr int kNumBars = 1 + 2 * kStages + 2 * kXYBufs + kPFullBars + 1 + 2 + 2;
+  // then (persistent kernels only) a_empty, acc_free, delta_full[2], delta_free[2], stage_full.
+  static constexpr int kNumBars = 1 + 2 * kStages + 2 * kXYBufs + kPFullBars + 1 + 2 + 7;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemUsed = kOffMisc + 16;
   static constexpr int kSmemBytes = (kSmemUsed + 1024) > 116 * 1024 ? (kSmemUsed + 1024) : 116 * 1024;
@@ -766,15 +790,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // the current item's dQ; the accumulation warp starts the next item's dQ once
 // those stores have read it out of TMEM (acc_free).  Barrier phases run on
 // across items: key stages, X/Y buffers and the "P stored" barriers by a
-// running block count, the tile and accumulator barriers by item.  (The same
-// scheme for the dK/dV pass measured slower on long rows: causal B1 H16
-// S16384 D64 840 against 732 us.)
+// running block count, the tile and accumulator barriers by item.
+// One more warp computes Delta = rowsum(dO o O) of each item's rows (the
+// preprocess kernel's arithmetic, from O and dO rows staged in shared memory
+// one item ahead), writes it to the workspace for the dK/dV pass, which then
+// runs after this one, and hands it to the softmax-gradient warps through
+// shared memory (delta_full), so the backward needs no separate Delta kernel.
+template <int D>
+struct DqpLayout {
+  static constexpr int kOffStage = (BwdLayout<D>::kSmemUsed + 127) / 128 * 128;
+  static constexpr int kStageBytes = 128 * D * 2;  // one item's rows of one tensor
+  static constexpr int kSmemBytes = kOffStage + 2 * kStageBytes + 1024;
+  static_assert(kSmemBytes <= 227 * 1024, "persistent dQ pass: shared memory");
+};
+
 template <int D, bool BF16>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __launch_bounds__(kDqpThreads, 1)
     fa_bwd_dqp_kernel(const __grid_constant__ CUtensorMap tm_a1, const __grid_constant__ CUtensorMap tm_a2,
                       const __grid_constant__ CUtensorMap tm_b1, const __grid_constant__ CUtensorMap tm_b2,
                       const BwdParams p, int n_items) {
   using L = BwdLayout<D>;
+  using DL = DqpLayout<D>;
   static_assert(D <= 64 && L::kTmemA, "persistent dQ pass: D <= 64, Q and dO in TMEM");
   using GA = typename L::GA;
   using GB = typename L::GB;
@@ -801,8 +837,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint64_t* bar_drain = bar_accfinal + 1;        // [2] one per MMA warp
   uint64_t* bar_aempty = bar_drain + 2;          // the item's Q, dO copies into TMEM done
   uint64_t* bar_accfree = bar_aempty + 1;        // the item's dQ read out by all 16 warps
+  uint64_t* bar_deltafull = bar_accfree + 1;     // [2] item n's Delta in buffer n % 2
+  uint64_t* bar_deltafree = bar_deltafull + 2;   // [2] buffer n % 2 read by all 16 warps
+  uint64_t* bar_stage = bar_deltafree + 2;       // an item's O, dO rows in the staging buffer
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 4);
+  // Two 128-row Delta buffers (item n in buffer n % 2), in the stage vectors'
+  // space, which the dQ pass does not use.
+  float* delta_buf = reinterpret_cast<float*>(smem + L::kOffVec);
+  static_assert(L::kStages * 2 * kPartnerRows >= 2 * 128, "Delta buffers");
 
   const int warp = warp_index();
   const int lane = threadIdx.x & 31;
@@ -853,6 +896,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(&bar_drain[1], 1);
     mbar_init(bar_aempty, 1);
     mbar_init(bar_accfree, 16);  // one arrival per softmax-gradient warp
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bar_deltafull[b], 1);
+      mbar_init(&bar_deltafree[b], 16);  // one arrival per softmax-gradient warp
+    }
+    mbar_init(bar_stage, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -869,7 +917,63 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t sB1 = smem_u32(smem + L::kOffB1);
   const uint32_t sB2 = smem_u32(smem + L::kOffB2);
 
-  if (warp == kProducerWarp) {
+  if (warp == kDeltaWarp) {
+    // ------------------------------------------------------------ Delta warp
+    // Lane 0 copies an item's O and dO rows into the staging buffer (one bulk
+    // copy each: a fixed-length head's rows are contiguous), one item ahead of
+    // the sums; D/8 lanes per row then sum dO o O from shared memory.
+    constexpr int kTpr = D / 8;
+    constexpr int kRowsPerStep = 32 / kTpr;
+    uint8_t* stage_o = smem + DL::kOffStage;
+    uint8_t* stage_do = stage_o + DL::kStageBytes;
+    auto issue = [&](const Item& w) {
+      const uint32_t bytes = static_cast<uint32_t>(min(128, S - w.own0)) * D * 2;
+      const int64_t off = (static_cast<int64_t>(w.bh) * S + w.own0) * D * 2;
+      mbar_arrive_expect_tx(bar_stage, 2 * bytes);
+      bulk_load(stage_o, static_cast<const char*>(p.o) + off, bytes, bar_stage);
+      bulk_load(stage_do, static_cast<const char*>(p.dout) + off, bytes, bar_stage);
+    };
+    bool ok = true;
+    int k = item_at(0);
+    if (k >= 0 && lane == 0) issue(decode(k));
+    int n = 0;  // item n's copy is the one in flight
+    for (int r = 0; ok && k >= 0; ++r, ++n) {
+      const Item w = decode(k);
+      const int64_t rowbase = static_cast<int64_t>(w.bh) * S;
+      // Buffer n % 2 was last read at the start of item n - 2.
+      if (n >= 2)
+        ok = warp_wait(&bar_deltafree[n & 1], ((n >> 1) - 1) & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutSoftmax);
+      if (ok) ok = warp_wait(bar_stage, n & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutSoftmax);
+      if (!ok) break;
+      float* buf = delta_buf + (n & 1) * 128;
+      const int sub16 = (lane % kTpr) * 16;
+#pragma unroll 4
+      for (int r0 = 0; r0 < 128; r0 += kRowsPerStep) {
+        const int rr = r0 + lane / kTpr;
+        const int row = w.own0 + rr;
+        float acc = 0.f;
+        if (row < S)
+          acc = chunk_dot<BF16>(*reinterpret_cast<const uint4*>(stage_o + rr * D * 2 + sub16),
+                                *reinterpret_cast<const uint4*>(stage_do + rr * D * 2 + sub16));
+        const float d = row_sum<D>(acc);
+        if (lane % kTpr == 0) {
+          buf[rr] = d;
+          if (row < S) p.delta[rowbase + row] = d;
+        }
+      }
+      k = item_at(r + 1);
+      __syncwarp();
+      if (lane == 0) {
+        if (k >= 0) {  // the staging buffer is free again: the next item's rows
+          fence_proxy_async_smem();
+          issue(decode(k));
+        }
+        mbar_arrive(&bar_deltafull[n & 1]);  // release: the buffer's writes reach its waiters
+      }
+    }
+    // Given up: the copy in flight lands before the CTA exits.
+    if (!ok && lane == 0) drain_wait(bar_stage, n & 1, p.err);
+  } else if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer (lane 0)
     if (lane == 0) {
       prefetch_tmap(&tm_a1);
@@ -1031,12 +1135,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const Item w = decode(k);
       const int my = w.own0 + q4 * 32 + lane;  // this thread's query
       const int64_t rowbase = static_cast<int64_t>(w.bh) * S;
-      // This row's L2 = L * log2 e and Delta (rows past S: L2 = +inf, so P = 0 exactly).
-      float my_l2 = INFINITY, my_delta = 0.f;
-      if (my < S) {
-        my_l2 = p.lse[rowbase + my] * kLog2e;
-        my_delta = p.delta[rowbase + my];
+      // This row's L2 = L * log2 e (rows past S: L2 = +inf, so P = 0 exactly)
+      // and its Delta, from the Delta warp.
+      const float my_l2 = my < S ? p.lse[rowbase + my] * kLog2e : INFINITY;
+      if (!warp_wait(&bar_deltafull[n & 1], (n >> 1) & 1, abort_flag, p.err, p.wait_ns, kErrTimeoutSoftmax)) {
+        alive = false;
+        break;
       }
+      const float my_delta = delta_buf[(n & 1) * 128 + q4 * 32 + lane];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_deltafree[n & 1]);
       // This group's blocks of the item: global block indices i0 + x with (i0 + x) % 2 == g.
       for (int x = (g - i0) & 1; x < w.nb; x += kBwdGroups) {
         const int i = i0 + x;
@@ -1532,16 +1640,16 @@ int bwd_sm_count() {
 template <int D, bool BF16>
 cudaError_t launch_dq_persistent_t(const CUtensorMap& a1, const CUtensorMap& a2, const CUtensorMap& b1,
                                    const CUtensorMap& b2, const BwdParams& p, cudaStream_t stream) {
-  using L = BwdLayout<D>;
+  constexpr int kSmem = DqpLayout<D>::kSmemBytes;
   auto kern = fa_bwd_dqp_kernel<D, BF16>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   // Work items: the query tiles of the non-persistent grid (B*H x n_tiles).
   const int64_t n_items = static_cast<int64_t>(p.BH) * p.n_tiles;
   if (n_items <= 0) return cudaSuccess;
   if (n_items > (1LL << 30)) return cudaErrorInvalidValue;
   const int grid = static_cast<int>(n_items < bwd_sm_count() ? n_items : bwd_sm_count());
-  kern<<<grid, kBwdThreads, L::kSmemBytes, stream>>>(a1, a2, b1, b2, p, static_cast<int>(n_items));
+  kern<<<grid, kDqpThreads, kSmem, stream>>>(a1, a2, b1, b2, p, static_cast<int>(n_items));
   return cudaGetLastError();
 }
 
@@ -1551,7 +1659,7 @@ cudaError_t launch_dq_persistent_t(const CUtensorMap& a1, const CUtensorMap& a2,
 template <int D, bool BF16>
 cudaError_t launch_dq_t(bool general, const BwdMaps& m, const BwdParams& p, cudaStream_t stream) {
   if (general) return launch_main_t<D, BF16, false, true>(m.q128, m.do128, m.k64, m.v64, p, stream);
-  if constexpr (D <= 64)
+  if constexpr (D <= 64)  // the persistent kernel: bwd_dq_computes_delta(D, false)
     return launch_dq_persistent_t<D, BF16>(m.q128, m.do128, m.k64, m.v64, p, stream);
   else
     return launch_main_t<D, BF16, false, false>(m.q128, m.do128, m.k64, m.v64, p, stream);
@@ -1643,5 +1751,7 @@ cudaError_t launch_bwd_dq(int D, bool bf16, bool general, const BwdMaps& m, cons
 }
 
 #undef FA_BWD_DISPATCH
+
+bool bwd_dq_computes_delta(int D, bool general) { return !general && D <= 64; }
 
 }  // namespace fa

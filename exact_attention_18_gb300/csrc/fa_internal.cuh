@@ -99,6 +99,10 @@ cudaError_t launch_bwd_dkdv(int D, bool bf16, bool general, const BwdMaps& maps,
                             cudaStream_t stream);
 cudaError_t launch_bwd_dq(int D, bool bf16, bool general, const BwdMaps& maps, const BwdParams& p,
                           cudaStream_t stream);
+// True when launch_bwd_dq's kernel computes Delta itself and writes it to p.delta
+// (the persistent dQ kernel): the backward then skips the Delta kernel and runs
+// the dQ pass before the dK/dV pass, which reads that Delta.
+bool bwd_dq_computes_delta(int D, bool general);
 // Sums the kv_splits partial dK/dV rows and writes dK, dV (only when kv_splits > 1);
 // rows: K/V rows (B*H_kv*S, or T*H_kv packed).
 cudaError_t launch_bwd_dkv_reduce(int D, bool bf16, const BwdParams& p, int64_t rows, cudaStream_t stream);

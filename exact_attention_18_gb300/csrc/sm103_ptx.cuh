@@ -155,6 +155,23 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+// 1-D bulk copy of `bytes` contiguous bytes global -> shared (both addresses
+// 16-byte aligned, `bytes` a multiple of 16); completion is signalled on `bar`
+// as transaction bytes.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Orders this thread's earlier generic-proxy accesses to shared memory before
+// its later async-proxy ones (a bulk copy into a buffer it has just read).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // 4-byte asynchronous copy global -> shared; with `valid` false nothing is
 // read and the destination is zero-filled.
 __device__ __forceinline__ void cp_async_4(void* dst, const void* src, bool valid) {

@@ -109,11 +109,13 @@ size_t fa_bwd_workspace_size(int64_t B, int64_t H, int64_t S, int64_t D);
 /*
  * Backward pass (recompute).  Given the forward inputs, its outputs o and lse,
  * and the loss gradient dout = dL/dO, writes dq, dk, dv ([B, H, S, D], same
- * dtype).  Three kernels run in order on `stream`:
+ * dtype).  Three passes run in order on `stream`:
  *   1. D_i = rowsum(dO o O) into the workspace (fp32);
  *   2. per 128-key block: dV = sum_i P^T dO and dK = scale * sum_i dS^T Q over the
  *      query blocks that see it, P = exp(S - L) recomputed from lse;
  *   3. per 128-query block: dQ = scale * sum_j dS K over its visible key blocks.
+ * At D <= 64 the dQ kernel computes D_i itself (and writes it to the
+ * workspace): two kernels then run, the dQ pass first and the dK/dV pass after.
  * workspace: device buffer of at least fa_bwd_workspace_size() bytes, 256-byte
  * aligned, owned by the caller; its contents on entry do not matter.
  */
@@ -123,12 +125,16 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  void* stream);
 
 /*
- * fa_bwd with timing marks.  Same arguments, same three launches, same
- * results; in addition, each non-NULL entry of `marks` (a cudaEvent_t passed
- * as void*, owned by the caller) is recorded on `stream`: marks[0] before the
- * Delta kernel, marks[1] after it, marks[2] after the dK/dV kernel, marks[3]
- * after the dQ kernel.  Lets a caller time each kernel with CUDA events on
- * the stream that runs it.  `marks` itself may be NULL.
+ * fa_bwd with timing marks.  Same arguments, same launches, same results;
+ * in addition, each non-NULL entry of `marks` (a cudaEvent_t passed as void*,
+ * owned by the caller) is recorded on `stream`, in this order: marks[0]
+ * before the first kernel; marks[1] after the Delta kernel, or after the dQ
+ * kernel where that computes Delta (fa_bwd, fa_bwd_gqa at D <= 64; the
+ * window and packed-batch calls always run the Delta kernel); marks[2] after
+ * the dK/dV kernel (and its partial-sum reduction); marks[3] after the dQ
+ * kernel where it runs last, else right after marks[2].  Lets a caller time
+ * each kernel with CUDA events on the stream that runs it.  `marks` itself
+ * may be NULL.
  */
 fa_status fa_bwd_marked(const void* q, const void* k, const void* v, const void* o, const void* dout,
                         const float* lse, void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t S,
@@ -147,7 +153,7 @@ fa_status fa_bwd_marked(const void* q, const void* k, const void* v, const void*
  * (few K/V heads, short sequences), s CTAs share a (K/V head, key block),
  * each over G/s of the group's heads (s the smallest divisor of G that gives
  * 304 CTAs, else G); they write fp32 partial sums to the workspace and a
- * fourth kernel adds them in a fixed order.  No atomics either way: results
+ * further kernel adds them in a fixed order.  No atomics either way: results
  * are deterministic.  Workspace: fa_bwd_gqa_workspace_size() bytes.  Other
  * conventions as fa_bwd; H_kv as in fa_fwd_gqa.
  */

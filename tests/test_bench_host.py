@@ -10,7 +10,7 @@ import sys
 import pytest
 
 import bench
-from seeded_inputs import CONFIGS, Workload
+from seeded_inputs import CONFIGS, PACKED_CONFIGS, Workload
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -60,6 +60,19 @@ def test_kernel_work_names_the_launched_forward():
     assert "fa_fwd_kernel" in bench.kernel_work(CONFIGS["c4"])
     kind, amount = bench.kernel_work(CONFIGS["c2"])["fa_bwd_dkdv_kernel"]
     assert kind == "tensor" and amount == 2 * bench.conv_flops(CONFIGS["c2"])[0]
+
+
+def test_backward_intervals_follow_the_launch_order():
+    """At D <= 64 with fixed lengths and no window the dQ pass computes Delta and runs first;
+    otherwise the Delta kernel, the dK/dV pass and the dQ pass run in that order."""
+    fused = ["fa_bwd_dq_kernel", "fa_bwd_dkdv_kernel", None]
+    split = ["fa_bwd_preprocess_kernel", "fa_bwd_dkdv_kernel", "fa_bwd_dq_kernel"]
+    assert bench.bwd_intervals(CONFIGS["c2"]) == fused
+    assert bench.bwd_intervals(CONFIGS["c4"]) == split            # D = 128
+    assert bench.bwd_intervals(CONFIGS["window"]) == split        # a window band
+    assert bench.bwd_intervals(PACKED_CONFIGS["varlen"]) == split
+    assert "fa_bwd_preprocess_kernel" not in bench.kernel_work(CONFIGS["c2"])
+    assert "fa_bwd_preprocess_kernel" in bench.kernel_work(CONFIGS["c4"])
 
 
 def test_traffic_is_dropped_when_the_kernel_sources_change(monkeypatch):

@@ -169,3 +169,33 @@ def test_bwd_workspace_checks(fa):
     small = torch.empty(16, dtype=torch.uint8, device="cuda")
     with pytest.raises(fa.FAError, match="FA_ERR_WORKSPACE"):
         fa.backward(q, k, v, o, inp["do"].cuda(), lse, workspace=small)
+
+
+@pytest.mark.parametrize("D,dtype,causal,S,gqa", [(64, "fp16", True, 1000, False), (32, "bf16", False, 300, False),
+                                                  (16, "fp16", True, 129, False), (64, "bf16", True, 777, True),
+                                                  (128, "fp16", True, 300, False)])
+def test_delta_left_in_the_workspace(fa, D, dtype, causal, S, gqa):
+    """The backward leaves D_i = rowsum(dO o O) of every query row at the start of its
+    workspace: computed by the dQ pass (D <= 64, which then runs before the dK/dV pass) or
+    by the Delta kernel (D = 128).  O and L are the oracle's forward, rounded to the
+    input dtype; a ragged last tile leaves rows past S in the last work item."""
+    H_kv = 2 if gqa else None
+    w = Workload("delta_ws", 2, 4, S, D, dtype, causal, backward=True, seed=91, H_kv=H_kv)
+    inp = make_inputs(w)
+    kx = oracle.expand_kv(inp["k"], w.H) if gqa else inp["k"]
+    vx = oracle.expand_kv(inp["v"], w.H) if gqa else inp["v"]
+    o_ref, l_ref = oracle.forward(inp["q"], kx, vx, causal, w.scale)
+    o_in = o_ref.to(inp["q"].dtype)
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+    o, lse = o_in.cuda(), l_ref.float().cuda()
+    ws_bytes = fa.fa_bwd_gqa_workspace_size(w.B, w.H, k.shape[1], S, D)
+    ws = torch.full((ws_bytes // 4,), float("nan"), dtype=torch.float32, device="cuda")
+    fa.backward(q, k, v, o, do, lse, causal=causal, scale=w.scale, workspace=ws)
+    assert fa.fa_check_device_errors(None) == 0, fa.fa_last_error_detail()
+    got = ws[: w.B * w.H * S].view(w.B, w.H, S).cpu().double()
+    ref = oracle.delta(o_in, inp["do"])
+    # Products of two 16-bit values are exact in fp32; D fp32 additions in any order stay
+    # within D * 2^-24 * sum |terms| of the exact sum.
+    bound = D * 2.0 ** -24 * (o_in.double() * inp["do"].double()).abs().sum(-1) * 1.01 + 1e-30
+    err = (got - ref).abs()
+    assert bool((err <= bound).all()), f"max |Delta - oracle| {float(err.max()):.3e}"
