@@ -11,7 +11,10 @@ the causal B4 H16 S4096 D64 fp16 workload, inputs resident in HBM.  Prints ONE J
             (copy streams and two buffer sets overlap neighbouring steps' copies
             with the kernels);
   roofline  the dominant kernel's algorithmic FLOPs (or bytes) per launch over
-            its CUDA-event duration, against the measured peak;
+            its CUDA-event duration, against the measured peak (kernel times come
+            from a second pass of the same steps with events between the
+            backward's kernels; the timed steps have none there, since such an
+            event keeps the dK/dV pass from overlapping the dQ pass's end);
   cpu_baseline  the fp64 CPU oracle on a bounded sample (rank 0, N = 1).
 
 `--impl reference` times the CPU oracle (the reference arm of this build) on
@@ -495,17 +498,25 @@ def main():
         return fa.fa_bwd_gqa_marked(q_, k_, v_, o_, do_, lse_, dq_, dk_, dv_, B, H, Hkv, S, D, w.causal, w.scale,
                                     dt_code, ws.data_ptr(), ws_bytes, sp, marks)
 
-    def step(ev=None):
+    def step(ev=None, inner=False):
+        """One step; ev: five events, e0 before the forward, e1 between forward and backward, e4
+        after the backward, and with `inner` e2, e3 between the backward's kernels (an event
+        between two kernels keeps the second from starting before the first has finished, so
+        the timed steps record none there)."""
         if ev is not None:
             ev[0].record(stream)
         st = fwd_call(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr())
         if st:
             raise RuntimeError(f"forward: {fa.fa_status_string(st)} {fa.fa_last_error_detail()}")
-        marks = None if ev is None else [e.cuda_event for e in ev[1:5]]
+        marks = [e.cuda_event for e in ev[1:5]] if ev is not None and inner else None
+        if ev is not None and not inner:
+            ev[1].record(stream)
         st = bwd_call(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
                       dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), marks)
         if st:
             raise RuntimeError(f"backward: {fa.fa_status_string(st)} {fa.fa_last_error_detail()}")
+        if ev is not None and not inner:
+            ev[4].record(stream)
 
     visible = os.environ.get("CUDA_VISIBLE_DEVICES")
     gpu_id = visible.split(",")[local].strip() if visible else str(local)
@@ -518,7 +529,8 @@ def main():
         raise RuntimeError("device error during warm-up: " + fa.fa_last_error_detail())
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
-    for e in evs:  # create the CUDA events (torch creates them on first record) before the C side records them
+    kevs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    for e in evs + kevs:  # create the CUDA events (torch creates them on first record) before the C side records them
         for x in e:
             x.record(stream)
     barrier()
@@ -528,26 +540,29 @@ def main():
         step(evs[i])
     barrier()
     t_wall1 = time.time()
+    # The same steps again with events between the backward's kernels: each kernel's time.
+    for i in range(args.steps):
+        flush.zero_()
+        step(kevs[i], inner=True)
+    torch.cuda.synchronize()
     if fa.fa_check_device_errors(sp) != 0:
         raise RuntimeError("device error during the timed steps: " + fa.fa_last_error_detail())
 
     slots = [fwd_kernel_name(w, n_split > 0)] + bwd_intervals(w)
     names = [n for n in slots if n is not None]
     per = {n: [] for n in names}
-    step_ms, bwd_step_ms = [], []
-    for e in evs:
+    for e in kevs:
         # fwd = e0->e1 (the forward call); the backward's kernels between the marks e1..e4
         ts = [e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2]), e[2].elapsed_time(e[3]), e[3].elapsed_time(e[4])]
         for n, t in zip(slots, ts):
             if n is not None:
                 per[n].append(t)
-        step_ms.append(e[0].elapsed_time(e[4]))
-        bwd_step_ms.append(e[1].elapsed_time(e[4]))
+    step_ms = [e[0].elapsed_time(e[4]) for e in evs]
     total_ms = max_over_ranks(sum(step_ms), dist, dev)
     f_fwd, f_bwd = conv_flops(w)
     value = job_throughput(f_fwd + f_bwd, args.steps, world, total_ms) / 1e12
-    fwd_ms = statistics.mean(per[names[0]])
-    bwd_ms = statistics.mean(bwd_step_ms)
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    bwd_ms = statistics.mean(e[1].elapsed_time(e[4]) for e in evs)
     peaks = load_peaks()
     unsplit = None
     if n_split:

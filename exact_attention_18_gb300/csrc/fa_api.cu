@@ -396,7 +396,9 @@ fa_status bwd_impl(const void* q, const void* k, const void* v, const void* o, c
     return st;
   }
   if ((st = mark(1))) return st;
-  if ((st = from_cuda(fa::launch_bwd_dkdv(Di, bf16, general, maps, p, s), "backward dK/dV launch"))) return st;
+  // After the dQ pass, the dK/dV pass's first CTAs start as the dQ pass's last ones finish.
+  if ((st = from_cuda(fa::launch_bwd_dkdv(Di, bf16, general, maps, p, s, fused_delta), "backward dK/dV launch")))
+    return st;
   if (splits > 1 &&
       (st = from_cuda(fa::launch_bwd_dkv_reduce(Di, bf16, p, kv_rows, s), "backward dK/dV reduce launch")))
     return st;

@@ -498,6 +498,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
       }
       if constexpr (KV_OUTER) {
+        // Delta may come from the kernel just before this one (a programmatic
+        // dependent launch after the persistent dQ pass): wait for it before the
+        // first read.  Nothing read earlier is written by that kernel.
+        if (it == 0) griddep_wait();
         float* v = vecs + st * 2 * kPN;
 #pragma unroll
         for (int h = 0; h < kPN; h += 32) {
@@ -916,6 +920,10 @@ __global__ void __launch_bounds__(kDqpThreads, 1)
   const uint32_t sA2 = smem_u32(smem + L::kOffA2);
   const uint32_t sB1 = smem_u32(smem + L::kOffB1);
   const uint32_t sB2 = smem_u32(smem + L::kOffB2);
+  // The dK/dV pass that follows may start its CTAs as this grid's CTAs exit
+  // (it cannot share an SM with one: registers); it waits for this grid to
+  // complete before it reads Delta.
+  griddep_launch_dependents();
 
   if (warp == kDeltaWarp) {
     // ------------------------------------------------------------ Delta warp
@@ -1361,7 +1369,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
         }
         // The block's L and Delta (partner queries past S read 0: their Q and
-        // dO rows are zero-filled, so P dO and dS vanish there).
+        // dO rows are zero-filled, so P dO and dS vanish there).  Delta may come
+        // from the kernel just before this one (as in fa_bwd_main_kernel).
+        if (it == 0) griddep_wait();
         float* v = vecs + st * 2 * kPN;
 #pragma unroll
         for (int h = 0; h < kPN; h += 32) {
@@ -1612,17 +1622,35 @@ cudaError_t launch_pre_t(const BwdParams& p, int64_t rows, cudaStream_t stream) 
   return cudaGetLastError();
 }
 
+// Launches `kern`; with `dependent`, as a programmatic dependent launch of the
+// kernel before it on `stream`: its CTAs may start while that kernel's last
+// CTAs still run, and it waits (griddep_wait) before reading that kernel's output.
+template <typename... Params, typename... Args>
+cudaError_t launch_kernel(void (*kern)(Params...), dim3 grid, int threads, int smem, cudaStream_t stream,
+                          bool dependent, const Args&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = dependent ? attr : nullptr;
+  cfg.numAttrs = dependent ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 template <int D, bool BF16, bool KV_OUTER, bool GENERAL>
 cudaError_t launch_main_t(const CUtensorMap& a1, const CUtensorMap& a2, const CUtensorMap& b1,
-                          const CUtensorMap& b2, const BwdParams& p, cudaStream_t stream) {
+                          const CUtensorMap& b2, const BwdParams& p, cudaStream_t stream, bool dependent = false) {
   using L = BwdLayout<D>;
   auto kern = fa_bwd_main_kernel<D, BF16, KV_OUTER, GENERAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
   if (e != cudaSuccess) return e;
   // dK/dV pass: kv_splits CTAs per (K/V head, key tile); dQ pass: one per (query head, query tile).
   dim3 grid(KV_OUTER ? p.BH / p.group * p.kv_splits : p.BH, p.n_tiles);
-  kern<<<grid, kBwdThreads, L::kSmemBytes, stream>>>(a1, a2, b1, b2, p);
-  return cudaGetLastError();
+  return launch_kernel(kern, grid, kBwdThreads, L::kSmemBytes, stream, dependent, a1, a2, b1, b2, p);
 }
 
 int bwd_sm_count() {
@@ -1667,7 +1695,8 @@ cudaError_t launch_dq_t(bool general, const BwdMaps& m, const BwdParams& p, cuda
 
 template <int D, bool BF16>
 cudaError_t launch_dkdv_persistent_t(const CUtensorMap& a1, const CUtensorMap& a2, const CUtensorMap& b1,
-                                     const CUtensorMap& b2, const BwdParams& p, cudaStream_t stream) {
+                                     const CUtensorMap& b2, const BwdParams& p, cudaStream_t stream,
+                                     bool dependent) {
   using L = BwdLayout<D>;
   auto kern = fa_bwd_dkdvp_kernel<D, BF16>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
@@ -1678,22 +1707,23 @@ cudaError_t launch_dkdv_persistent_t(const CUtensorMap& a1, const CUtensorMap& a
   if (n_items <= 0) return cudaSuccess;
   if (n_items > (1LL << 30)) return cudaErrorInvalidValue;
   const int grid = static_cast<int>(n_items < bwd_sm_count() ? n_items : bwd_sm_count());
-  kern<<<grid, kBwdThreads, L::kSmemBytes, stream>>>(a1, a2, b1, b2, p, gx, static_cast<int>(n_items));
-  return cudaGetLastError();
+  return launch_kernel(kern, dim3(grid), kBwdThreads, L::kSmemBytes, stream, dependent, a1, a2, b1, b2, p, gx,
+                       static_cast<int>(n_items));
 }
 
 // The dK/dV pass: the persistent kernel for fixed-length calls at D <= 64 whose items average at
 // most 32 partner blocks (query heads per item x 64-row query blocks, halved under the causal
 // mask); the per-tile grid otherwise.
 template <int D, bool BF16>
-cudaError_t launch_dkdv_t(bool general, const BwdMaps& m, const BwdParams& p, cudaStream_t stream) {
-  if (general) return launch_main_t<D, BF16, true, true>(m.k128, m.v128, m.q64, m.do64, p, stream);
+cudaError_t launch_dkdv_t(bool general, const BwdMaps& m, const BwdParams& p, cudaStream_t stream,
+                          bool dependent) {
+  if (general) return launch_main_t<D, BF16, true, true>(m.k128, m.v128, m.q64, m.do64, p, stream, dependent);
   if constexpr (D <= 64) {
     const int64_t blocks = static_cast<int64_t>(p.group / p.kv_splits) * ((p.S + kPartnerRows - 1) / kPartnerRows);
     if ((p.causal ? blocks / 2 : blocks) <= 32)
-      return launch_dkdv_persistent_t<D, BF16>(m.k128, m.v128, m.q64, m.do64, p, stream);
+      return launch_dkdv_persistent_t<D, BF16>(m.k128, m.v128, m.q64, m.do64, p, stream, dependent);
   }
-  return launch_main_t<D, BF16, true, false>(m.k128, m.v128, m.q64, m.do64, p, stream);
+  return launch_main_t<D, BF16, true, false>(m.k128, m.v128, m.q64, m.do64, p, stream, dependent);
 }
 
 template <int D, bool BF16>
@@ -1731,8 +1761,8 @@ cudaError_t launch_bwd_preprocess(int D, bool bf16, const BwdParams& p, int64_t 
 }
 
 cudaError_t launch_bwd_dkdv(int D, bool bf16, bool general, const BwdMaps& m, const BwdParams& p,
-                            cudaStream_t stream) {
-#define FA_DKDV(DD, BB) launch_dkdv_t<DD, BB>(general, m, p, stream)
+                            cudaStream_t stream, bool dependent) {
+#define FA_DKDV(DD, BB) launch_dkdv_t<DD, BB>(general, m, p, stream, dependent)
   FA_BWD_DISPATCH(FA_DKDV)
 #undef FA_DKDV
 }

@@ -95,8 +95,11 @@ cudaError_t launch_merge_lse(int D, bool bf16, const float* o_part, const float*
                              void* o, float* lse, cudaStream_t stream);
 
 cudaError_t launch_bwd_preprocess(int D, bool bf16, const BwdParams& p, int64_t rows, cudaStream_t stream);
+// dependent: launch as a programmatic dependent launch of the kernel just
+// before it on `stream` (the persistent dQ pass that computed Delta), which
+// the dK/dV kernels wait for before they read Delta.
 cudaError_t launch_bwd_dkdv(int D, bool bf16, bool general, const BwdMaps& maps, const BwdParams& p,
-                            cudaStream_t stream);
+                            cudaStream_t stream, bool dependent);
 cudaError_t launch_bwd_dq(int D, bool bf16, bool general, const BwdMaps& maps, const BwdParams& p,
                           cudaStream_t stream);
 // True when launch_bwd_dq's kernel computes Delta itself and writes it to p.delta
