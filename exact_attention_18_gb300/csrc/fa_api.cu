@@ -391,20 +391,21 @@ fa_status bwd_impl(const void* q, const void* k, const void* v, const void* o, c
   // Delta then dK/dV then dQ; or, when the dQ kernel computes Delta, dQ then dK/dV.
   if ((st = mark(0))) return st;
   if (fused_delta) {
-    if ((st = from_cuda(fa::launch_bwd_dq(Di, bf16, general, maps, p, s), "backward dQ launch"))) return st;
+    if ((st = from_cuda(fa::launch_bwd_dq(Di, bf16, general, maps, p, s, false), "backward dQ launch"))) return st;
   } else if ((st = from_cuda(fa::launch_bwd_preprocess(Di, bf16, p, q_rows, s), "backward preprocess launch"))) {
     return st;
   }
   if ((st = mark(1))) return st;
-  // After the dQ pass, the dK/dV pass's first CTAs start as the dQ pass's last ones finish.
-  if ((st = from_cuda(fa::launch_bwd_dkdv(Di, bf16, general, maps, p, s, fused_delta), "backward dK/dV launch")))
+  // The second and third kernels are programmatic dependent launches: their
+  // first CTAs start as the previous kernel's last ones finish.
+  if ((st = from_cuda(fa::launch_bwd_dkdv(Di, bf16, general, maps, p, s, true), "backward dK/dV launch")))
     return st;
   if (splits > 1 &&
       (st = from_cuda(fa::launch_bwd_dkv_reduce(Di, bf16, p, kv_rows, s), "backward dK/dV reduce launch")))
     return st;
   if ((st = mark(2))) return st;
   if (!fused_delta &&
-      (st = from_cuda(fa::launch_bwd_dq(Di, bf16, general, maps, p, s), "backward dQ launch")))
+      (st = from_cuda(fa::launch_bwd_dq(Di, bf16, general, maps, p, s, true), "backward dQ launch")))
     return st;
   return mark(3);
 }

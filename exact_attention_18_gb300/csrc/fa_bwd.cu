@@ -95,6 +95,8 @@ __device__ __forceinline__ float row_delta(const void* o, const void* dout, int6
 
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) fa_bwd_preprocess_kernel(const BwdParams p, int64_t rows) {
+  // The dK/dV pass after it may start its CTAs; it waits for this grid before reading Delta.
+  griddep_launch_dependents();
   constexpr int kTpr = D / 8;           // threads per row
   constexpr int kRowsPerWarp = 32 / kTpr;
   const int lane = threadIdx.x & 31;
@@ -454,6 +456,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t sA2 = smem_u32(smem + L::kOffA2);
   const uint32_t sB1 = smem_u32(smem + L::kOffB1);
   const uint32_t sB2 = smem_u32(smem + L::kOffB2);
+  // The dQ pass after the dK/dV pass may start its CTAs as this grid's last
+  // ones run; it reads nothing this pass writes before its griddep_wait.
+  if constexpr (KV_OUTER) griddep_launch_dependents();
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
@@ -640,6 +645,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // dQ pass: this thread's query row owns its L2 = L * log2 e and Delta
     // (rows past S: L2 = +inf, so their probabilities are exactly 0).
     float my_l2 = INFINITY, my_delta = 0.f;
+    // Delta comes from a kernel before this one, which may still be running
+    // when this pass is a programmatic dependent launch.
+    if (!KV_OUTER) griddep_wait();
     if (!KV_OUTER && my < S) {
       const int64_t li = GENERAL ? static_cast<int64_t>(own_h) * lstride + loff + my : rowbase + my;
       my_l2 = p.lse[li] * kLog2e;
@@ -938,8 +946,11 @@ __global__ void __launch_bounds__(kDqpThreads, 1)
       const uint32_t bytes = static_cast<uint32_t>(min(128, S - w.own0)) * D * 2;
       const int64_t off = (static_cast<int64_t>(w.bh) * S + w.own0) * D * 2;
       mbar_arrive_expect_tx(bar_stage, 2 * bytes);
-      bulk_load(stage_o, static_cast<const char*>(p.o) + off, bytes, bar_stage);
-      bulk_load(stage_do, static_cast<const char*>(p.dout) + off, bytes, bar_stage);
+      // Evict-first: these lines are not read again soon (the item's dO tile
+      // comes in through its own TMA load), and K, V blocks keep their L2 place.
+      const uint64_t pol = l2_policy_evict_first();
+      bulk_load(stage_o, static_cast<const char*>(p.o) + off, bytes, bar_stage, pol);
+      bulk_load(stage_do, static_cast<const char*>(p.dout) + off, bytes, bar_stage, pol);
     };
     bool ok = true;
     int k = item_at(0);
@@ -1685,12 +1696,12 @@ cudaError_t launch_dq_persistent_t(const CUtensorMap& a1, const CUtensorMap& a2,
 // B4 H16 S4096 D64 185 -> 165 us, B1 H16 S16384 D64 547 -> 538 us); at D = 128 the per-tile
 // grid (the persistent kernel was as fast at B2 H32 S8192, 1.6 % slower at B1 H8 S32768).
 template <int D, bool BF16>
-cudaError_t launch_dq_t(bool general, const BwdMaps& m, const BwdParams& p, cudaStream_t stream) {
-  if (general) return launch_main_t<D, BF16, false, true>(m.q128, m.do128, m.k64, m.v64, p, stream);
+cudaError_t launch_dq_t(bool general, const BwdMaps& m, const BwdParams& p, cudaStream_t stream, bool dependent) {
+  if (general) return launch_main_t<D, BF16, false, true>(m.q128, m.do128, m.k64, m.v64, p, stream, dependent);
   if constexpr (D <= 64)  // the persistent kernel: bwd_dq_computes_delta(D, false)
     return launch_dq_persistent_t<D, BF16>(m.q128, m.do128, m.k64, m.v64, p, stream);
   else
-    return launch_main_t<D, BF16, false, false>(m.q128, m.do128, m.k64, m.v64, p, stream);
+    return launch_main_t<D, BF16, false, false>(m.q128, m.do128, m.k64, m.v64, p, stream, dependent);
 }
 
 template <int D, bool BF16>
@@ -1774,8 +1785,8 @@ cudaError_t launch_bwd_dkv_reduce(int D, bool bf16, const BwdParams& p, int64_t 
 }
 
 cudaError_t launch_bwd_dq(int D, bool bf16, bool general, const BwdMaps& m, const BwdParams& p,
-                          cudaStream_t stream) {
-#define FA_DQ(DD, BB) launch_dq_t<DD, BB>(general, m, p, stream)
+                          cudaStream_t stream, bool dependent) {
+#define FA_DQ(DD, BB) launch_dq_t<DD, BB>(general, m, p, stream, dependent)
   FA_BWD_DISPATCH(FA_DQ)
 #undef FA_DQ
 }

@@ -96,12 +96,15 @@ cudaError_t launch_merge_lse(int D, bool bf16, const float* o_part, const float*
 
 cudaError_t launch_bwd_preprocess(int D, bool bf16, const BwdParams& p, int64_t rows, cudaStream_t stream);
 // dependent: launch as a programmatic dependent launch of the kernel just
-// before it on `stream` (the persistent dQ pass that computed Delta), which
-// the dK/dV kernels wait for before they read Delta.
+// before it on `stream` (a backward kernel of the same call): its CTAs may
+// start while that kernel runs, and it waits for that kernel's grid before it
+// reads Delta.  Only the kernel that computes Delta (the Delta kernel, or the
+// persistent dQ pass) runs before them otherwise; the dK/dV pass (and its
+// partial-sum reduction) writes nothing the dQ pass reads.
 cudaError_t launch_bwd_dkdv(int D, bool bf16, bool general, const BwdMaps& maps, const BwdParams& p,
                             cudaStream_t stream, bool dependent);
 cudaError_t launch_bwd_dq(int D, bool bf16, bool general, const BwdMaps& maps, const BwdParams& p,
-                          cudaStream_t stream);
+                          cudaStream_t stream, bool dependent);
 // True when launch_bwd_dq's kernel computes Delta itself and writes it to p.delta
 // (the persistent dQ kernel): the backward then skips the Delta kernel and runs
 // the dQ pass before the dK/dV pass, which reads that Delta.
