@@ -99,3 +99,32 @@ def test_repeated_calls_of_the_other_paths(fa, path):
     first = call()
     for rep in range(REPEATS):
         _same(first, call(), names, rep)
+
+
+@pytest.mark.parametrize("D,dtype,path", [(64, "fp16", "fixed"), (32, "bf16", "gqa"), (128, "bf16", "fixed"),
+                                          (64, "fp16", "window")])
+def test_stale_workspace_never_reaches_the_gradients(fa, D, dtype, path):
+    """The backward's kernels overlap: each starts its CTAs while the one before it finishes,
+    and waits for it only before reading Delta, which the Delta kernel (or, at D <= 64 with
+    fixed lengths, the dQ pass) writes into the workspace during the same call.  With the
+    workspace filled with NaN before every call, a read of Delta before it is written would
+    show up as NaN in dQ, dK or dV; every call must also reproduce the first one's bits."""
+    H_kv = 4 if path == "gqa" else None
+    window = (512, 0) if path == "window" else None
+    w = Workload("stale_ws", 2, 16, 2048, D, dtype, True, backward=True, seed=93, H_kv=H_kv, window=window)
+    inp = make_inputs(w)
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+    o, lse = fa.forward(q, k, v, causal=True, scale=w.scale, window=window)
+    ws_bytes = fa.fa_bwd_gqa_workspace_size(w.B, w.H, k.shape[1], w.S, D)
+    ws = torch.empty(ws_bytes // 4, dtype=torch.float32, device="cuda")
+    first = None
+    for rep in range(REPEATS):
+        ws.fill_(float("nan"))
+        g = fa.backward(q, k, v, o, do, lse, causal=True, scale=w.scale, window=window, workspace=ws)
+        assert fa.fa_check_device_errors(None) == 0, fa.fa_last_error_detail()
+        for name, t in zip(("dQ", "dK", "dV"), g):
+            assert bool(torch.isfinite(t).all()), f"call {rep + 1}: {name} has non-finite values"
+        if first is None:
+            first = g
+        else:
+            _same(first, g, ("dQ", "dK", "dV"), rep)
