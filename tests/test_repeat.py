@@ -128,3 +128,36 @@ def test_stale_workspace_never_reaches_the_gradients(fa, D, dtype, path):
             first = g
         else:
             _same(first, g, ("dQ", "dK", "dV"), rep)
+
+
+@pytest.mark.parametrize("D,dtype", [(64, "fp16"), (128, "bf16")])
+def test_marked_backward_gives_the_same_bits(fa, D, dtype):
+    """fa_bwd_marked runs the same kernels as fa_bwd, with events recorded between them (at
+    D = 64 the dQ pass, which computes Delta, first; at D = 128 the Delta kernel first): the
+    results are bit-identical, the four events complete in order, and at D = 64 no kernel runs
+    between the last two."""
+    w = Workload("marked", 2, 8, 1024, D, dtype, True, backward=True, seed=95)
+    inp = make_inputs(w)
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+    o, lse = fa.forward(q, k, v, causal=True, scale=w.scale)
+    ref = fa.backward(q, k, v, o, do, lse, causal=True, scale=w.scale)
+    ws_bytes = fa.fa_bwd_workspace_size(w.B, w.H, w.S, D)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    got = [torch.full_like(q, float("nan")) for _ in range(3)]
+    stream = torch.cuda.current_stream()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    for e in ev:  # create the events before the library records them
+        e.record(stream)
+    dt = fa.FA_FP16 if dtype == "fp16" else fa.FA_BF16
+    st = fa.fa_bwd_marked(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
+                          got[0].data_ptr(), got[1].data_ptr(), got[2].data_ptr(), w.B, w.H, w.S, D, True, w.scale,
+                          dt, ws.data_ptr(), ws_bytes, stream.cuda_stream, [e.cuda_event for e in ev])
+    assert st == 0, fa.fa_last_error_detail()
+    torch.cuda.synchronize()
+    assert fa.fa_check_device_errors(None) == 0, fa.fa_last_error_detail()
+    _same(ref, got, ("dQ", "dK", "dV"), 0)
+    gaps = [ev[i].elapsed_time(ev[i + 1]) for i in range(3)]
+    assert all(g >= 0 for g in gaps), gaps
+    assert gaps[0] > 0 and gaps[1] > 0, gaps
+    if D == 64:
+        assert gaps[2] < 0.5 * min(gaps[0], gaps[1]), gaps
