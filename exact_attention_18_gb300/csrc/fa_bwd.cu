@@ -527,6 +527,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         cp_async_mbar_arrive(&bar_bfull[st]);
       }
     }
+    // A CTA with no partner block (a key tile past a short sample's end) still
+    // waits for the kernel before it, so that this grid never completes before
+    // that one, whatever follows on the stream.
+    if constexpr (KV_OUTER) {
+      if (it == 0) griddep_wait();
+    }
     // Teardown: every copy issued must land before the CTA exits.
     if (lane == 0) drain_wait(bar_afull, 0, p.err);
     for (int x = (it > L::kStages ? it - L::kStages : 0); x < it; ++x)
